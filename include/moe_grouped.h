@@ -1,0 +1,194 @@
+/* moe_grouped.h - C ABI of the grouped routed-expert decode for the verify window (GB300, sm_103a).
+ *
+ * The operation (from the pages of one inference engine):
+ *  - #2058 "Verify window: the routed experts' gate/up with the group's q8_1 rows in shared
+ *    memory", sections "Why" and "What changed": the window's T = 1-4 tokens are routed to top-k
+ *    experts and grouped by expert; each group's block-quantized gate/up weights are read once
+ *    and applied, as integer block dot products with fp32 block scales, to each of the group's
+ *    1-4 q8_1 activation rows.
+ *  - #363 "experts: smaller and fewer launches for the verify window's PCIe call", section "What
+ *    changes": the group count n_groups lives on the device; group-stride launches sized by
+ *    grid_groups (0 = cap_groups) make empty and near-empty calls cheap; SwiGLU and the q8_1
+ *    quantization run as one kernel over the call's own entries [grp_start[0],
+ *    grp_start[n_groups]); the SwiGLU product is rounded to fp32 on its own. Section
+ *    "Exactness": a second call's entries may start past 0, its destinations are scattered, and
+ *    rows a call does not own are never written.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers unless marked (host). The caller owns every buffer; no entry
+ *    point allocates device memory, and every launch is asynchronous on `stream` (capturable in
+ *    a CUDA graph).
+ *  - The return value is MOE_OK or a negative MOE_E_* code for errors the host can see (null
+ *    pointer, unsupported format, bad shape, bad capacity, a failed launch). Nothing is launched
+ *    when an argument error is returned.
+ *  - Errors in device-resident data (an expert id out of range, *n_groups above cap_groups,
+ *    grp_start not monotone or outside [0, cap_entries], an entry's row index out of range, a
+ *    weight pointer not 16-byte aligned, a bounded wait that gave up) are reported by OR-ing
+ *    MOE_ERR_* bits into *err when err is not NULL; the offending group or entry is skipped (its
+ *    rows are not written), *n_groups is clamped to cap_groups. Kernels never trap and never wait
+ *    without a time limit.
+ *  - Shapes: n_embd and n_ff are multiples of 256.
+ *
+ * Weight formats (this library's own byte layouts; the pages name real formats but print none).
+ * Little-endian, fp16 fields are IEEE binary16. A row of K weights is K/32 blocks (K/256
+ * super-blocks for CB2/CB3) packed without padding:
+ *   MOE_Q8_0 (34 B / 32 w) : u16 d, i8 q[32]                         w = d*q
+ *   MOE_Q4B  (20 B / 32 w) : u16 d, u16 m, u8 qs[16]                 w = d*code + m
+ *   MOE_NL4  (18 B / 32 w) : u16 d, u8 qs[16]                        w = d*table[code]
+ *        code j = qs[j] & 15 for j < 16, qs[j-16] >> 4 for j >= 16; table = 16 int8 (codebook)
+ *   MOE_CB2  (70 B / 256 w): u16 D, u8 idx[32], u8 sign[32], u8 sub[4]
+ *        weight n: +-grid[idx[n/8]][n%8], bit n%8 of sign[n/8] negates; grid = 256x8 int8
+ *   MOE_CB3  (102 B / 256 w): u16 D, u8 idx[64], u8 sign[32], u8 sub[4]
+ *        weight n: +-grid[idx[n/4]][n%4], bit n%8 of sign[n/8] negates; grid = 256x4 int8
+ *   CB sub-block j (32 weights): ls = 2*((sub[j/2] >> 4*(j%2)) & 15) + 1, w = D*ls*(+-grid).
+ *   CB grids must hold odd values only (the kernels rely on it; an even entry sets
+ *   MOE_ERR_CODEBOOK).
+ * Gate/up blob of an expert: n_ff gate rows then n_ff up rows, each of n_embd weights.
+ * Down blob of an expert: n_embd rows of n_ff weights. Blob pointers must be 16-byte aligned.
+ *
+ * q8_1 activation block (36 B per 32 values): fp16 d = amax/127, fp16 s = d * sum(q),
+ * int8 q[32] = round-half-away-from-zero(x/d) (an all-zero block has d = s = 0, q = 0).
+ */
+#ifndef MOE_GROUPED_H
+#define MOE_GROUPED_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- weight formats */
+#define MOE_Q8_0 1
+#define MOE_Q4B 2
+#define MOE_NL4 3
+#define MOE_CB2 4
+#define MOE_CB3 5
+
+/* ---- host-visible status codes */
+#define MOE_OK 0
+#define MOE_E_NULL (-1)  /* a required pointer is NULL */
+#define MOE_E_TYPE (-2)  /* unsupported weight format, or a codebook missing for NL4/CB2/CB3 */
+#define MOE_E_SHAPE (-3) /* n_embd / n_ff not a positive multiple of 256, bad rows/cols/T/k */
+#define MOE_E_CAP (-4)   /* cap_groups / cap_entries / n_experts not positive, or too large */
+#define MOE_E_CUDA (-5)  /* a CUDA runtime call failed (launch, attribute, device query) */
+#define MOE_E_ALIGN (-6) /* a host-checkable pointer is not suitably aligned */
+
+/* ---- device-side error bits, OR-ed into *err */
+#define MOE_ERR_NGROUPS 1   /* *n_groups < 0 or > cap_groups (clamped) */
+#define MOE_ERR_EXPERT 2    /* a group's expert id outside [0, n_experts) (group skipped) */
+#define MOE_ERR_START 4     /* grp_start not monotone or outside [0, cap_entries] (group skipped) */
+#define MOE_ERR_ENTRY 8     /* an entry's source or destination row out of range (entry skipped) */
+#define MOE_ERR_ALIGN 16    /* an expert's weight pointer not 16-byte aligned (group skipped) */
+#define MOE_ERR_CODEBOOK 32 /* a CB grid value is even (results of that call are unspecified) */
+#define MOE_ERR_TIMEOUT 64  /* a bounded wait on a staged weight tile gave up */
+#define MOE_ERR_ROUTE 128   /* a routed expert id outside [0, n_experts) (entry dropped) */
+
+/* One q8_1 block (36 bytes). d and s are IEEE binary16 bit patterns. */
+typedef struct moe_q8_1 {
+    uint16_t d;
+    uint16_t s;
+    int8_t q[32];
+} moe_q8_1;
+
+/* A weight format: type = MOE_*; codebook = device pointer to the NL4 table (16 int8), the
+ * CB2 grid (256x8 int8) or the CB3 grid (256x4 int8); NULL for Q8_0 and Q4B. */
+typedef struct moe_wfmt {
+    int32_t type;
+    const int8_t* codebook;
+} moe_wfmt;
+
+/* Bytes of one row of K weights in format `type` (0 if K is not valid for it). Host only. */
+int64_t moe_row_bytes(int type, int K);
+
+/* Text for a status code or for a set of MOE_ERR_* bits (static storage). Host only. */
+const char* moe_strerror(int status);
+
+/* q8_1 quantization of activations (a1 in the step list; the quantizer of #363 "What changes").
+ * x: fp32 [rows][cols], row-major; xq: [rows][cols/32] blocks. cols % 32 == 0. */
+int moe_quantize_q8_1(const float* x, int64_t rows, int64_t cols, moe_q8_1* xq,
+                      cudaStream_t stream);
+
+/* Routing/grouping of a window (the groups that #363 "What changes" passes to the calls).
+ * topk_ids: int32 [T][k] expert ids (distinct per token). Groups are ordered by ascending expert
+ * id; entries of a group by ascending (t, slot). Entries are numbered from entry_base.
+ * Outputs: grp_expert[G], grp_start[G+1] (grp_start[G] = entry_base + valid entries),
+ * *n_groups = G, and for every produced entry e: ent_src[e] = t (row of the q8_1 activations),
+ * ent_dst[e] = t*k + slot (destination row). Ids outside [0, n_experts) are dropped and set
+ * MOE_ERR_ROUTE. Arrays indexed by e must hold entry_base + T*k elements; grp_expert T*k and
+ * grp_start T*k + 1. T*k <= 1024. */
+int moe_route_group(const int32_t* topk_ids, int T, int k, int n_experts, int entry_base,
+                    int32_t* grp_expert, int32_t* grp_start, int32_t* n_groups,
+                    int32_t* ent_src, int32_t* ent_dst, int32_t* err, cudaStream_t stream);
+
+/* Grouped gate/up (a2). For each group g < *n_groups with expert x = grp_expert[g] and each
+ * entry e in [grp_start[g], grp_start[g+1]): gu[e][r] = sum over 32-blocks b of the block
+ * contribution of row r of w_gu[x] against xq[ent_src[e]] block b, for r < 2*n_ff (gate rows
+ * then up rows). Block contributions: Q8_0/NL4 d_w*d_x*isum; Q4B d_w*d_x*isum + m_w*s_x;
+ * CB2/CB3 D*d_x*(ls*isum) per 32-weight sub-block; isum = exact integer sum of w_code*q.
+ * w_gu: device array of n_experts device pointers (host-written table). xq: [n_xq_rows][n_embd/32].
+ * gu: fp32 [cap_entries][2*n_ff]; only the rows of this call's entries are written.
+ * grid_groups: 0 = cap_groups, > cap_groups is treated as cap_groups; it sizes the launch only,
+ * results do not depend on it. */
+int moe_grouped_gu(moe_wfmt fmt, int n_embd, int n_ff, const void* const* w_gu, int n_experts,
+                   const int32_t* grp_expert, const int32_t* grp_start, const int32_t* n_groups,
+                   int cap_groups, int grid_groups, const moe_q8_1* xq, int n_xq_rows,
+                   const int32_t* ent_src, int cap_entries, float* gu, int32_t* err,
+                   cudaStream_t stream);
+
+/* Fused SwiGLU + q8_1 (a3, #363 "What changes"). For e in [grp_start[0], grp_start[*n_groups])
+ * and j < n_ff: h = fp32(silu(gu[e][j]) * gu[e][n_ff+j]), silu(g) = g / (1 + exp(-g)) in fp32,
+ * then q8_1 of each 32 consecutive h into hq[e][j/32]. hq: [cap_entries][n_ff/32]. */
+int moe_swiglu_q8_1(const float* gu, int n_ff, const int32_t* grp_start, const int32_t* n_groups,
+                    int cap_groups, int cap_entries, moe_q8_1* hq, int32_t* err,
+                    cudaStream_t stream);
+
+/* Grouped down (a4). For each group and entry e: out[ent_dst[e]][n] = sum over blocks of row n
+ * of w_down[x] against hq[e], for n < n_embd. out: fp32 with out_rows rows of stride
+ * out_row_stride floats (>= n_embd); rows not named by this call's entries are not written. */
+int moe_grouped_down(moe_wfmt fmt, int n_embd, int n_ff, const void* const* w_down,
+                     int n_experts, const int32_t* grp_expert, const int32_t* grp_start,
+                     const int32_t* n_groups, int cap_groups, int grid_groups,
+                     const moe_q8_1* hq, int cap_entries, const int32_t* ent_dst, float* out,
+                     int64_t out_rows, int64_t out_row_stride, int32_t* err,
+                     cudaStream_t stream);
+
+/* Flags for moe_expert_call.flags */
+#define MOE_F_PDL 1 /* chain the three kernels with programmatic dependent launch */
+
+/* One native_expert_grouped-style call (#363): gate/up, SwiGLU + q8_1, down on one stream. */
+typedef struct moe_expert_call {
+    moe_wfmt gu_fmt, down_fmt;
+    int32_t n_embd, n_ff, n_experts;
+    const void* const* w_gu;   /* [n_experts] device pointers to gate/up blobs */
+    const void* const* w_down; /* [n_experts] device pointers to down blobs */
+    const int32_t* grp_expert; /* [cap_groups] */
+    const int32_t* grp_start;  /* [cap_groups + 1] */
+    const int32_t* n_groups;   /* device scalar */
+    int32_t cap_groups, grid_groups, cap_entries;
+    const moe_q8_1* xq;        /* [n_xq_rows][n_embd/32] */
+    int32_t n_xq_rows;
+    const int32_t* ent_src;    /* [cap_entries] */
+    const int32_t* ent_dst;    /* [cap_entries] */
+    float* gu;                 /* scratch [cap_entries][2*n_ff] */
+    moe_q8_1* hq;              /* scratch [cap_entries][n_ff/32] */
+    float* out;                /* [out_rows][out_row_stride] */
+    int64_t out_rows, out_row_stride;
+    int32_t* err;              /* optional */
+    int32_t flags;             /* MOE_F_* */
+} moe_expert_call;
+
+int moe_expert_grouped(const moe_expert_call* call, cudaStream_t stream);
+
+/* Test hook: the per-32-block integer sums of `rows` consecutive rows of one blob (row bytes
+ * apart) against one q8_1 row xq[K/32], computed by the same device decode and dot-product
+ * code as the grouped kernels: isum[r][b] = sum_i w_code_i * q_i (exact int32). */
+int moe_test_block_isum(moe_wfmt fmt, int K, const void* blob, int rows, const moe_q8_1* xq,
+                        int32_t* isum, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GROUPED_H */

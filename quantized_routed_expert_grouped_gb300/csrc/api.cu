@@ -1,0 +1,332 @@
+// api.cu - the C ABI (moe_grouped.h): host-side argument checks, launch planning and launches.
+// Every function validates what the host can see, plans the launch geometry from the shapes
+// and the device's SM count, and enqueues kernels on the caller's stream. Nothing here reads
+// device memory or allocates.
+#include <cstdio>
+#include <mutex>
+
+#include "internal.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr int kSmemBudget = 227 * 1024;
+
+bool cb_type(int t) { return t == MOE_CB2 || t == MOE_CB3; }
+bool valid_type(int t) { return t >= MOE_Q8_0 && t <= MOE_CB3; }
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    static std::mutex mu;
+    static int cache[64] = {0};
+    std::lock_guard<std::mutex> g(mu);
+    if (dev < 64 && cache[dev]) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+int check_fmt(const moe_wfmt& f) {
+    if (!valid_type(f.type)) return MOE_E_TYPE;
+    if ((f.type == MOE_NL4 || cb_type(f.type)) && f.codebook == nullptr) return MOE_E_TYPE;
+    return MOE_OK;
+}
+
+int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+// Launch geometry and shared-memory layout of one grouped GEMV (K weights per row, `rows`
+// rows per expert), filled into `a` and `p`.
+int plan_gemv(int type, int K, int rows, GemvArgs& a, GemvPlan& p) {
+    const int nch = K / 256;
+    const int64_t rb = moe_row_bytes(type, K);
+    if (nch <= 0 || rb <= 0 || rows <= 0 || rows % 8) return MOE_E_SHAPE;
+    const int R = cb_type(type) ? 2 : 1;
+    const int maxt = cb_type(type) ? 384 : 512;
+    const int nb = K / 32, nbp = nb + nb / 8;
+    // fixed part of shared memory (everything but the staging ring)
+    auto fixed_bytes = [&](int RT) {
+        int f = cb_type(type) ? 32768 : 0;                     // codebook replicas
+        f += round_up(4 * 2 * nbp * 16, 128);                  // staged activation codes
+        f += round_up(4 * nb * 4, 128) * 2;                    // fp32 scales + aux
+        f += round_up(nch * 4 * RT * 4, 128);                  // partial sums
+        f += 128 + 128;                                        // barriers + misc
+        return f;
+    };
+    for (int QR : {32, 16, 8}) {
+        const int NT = round_up(nch * QR, 32);
+        const int RT = QR * R;
+        const int64_t tile = static_cast<int64_t>(RT) * rb;
+        if (NT > maxt || tile > 72 * 1024) continue;
+        const int stage_bytes = round_up(static_cast<int>(tile) + 16, 128);
+        const int fixed = fixed_bytes(RT);
+        int stages = (kSmemBudget - fixed) / stage_bytes;
+        if (stages > 4) stages = 4;
+        if (stages < 2) continue;
+        p.R = R;
+        p.QR = QR;
+        p.RT = RT;
+        p.NT = NT;
+        p.stages = stages;
+        p.stage_bytes = stage_bytes;
+        // layout: ring | codebook | act codes | dx | aux | partials | barriers | misc
+        int off = stages * stage_bytes;
+        a.off_cb = off;
+        off += cb_type(type) ? 32768 : 0;
+        a.off_actq = off;
+        off += round_up(4 * 2 * nbp * 16, 128);
+        a.off_dx = off;
+        off += round_up(4 * nb * 4, 128);
+        a.off_aux = off;
+        off += round_up(4 * nb * 4, 128);
+        a.off_part = off;
+        off += round_up(nch * 4 * RT * 4, 128);
+        a.off_bar = off;
+        off += 128;
+        a.off_misc = off;
+        off += 128;
+        p.smem = off;
+        a.K = K;
+        a.rows = rows;
+        a.row_bytes = static_cast<int>(rb);
+        a.nch = nch;
+        a.QR = QR;
+        a.RT = RT;
+        a.stages = stages;
+        a.stage_bytes = stage_bytes;
+        a.nb = nb;
+        a.nbp = nbp;
+        return MOE_OK;
+    }
+    return MOE_E_SHAPE;
+}
+
+cudaError_t occupancy(int type, int NT, int smem, int* ctas) {
+    switch (type) {
+    case MOE_Q8_0: return gemv_occupancy_q8_0(NT, smem, ctas);
+    case MOE_Q4B: return gemv_occupancy_q4b(NT, smem, ctas);
+    case MOE_NL4: return gemv_occupancy_nl4(NT, smem, ctas);
+    case MOE_CB2: return gemv_occupancy_cb2(NT, smem, ctas);
+    default: return gemv_occupancy_cb3(NT, smem, ctas);
+    }
+}
+
+cudaError_t launch_gemv(int type, const GemvArgs& a, int grid, int NT, int smem, cudaStream_t s, bool pdl) {
+    switch (type) {
+    case MOE_Q8_0: return launch_gemv_q8_0(a, grid, NT, smem, s, pdl);
+    case MOE_Q4B: return launch_gemv_q4b(a, grid, NT, smem, s, pdl);
+    case MOE_NL4: return launch_gemv_nl4(a, grid, NT, smem, s, pdl);
+    case MOE_CB2: return launch_gemv_cb2(a, grid, NT, smem, s, pdl);
+    default: return launch_gemv_cb3(a, grid, NT, smem, s, pdl);
+    }
+}
+
+// Persistent grid: every SM's resident CTAs, but no more than grid_groups x tiles per group.
+int run_gemv(int type, GemvArgs& a, int grid_groups, cudaStream_t s, bool pdl) {
+    GemvPlan p;
+    int rc = plan_gemv(type, a.K, a.rows, a, p);
+    if (rc != MOE_OK) return rc;
+    int ctas = 0;
+    if (occupancy(type, p.NT, p.smem, &ctas) != cudaSuccess || ctas < 1) return MOE_E_CUDA;
+    const int sms = sm_count();
+    if (sms <= 0) return MOE_E_CUDA;
+    const int gg = grid_groups <= 0 || grid_groups > a.cap_groups ? a.cap_groups : grid_groups;
+    const int64_t tiles = (a.rows + p.RT - 1) / p.RT;
+    int64_t grid = static_cast<int64_t>(gg) * tiles;
+    if (grid > static_cast<int64_t>(sms) * ctas) grid = static_cast<int64_t>(sms) * ctas;
+    if (grid < 1) grid = 1;
+    if (launch_gemv(type, a, static_cast<int>(grid), p.NT, p.smem, s, pdl) != cudaSuccess) return MOE_E_CUDA;
+    return MOE_OK;
+}
+
+int check_dims(int n_embd, int n_ff) {
+    if (n_embd <= 0 || n_ff <= 0 || n_embd % 256 || n_ff % 256) return MOE_E_SHAPE;
+    return MOE_OK;
+}
+
+int gu_impl(moe_wfmt fmt, int n_embd, int n_ff, const void* const* w_gu, int n_experts, const int32_t* grp_expert,
+            const int32_t* grp_start, const int32_t* n_groups, int cap_groups, int grid_groups, const moe_q8_1* xq,
+            int n_xq_rows, const int32_t* ent_src, int cap_entries, float* gu, int32_t* err, cudaStream_t stream,
+            bool pdl) {
+    int rc = check_fmt(fmt);
+    if (rc) return rc;
+    if ((rc = check_dims(n_embd, n_ff))) return rc;
+    if (!w_gu || !grp_expert || !grp_start || !n_groups || !xq || !ent_src || !gu) return MOE_E_NULL;
+    if (n_experts <= 0 || cap_groups <= 0 || cap_entries <= 0 || n_xq_rows <= 0) return MOE_E_CAP;
+    GemvArgs a = {};
+    a.w = w_gu;
+    a.n_experts = n_experts;
+    a.K = n_embd;
+    a.rows = 2 * n_ff;
+    a.grp_expert = grp_expert;
+    a.grp_start = grp_start;
+    a.n_groups = n_groups;
+    a.cap_groups = cap_groups;
+    a.cap_entries = cap_entries;
+    a.act = xq;
+    a.n_act_rows = n_xq_rows;
+    a.ent_in = ent_src;
+    a.ent_out = nullptr;
+    a.out = gu;
+    a.out_rows = cap_entries;
+    a.out_stride = 2 * static_cast<int64_t>(n_ff);
+    a.err = err;
+    a.codebook = fmt.codebook;
+    a.prefetch_before_wait = 0;
+    return run_gemv(fmt.type, a, grid_groups, stream, pdl);
+}
+
+int down_impl(moe_wfmt fmt, int n_embd, int n_ff, const void* const* w_down, int n_experts,
+              const int32_t* grp_expert, const int32_t* grp_start, const int32_t* n_groups, int cap_groups,
+              int grid_groups, const moe_q8_1* hq, int cap_entries, const int32_t* ent_dst, float* out,
+              int64_t out_rows, int64_t out_row_stride, int32_t* err, cudaStream_t stream, bool pdl,
+              bool prefetch_before_wait) {
+    int rc = check_fmt(fmt);
+    if (rc) return rc;
+    if ((rc = check_dims(n_embd, n_ff))) return rc;
+    if (!w_down || !grp_expert || !grp_start || !n_groups || !hq || !ent_dst || !out) return MOE_E_NULL;
+    if (n_experts <= 0 || cap_groups <= 0 || cap_entries <= 0 || out_rows <= 0) return MOE_E_CAP;
+    if (out_row_stride < n_embd) return MOE_E_SHAPE;
+    GemvArgs a = {};
+    a.w = w_down;
+    a.n_experts = n_experts;
+    a.K = n_ff;
+    a.rows = n_embd;
+    a.grp_expert = grp_expert;
+    a.grp_start = grp_start;
+    a.n_groups = n_groups;
+    a.cap_groups = cap_groups;
+    a.cap_entries = cap_entries;
+    a.act = hq;
+    a.n_act_rows = cap_entries;
+    a.ent_in = nullptr;
+    a.ent_out = ent_dst;
+    a.out = out;
+    a.out_rows = out_rows;
+    a.out_stride = out_row_stride;
+    a.err = err;
+    a.codebook = fmt.codebook;
+    a.prefetch_before_wait = prefetch_before_wait ? 1 : 0;
+    return run_gemv(fmt.type, a, grid_groups, stream, pdl);
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t moe_row_bytes(int type, int K) {
+    if (K <= 0 || K % 32) return 0;
+    switch (type) {
+    case MOE_Q8_0: return static_cast<int64_t>(K / 32) * 34;
+    case MOE_Q4B: return static_cast<int64_t>(K / 32) * 20;
+    case MOE_NL4: return static_cast<int64_t>(K / 32) * 18;
+    case MOE_CB2: return K % 256 ? 0 : static_cast<int64_t>(K / 256) * 70;
+    case MOE_CB3: return K % 256 ? 0 : static_cast<int64_t>(K / 256) * 102;
+    }
+    return 0;
+}
+
+const char* moe_strerror(int status) {
+    switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_E_NULL: return "a required pointer is NULL";
+    case MOE_E_TYPE: return "unsupported weight format or missing codebook";
+    case MOE_E_SHAPE: return "unsupported shape (n_embd and n_ff must be positive multiples of 256)";
+    case MOE_E_CAP: return "capacity or count not positive or too large";
+    case MOE_E_CUDA: return "a CUDA runtime call failed";
+    case MOE_E_ALIGN: return "pointer not suitably aligned";
+    }
+    return "unknown status";
+}
+
+int moe_quantize_q8_1(const float* x, int64_t rows, int64_t cols, moe_q8_1* xq, cudaStream_t stream) {
+    if (!x || !xq) return MOE_E_NULL;
+    if (rows < 0 || cols <= 0 || cols % 32) return MOE_E_SHAPE;
+    return launch_quantize_q8_1(x, rows, cols, xq, stream, false) == cudaSuccess ? MOE_OK : MOE_E_CUDA;
+}
+
+int moe_route_group(const int32_t* topk_ids, int T, int k, int n_experts, int entry_base, int32_t* grp_expert,
+                    int32_t* grp_start, int32_t* n_groups, int32_t* ent_src, int32_t* ent_dst, int32_t* err,
+                    cudaStream_t stream) {
+    if (!topk_ids || !grp_expert || !grp_start || !n_groups || !ent_src || !ent_dst) return MOE_E_NULL;
+    if (T <= 0 || k <= 0 || T * k > 1024) return MOE_E_SHAPE;
+    if (n_experts <= 0 || entry_base < 0) return MOE_E_CAP;
+    return launch_route_group(topk_ids, T, k, n_experts, entry_base, grp_expert, grp_start, n_groups, ent_src,
+                              ent_dst, err, stream) == cudaSuccess
+               ? MOE_OK
+               : MOE_E_CUDA;
+}
+
+int moe_grouped_gu(moe_wfmt fmt, int n_embd, int n_ff, const void* const* w_gu, int n_experts,
+                   const int32_t* grp_expert, const int32_t* grp_start, const int32_t* n_groups, int cap_groups,
+                   int grid_groups, const moe_q8_1* xq, int n_xq_rows, const int32_t* ent_src, int cap_entries,
+                   float* gu, int32_t* err, cudaStream_t stream) {
+    return gu_impl(fmt, n_embd, n_ff, w_gu, n_experts, grp_expert, grp_start, n_groups, cap_groups, grid_groups, xq,
+                   n_xq_rows, ent_src, cap_entries, gu, err, stream, false);
+}
+
+int moe_swiglu_q8_1(const float* gu, int n_ff, const int32_t* grp_start, const int32_t* n_groups, int cap_groups,
+                    int cap_entries, moe_q8_1* hq, int32_t* err, cudaStream_t stream) {
+    if (!gu || !grp_start || !n_groups || !hq) return MOE_E_NULL;
+    if (n_ff <= 0 || n_ff % 32) return MOE_E_SHAPE;
+    if (cap_groups <= 0 || cap_entries <= 0) return MOE_E_CAP;
+    return launch_swiglu_q8_1(gu, n_ff, grp_start, n_groups, cap_groups, cap_entries, hq, err, stream, false) ==
+                   cudaSuccess
+               ? MOE_OK
+               : MOE_E_CUDA;
+}
+
+int moe_grouped_down(moe_wfmt fmt, int n_embd, int n_ff, const void* const* w_down, int n_experts,
+                     const int32_t* grp_expert, const int32_t* grp_start, const int32_t* n_groups, int cap_groups,
+                     int grid_groups, const moe_q8_1* hq, int cap_entries, const int32_t* ent_dst, float* out,
+                     int64_t out_rows, int64_t out_row_stride, int32_t* err, cudaStream_t stream) {
+    return down_impl(fmt, n_embd, n_ff, w_down, n_experts, grp_expert, grp_start, n_groups, cap_groups, grid_groups,
+                     hq, cap_entries, ent_dst, out, out_rows, out_row_stride, err, stream, false, false);
+}
+
+int moe_expert_grouped(const moe_expert_call* c, cudaStream_t stream) {
+    if (!c) return MOE_E_NULL;
+    int rc;
+    if ((rc = check_fmt(c->gu_fmt)) || (rc = check_fmt(c->down_fmt))) return rc;
+    if ((rc = check_dims(c->n_embd, c->n_ff))) return rc;
+    if (!c->w_gu || !c->w_down || !c->grp_expert || !c->grp_start || !c->n_groups || !c->xq || !c->ent_src ||
+        !c->ent_dst || !c->gu || !c->hq || !c->out)
+        return MOE_E_NULL;
+    if (c->n_experts <= 0 || c->cap_groups <= 0 || c->cap_entries <= 0 || c->n_xq_rows <= 0 || c->out_rows <= 0)
+        return MOE_E_CAP;
+    if (c->out_row_stride < c->n_embd) return MOE_E_SHAPE;
+    const bool pdl = (c->flags & MOE_F_PDL) != 0;
+    rc = gu_impl(c->gu_fmt, c->n_embd, c->n_ff, c->w_gu, c->n_experts, c->grp_expert, c->grp_start, c->n_groups,
+                 c->cap_groups, c->grid_groups, c->xq, c->n_xq_rows, c->ent_src, c->cap_entries, c->gu, c->err, stream,
+                 pdl);
+    if (rc) return rc;
+    if (launch_swiglu_q8_1(c->gu, c->n_ff, c->grp_start, c->n_groups, c->cap_groups, c->cap_entries, c->hq, c->err,
+                           stream, pdl) != cudaSuccess)
+        return MOE_E_CUDA;
+    // the down kernel's weights and groups are inputs of this call (complete before its gate/up
+    // ran), so under PDL it may start streaming weight tiles before its dependency wait
+    return down_impl(c->down_fmt, c->n_embd, c->n_ff, c->w_down, c->n_experts, c->grp_expert, c->grp_start,
+                     c->n_groups, c->cap_groups, c->grid_groups, c->hq, c->cap_entries, c->ent_dst, c->out,
+                     c->out_rows, c->out_row_stride, c->err, stream, pdl, pdl);
+}
+
+int moe_test_block_isum(moe_wfmt fmt, int K, const void* blob, int rows, const moe_q8_1* xq, int32_t* isum,
+                        cudaStream_t stream) {
+    int rc = check_fmt(fmt);
+    if (rc) return rc;
+    if (!blob || !xq || !isum) return MOE_E_NULL;
+    if (K <= 0 || K % 256 || rows <= 0) return MOE_E_SHAPE;
+    cudaError_t e;
+    switch (fmt.type) {
+    case MOE_Q8_0: e = launch_isum_q8_0(fmt.codebook, K, blob, rows, xq, isum, stream); break;
+    case MOE_Q4B: e = launch_isum_q4b(fmt.codebook, K, blob, rows, xq, isum, stream); break;
+    case MOE_NL4: e = launch_isum_nl4(fmt.codebook, K, blob, rows, xq, isum, stream); break;
+    case MOE_CB2: e = launch_isum_cb2(fmt.codebook, K, blob, rows, xq, isum, stream); break;
+    default: e = launch_isum_cb3(fmt.codebook, K, blob, rows, xq, isum, stream); break;
+    }
+    return e == cudaSuccess ? MOE_OK : MOE_E_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,89 @@
+// internal.h - launchers and launch geometry shared by the C-ABI layer and the kernel files.
+// Internal header (not part of the C ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "moe_grouped.h"
+
+namespace moe {
+
+// Launch `kern` with an optional programmatic-dependent-launch edge to the previous work on the
+// stream (the kernel itself calls griddepcontrol.wait before reading dependent data).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          bool pdl, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// Arguments of one grouped GEMV launch (gate/up or down).
+struct GemvArgs {
+    const void* const* w;  // [n_experts] blob pointers
+    int n_experts;
+    int K;          // weights per row
+    int rows;       // rows per expert
+    int row_bytes;  // bytes per row
+    int nch;        // 256-weight chunks per row
+    int QR;         // row groups per tile (threads per chunk column)
+    int RT;         // maximum rows per tile (QR * rows per thread)
+    int stages;     // staging ring depth
+    int stage_bytes;  // bytes per ring slot (tile + slack, multiple of 128)
+    const int32_t* grp_expert;
+    const int32_t* grp_start;
+    const int32_t* n_groups;
+    int cap_groups;
+    int cap_entries;
+    const moe_q8_1* act;  // activation rows
+    int n_act_rows;
+    const int32_t* ent_in;   // entry -> activation row (nullptr: the entry itself)
+    const int32_t* ent_out;  // entry -> output row (nullptr: the entry itself)
+    float* out;
+    int64_t out_rows;
+    int64_t out_stride;
+    int32_t* err;
+    const int8_t* codebook;
+    int prefetch_before_wait;  // weight tiles may be requested before griddepcontrol.wait
+    // dynamic shared-memory layout (byte offsets)
+    int off_bar, off_actq, off_dx, off_aux, off_part, off_cb, off_misc;
+    int nb;   // activation blocks per row (K/32)
+    int nbp;  // padded block slots per activation half-row
+};
+
+struct GemvPlan {
+    int R, QR, RT, NT, stages, stage_bytes, smem, ctas_per_sm;
+};
+
+cudaError_t launch_quantize_q8_1(const float* x, int64_t rows, int64_t cols, moe_q8_1* xq, cudaStream_t s,
+                                 bool pdl);
+cudaError_t launch_swiglu_q8_1(const float* gu, int n_ff, const int32_t* grp_start, const int32_t* n_groups,
+                               int cap_groups, int cap_entries, moe_q8_1* hq, int32_t* err, cudaStream_t s,
+                               bool pdl);
+cudaError_t launch_route_group(const int32_t* topk_ids, int T, int k, int n_experts, int entry_base,
+                               int32_t* grp_expert, int32_t* grp_start, int32_t* n_groups, int32_t* ent_src,
+                               int32_t* ent_dst, int32_t* err, cudaStream_t s);
+
+// Per-format grouped GEMV and test-hook launchers (one translation unit per format).
+#define MOE_DECLARE_FORMAT(NAME)                                                                       \
+    cudaError_t launch_gemv_##NAME(const GemvArgs& a, int grid, int NT, int smem, cudaStream_t s, bool pdl); \
+    cudaError_t gemv_occupancy_##NAME(int NT, int smem, int* ctas);                                     \
+    cudaError_t launch_isum_##NAME(const int8_t* codebook, int K, const void* blob, int rows,           \
+                                   const moe_q8_1* xq, int32_t* isum, cudaStream_t s);
+MOE_DECLARE_FORMAT(q8_0)
+MOE_DECLARE_FORMAT(q4b)
+MOE_DECLARE_FORMAT(nl4)
+MOE_DECLARE_FORMAT(cb2)
+MOE_DECLARE_FORMAT(cb3)
+#undef MOE_DECLARE_FORMAT
+
+}  // namespace moe

@@ -1,0 +1,68 @@
+"""The C-ABI library on the CPU: it loads, exports every entry point the headers declare, and
+rejects bad host-visible arguments before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def m():
+    from quantized_routed_expert_grouped_gb300 import build
+    build.build()
+    import quantized_routed_expert_grouped_gb300 as mod
+    mod.lib()
+    return mod
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"^\s*(?:int|int64_t|const char\*)\s+(moe_\w+)\s*\(", src, re.M))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(m):
+    names = _declared()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(m.lib(), n), n
+
+
+def test_row_bytes_and_strerror(m):
+    assert m.row_bytes(m.CB3, 2560) == 1020 and m.row_bytes(m.CB2, 2560) == 700
+    assert m.row_bytes(m.NL4, 768) == 432 and m.row_bytes(m.Q8_0, 512) == 544 and m.row_bytes(m.Q4B, 4096) == 2560
+    assert m.row_bytes(m.CB3, 100) == 0 and m.row_bytes(99, 256) == 0
+    assert "shape" in m.strerror(-3)
+
+
+def test_host_argument_errors(m):
+    L = m.lib()
+    W = m.WFmt
+    dummy = ctypes.c_void_p(16)
+    # unsupported type, missing codebook, bad shape, NULL pointers, bad capacities
+    assert L.moe_grouped_gu(W(9, None), 2560, 768, dummy, 1, dummy, dummy, dummy, 1, 0, dummy, 1, dummy, 1, dummy,
+                            None, None) == -2
+    assert L.moe_grouped_gu(W(5, None), 2560, 768, dummy, 1, dummy, dummy, dummy, 1, 0, dummy, 1, dummy, 1, dummy,
+                            None, None) == -2
+    assert L.moe_grouped_gu(W(1, None), 2500, 768, dummy, 1, dummy, dummy, dummy, 1, 0, dummy, 1, dummy, 1, dummy,
+                            None, None) == -3
+    assert L.moe_grouped_gu(W(1, None), 2560, 768, None, 1, dummy, dummy, dummy, 1, 0, dummy, 1, dummy, 1, dummy,
+                            None, None) == -1
+    assert L.moe_grouped_gu(W(1, None), 2560, 768, dummy, 0, dummy, dummy, dummy, 1, 0, dummy, 1, dummy, 1, dummy,
+                            None, None) == -4
+    assert L.moe_grouped_down(W(3, None), 2560, 768, dummy, 1, dummy, dummy, dummy, 1, 0, dummy, 1, dummy, dummy,
+                              4, 2560, None, None) == -2
+    assert L.moe_grouped_down(W(1, None), 2560, 768, dummy, 1, dummy, dummy, dummy, 1, 0, dummy, 1, dummy, dummy,
+                              4, 100, None, None) == -3
+    assert L.moe_swiglu_q8_1(dummy, 100, dummy, dummy, 1, 1, dummy, None, None) == -3
+    assert L.moe_quantize_q8_1(None, 1, 32, dummy, None) == -1
+    assert L.moe_quantize_q8_1(dummy, 1, 33, dummy, None) == -3
+    assert L.moe_route_group(dummy, 40, 32, 8, 0, dummy, dummy, dummy, dummy, dummy, None, None) == -3
+    assert L.moe_expert_grouped(None, None) == -1
+    assert L.moe_test_block_isum(W(1, None), 300, dummy, 1, dummy, dummy, None) == -3
