@@ -1,0 +1,441 @@
+"""Benchmark: the verify window's grouped routed-expert decode, 48 layers in one CUDA graph.
+
+Workload (the decode-window configuration): 48 layers, each with its own 128 experts, top-8
+routing, n_embd 2560, n_ff 768, CB3 gate/up and NL4 down weights (16.4 GB resident pool, seeded
+synthetic bytes), window sizes T = 1, 2, 3, 4. Per layer the graph runs the whole hot path:
+routing/grouping, activation q8_1, grouped gate/up, fused SwiGLU + q8_1, grouped down, chained
+with programmatic dependent launch; every kernel waits for the previous layer before reading.
+
+One step = one launch of each of the four window graphs (T = 1..4). value = mean microseconds
+per window over the four T (lower is better); per-T microseconds and weight-stream bandwidth are
+in "per_T". Every window reads >= 1 GB of weights, far more than L2 (129 MB), so no flush is
+needed between launches.
+
+--impl reference times the CPU oracle instead (bounded sample: one layer per T per step,
+scaled to a 48-layer window).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WL = synth.WORKLOADS["window48"]
+GU_T, DN_T = WL.pairs[0]
+TS = (1, 2, 3, 4)
+METRIC = "us_per_verify_window_48L"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def routing_for(layer, T):
+    return synth.routing(T, WL.k, WL.E, WL.seed * 1000 + layer * 10 + T + 5)
+
+
+def acts_for(layer, T):
+    return synth.activations(T, WL.N, WL.seed * 1000 + layer * 10 + T, WL.outliers)
+
+
+def weight_bytes_per_window(T):
+    gu_b = synth.blob_bytes(GU_T, 2 * WL.F, WL.N)
+    dn_b = synth.blob_bytes(DN_T, WL.N, WL.F)
+    groups = [len(np.unique(routing_for(l, T))) for l in range(WL.layers)]
+    return sum(groups) * (gu_b + dn_b), sum(groups) * gu_b, groups
+
+
+# ------------------------------------------------------------------ clocks
+
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev):
+        self.dev = dev
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [l.strip().split(", ") for l in self.f.read().splitlines() if l.strip()]
+        os.unlink(self.f.name)
+        sm = [float(r[1]) for r in rows if len(r) > 8 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) > 8 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows if len(r) > 8 for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+
+class Window:
+    """Device state of one T: inputs, routing outputs, scratch and the captured 48-layer graph."""
+
+    def __init__(self, m, T, tab_gu, tab_dn, cb_gu, cb_dn, dev):
+        self.T = T
+        L, n = WL.layers, T * WL.k
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.ids_h = torch.from_numpy(np.stack([routing_for(l, T) for l in range(L)])).pin_memory()
+        self.x_h = torch.from_numpy(np.stack([acts_for(l, T) for l in range(L)])).pin_memory()
+        self.out_h = torch.empty((L, n, WL.N), dtype=torch.float32).pin_memory()
+        self.ids = self.ids_h.to(dev)
+        self.x = self.x_h.to(dev)
+        self.ge = torch.zeros((L, n), **i32)
+        self.gs = torch.zeros((L, n + 1), **i32)
+        self.ng = torch.zeros((L, 1), **i32)
+        self.es = torch.zeros((L, n), **i32)
+        self.ed = torch.zeros((L, n), **i32)
+        self.xq = torch.zeros((L, T, WL.N // 32, 36), dtype=torch.uint8, device=dev)
+        self.gu = torch.zeros((n, 2 * WL.F), dtype=torch.float32, device=dev)
+        self.hq = torch.zeros((n, WL.F // 32, 36), dtype=torch.uint8, device=dev)
+        self.out = torch.zeros((L, n, WL.N), dtype=torch.float32, device=dev)
+        self.err = torch.zeros(1, **i32)
+        self.calls = [m.ExpertCall(GU_T, cb_gu, DN_T, cb_dn, WL.N, WL.F, tab_gu[l], tab_dn[l], WL.E, self.ge[l],
+                                   self.gs[l], self.ng[l], n, 0, n, self.xq[l], self.es[l], self.ed[l], self.gu,
+                                   self.hq, self.out[l], self.err, m.F_PDL) for l in range(L)]
+        self.m = m
+        self.graph = None
+
+    def run_layers(self, stream=None):
+        m = self.m
+        for l in range(WL.layers):
+            m.route_group(self.ids[l], WL.E, 0, self.ge[l], self.gs[l], self.ng[l], self.es[l], self.ed[l],
+                          self.err, stream=stream)
+            m.quantize_q8_1(self.x[l], self.xq[l], stream=stream)
+            self.calls[l](stream)
+
+    def capture(self):
+        self.run_layers()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            self.run_layers()
+        self.graph = g
+        return g
+
+
+def launches_per_window():
+    return WL.layers * 5  # route, quantize, gate/up, SwiGLU+q8_1, down
+
+
+def run_ours(args, rank, world):
+    import quantized_routed_expert_grouped_gb300 as m
+    from quantized_routed_expert_grouped_gb300 import build as cuda_build
+
+    cuda_build.build()
+    m.lib()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    hbm_peak, peak_kind = peaks()
+    t0 = time.time()
+    gu_b = synth.blob_bytes(GU_T, 2 * WL.F, WL.N)
+    dn_b = synth.blob_bytes(DN_T, WL.N, WL.F)
+    pool_gu = torch.empty((WL.layers, WL.E, gu_b), dtype=torch.uint8, device=dev)
+    pool_dn = torch.empty((WL.layers, WL.E, dn_b), dtype=torch.uint8, device=dev)
+    for l in range(WL.layers):
+        pool_gu[l] = synth.weight_blobs(GU_T, 2 * WL.F, WL.N, WL.E, synth.derive_key(WL.seed, l, GU_T, 0), dev)
+        pool_dn[l] = synth.weight_blobs(DN_T, WL.N, WL.F, WL.E, synth.derive_key(WL.seed, l, DN_T, 1), dev)
+    tab = lambda p, l: torch.tensor([p[l, x].data_ptr() for x in range(WL.E)], dtype=torch.int64, device=dev)
+    tab_gu = [tab(pool_gu, l) for l in range(WL.layers)]
+    tab_dn = [tab(pool_dn, l) for l in range(WL.layers)]
+    cb_gu = torch.from_numpy(synth.codebook(GU_T, WL.seed * 7 + 1).ravel().copy()).to(dev)
+    cb_dn = torch.from_numpy(synth.codebook(DN_T, WL.seed * 7 + 2).ravel().copy()).to(dev)
+    setup_s = time.time() - t0
+
+    wins = {T: Window(m, T, tab_gu, tab_dn, cb_gu, cb_dn, dev) for T in TS}
+    for w in wins.values():
+        w.capture()
+    torch.cuda.synchronize()
+    if int(wins[1].err.item()):
+        raise RuntimeError(f"device error bits {int(wins[1].err.item())}")
+
+    s = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        for T in TS:
+            wins[T].graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    # ---- timed region: K steps, each the four window graphs; per-T events
+    per_t = {T: [] for T in TS}
+    clocks = Clocks(dev.index)
+    clocks.start()
+    t_start, t_end = ev(), ev()
+    torch.cuda.synchronize()
+    t_start.record(s)
+    for _ in range(args.steps):
+        for T in TS:
+            a, b = ev(), ev()
+            a.record(s)
+            wins[T].graph.replay()
+            b.record(s)
+            per_t[T].append((a, b))
+    t_end.record(s)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    us_t = {T: float(np.median([a.elapsed_time(b) * 1e3 for a, b in per_t[T]])) for T in TS}
+    windows = args.steps * len(TS) * world
+    value = total_ms * 1e3 / windows
+    bytes_t = {T: weight_bytes_per_window(T) for T in TS}
+    per_T = {str(T): {"us": round(us_t[T], 2), "weight_bytes": bytes_t[T][0],
+                      "GBps": round(bytes_t[T][0] / (us_t[T] * 1e-6) / 1e9, 1),
+                      "frac_of_measured_hbm": round(bytes_t[T][0] / (us_t[T] * 1e-6) / 1e9 / hbm_peak, 4),
+                      "groups_per_layer": round(float(np.mean(bytes_t[T][2])), 2)} for T in TS}
+
+    # ---- dominant kernel (grouped gate/up) timed on its own, T = 4, all 48 layers per launch set
+    roof = gate_up_roofline(m, wins[4], bytes_t[4], hbm_peak, peak_kind, s)
+
+    # ---- end to end: pinned host inputs -> device, the window graphs, outputs -> host
+    e2e = end_to_end(wins, args, s, world, dev)
+
+    launches = args.steps * len(TS) * launches_per_window()
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "us/window", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8 dp4a + fp32", "data": "synthetic",
+        "config": {"workload": "window48: 48 layers x 128 experts, top-8, n_embd 2560, n_ff 768, CB3 gate/up + "
+                               "NL4 down (16.4 GB pool), T=1..4, one CUDA graph per T",
+                   "l2": "inputs larger than L2 (>= 1 GB of weights per window), no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "per_T": per_T, "roofline": roof, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+        "setup_s": round(setup_s, 1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(sample_layers=args.cpu_layers)
+    return line
+
+
+def gate_up_roofline(m, w, bytes_t, hbm_peak, peak_kind, s):
+    """The grouped gate/up kernel launched alone for the 48 layers of the T = 4 window (inputs
+    already routed and quantized), CUDA events on the launching stream."""
+    for l in range(WL.layers):
+        m.grouped_gu(GU_T, w.calls[l]._keep[0], WL.N, WL.F, w.calls[l]._keep[2], WL.E, w.ge[l], w.gs[l], w.ng[l],
+                     w.T * WL.k, 0, w.xq[l], w.es[l], w.T * WL.k, w.gu, w.err, stream=s)
+    torch.cuda.synchronize()
+    reps = 5
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(reps):
+        for l in range(WL.layers):
+            m.grouped_gu(GU_T, w.calls[l]._keep[0], WL.N, WL.F, w.calls[l]._keep[2], WL.E, w.ge[l], w.gs[l],
+                         w.ng[l], w.T * WL.k, 0, w.xq[l], w.es[l], w.T * WL.k, w.gu, w.err, stream=s)
+    b.record(s)
+    torch.cuda.synchronize()
+    dur_s = a.elapsed_time(b) * 1e-3 / (reps * WL.layers)
+    per_launch = bytes_t[1] / WL.layers
+    ach = per_launch / dur_s / 1e9
+    return {"kernel": "grouped gate/up (CB3, T=4)", "bound": "hbm", "achieved": round(ach, 1),
+            "peak": hbm_peak, "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": None,
+            "peak_kind": peak_kind, "bytes_per_launch": int(per_launch), "us_per_launch": round(dur_s * 1e6, 2)}
+
+
+def end_to_end(wins, args, s, world, dev):
+    steps = max(2, args.steps // 2)
+    h2d = sum(w.x_h.numel() * 4 + w.ids_h.numel() * 4 for w in wins.values())
+    d2h = sum(w.out_h.numel() * 4 for w in wins.values())
+    for _ in range(2):
+        for w in wins.values():
+            w.x.copy_(w.x_h, non_blocking=True)
+            w.ids.copy_(w.ids_h, non_blocking=True)
+            w.graph.replay()
+            w.out_h.copy_(w.out, non_blocking=True)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(steps):
+        for w in wins.values():
+            w.x.copy_(w.x_h, non_blocking=True)
+            w.ids.copy_(w.ids_h, non_blocking=True)
+            w.graph.replay()
+            w.out_h.copy_(w.out, non_blocking=True)
+    b.record(s)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(ms * 1e3 / (steps * len(wins) * world), 3), "unit": "us/window",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_layer(o, layer, T):
+    ids = routing_for(layer, T)
+    x = acts_for(layer, T)
+    r = o.route_group(ids, WL.E)
+    G, n = r["n_groups"], T * WL.k
+    key_gu = synth.derive_key(WL.seed, layer, GU_T, 0)
+    key_dn = synth.derive_key(WL.seed, layer, DN_T, 1)
+    gub = [np.zeros(1, np.uint8)] * WL.E
+    dnb = [np.zeros(1, np.uint8)] * WL.E
+    for e in r["grp_expert"]:
+        gub[e] = synth.weight_blobs(GU_T, 2 * WL.F, WL.N, 1, key_gu, "cpu", first_blob=int(e))[0].numpy()
+        dnb[e] = synth.weight_blobs(DN_T, WL.N, WL.F, 1, key_dn, "cpu", first_blob=int(e))[0].numpy()
+    cb_gu = synth.codebook(GU_T, WL.seed * 7 + 1)
+    cb_dn = synth.codebook(DN_T, WL.seed * 7 + 2)
+    t0 = time.perf_counter()
+    xq = o.quantize_q8_1(x)
+    gu = np.zeros((n, 2 * WL.F))
+    o.grouped_gemv(GU_T, WL.N, 2 * WL.F, gub, r["grp_expert"], r["grp_start"], G, xq, ent_in=r["ent_src"],
+                   out=gu, cb=cb_gu)
+    hq = np.zeros((n, WL.F // 32, 36), np.uint8)
+    o.swiglu_q8_1(gu.astype(np.float32), WL.F, r["grp_start"][0], r["grp_start"][G], hq)
+    out = np.zeros((n, WL.N))
+    o.grouped_gemv(DN_T, WL.F, WL.N, dnb, r["grp_expert"], r["grp_start"], G, hq, ent_out=r["ent_dst"], out=out,
+                   cb=cb_dn)
+    o.route_group(ids, WL.E)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(sample_layers=1):
+    import oracle
+    o = oracle.get()
+    per_t = {}
+    for T in TS:
+        secs = [oracle_layer(o, l, T) for l in range(sample_layers)]
+        per_t[T] = float(np.mean(secs)) * WL.layers * 1e6
+    return {"value": round(float(np.mean(list(per_t.values()))), 1), "unit": "us/window", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{sample_layers} layer(s) per T=1..4 of the 48-layer window, single-threaded C oracle "
+                      f"(fp64 block sums), scaled x48 layers",
+            "per_T_us": {str(T): round(v, 1) for T, v in per_t.items()}}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    o = oracle.get()
+    oracle_layer(o, 0, 1)
+    for _ in range(args.warmup):
+        oracle_layer(o, 0, 1)
+    times = []
+    t0 = time.perf_counter()
+    for step in range(args.steps):
+        lay = step % WL.layers
+        times.append(sum(oracle_layer(o, lay, T) for T in TS))
+    wall = time.perf_counter() - t0
+    value = float(np.mean(times)) * WL.layers / len(TS) * 1e6
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "us/window", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall * 1e3 / args.steps, 2),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "int32 + fp64",
+            "data": "synthetic",
+            "config": {"workload": "window48: 48 layers x 128 experts, top-8, n_embd 2560, n_ff 768, CB3 gate/up + "
+                                   "NL4 down, T=1..4",
+                       "l2": "n/a (CPU)", "parallelism": "single CPU thread"},
+            "cpu_baseline": {"value": round(value, 1), "unit": "us/window", "cores": 1, "kind": "oracle",
+                             "sample": "per step: one layer at each T=1..4 (layer = step mod 48), scaled x48"},
+            "e2e": {"value": round(value, 1), "unit": "us/window", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_case(args):
+    """One layer of the window at T = args.case_t, run eagerly a few times: the small case for
+    kernel-level profiling (about 0.4 GB on the device)."""
+    import quantized_routed_expert_grouped_gb300 as m
+    from quantized_routed_expert_grouped_gb300 import build as cuda_build
+
+    cuda_build.build()
+    m.lib()
+    dev = torch.device("cuda", 0)
+    T = args.case_t
+    pool_gu = synth.weight_blobs(GU_T, 2 * WL.F, WL.N, WL.E, synth.derive_key(WL.seed, 0, GU_T, 0), dev)
+    pool_dn = synth.weight_blobs(DN_T, WL.N, WL.F, WL.E, synth.derive_key(WL.seed, 0, DN_T, 1), dev)
+    tab = lambda p: torch.tensor([p[x].data_ptr() for x in range(WL.E)], dtype=torch.int64, device=dev)
+    cb_gu = torch.from_numpy(synth.codebook(GU_T, WL.seed * 7 + 1).ravel().copy()).to(dev)
+    cb_dn = torch.from_numpy(synth.codebook(DN_T, WL.seed * 7 + 2).ravel().copy()).to(dev)
+    n = T * WL.k
+    i32 = dict(dtype=torch.int32, device=dev)
+    ids = torch.from_numpy(routing_for(0, T)).to(dev)
+    x = torch.from_numpy(acts_for(0, T)).to(dev)
+    ge, gs, ng = torch.zeros(n, **i32), torch.zeros(n + 1, **i32), torch.zeros(1, **i32)
+    es, ed, err = torch.zeros(n, **i32), torch.zeros(n, **i32), torch.zeros(1, **i32)
+    xq = torch.zeros((T, WL.N // 32, 36), dtype=torch.uint8, device=dev)
+    gu = torch.zeros((n, 2 * WL.F), dtype=torch.float32, device=dev)
+    hq = torch.zeros((n, WL.F // 32, 36), dtype=torch.uint8, device=dev)
+    out = torch.zeros((n, WL.N), dtype=torch.float32, device=dev)
+    call = m.ExpertCall(GU_T, cb_gu, DN_T, cb_dn, WL.N, WL.F, tab(pool_gu), tab(pool_dn), WL.E, ge, gs, ng, n, 0, n,
+                        xq, es, ed, gu, hq, out, err, m.F_PDL)
+    for _ in range(args.steps):
+        m.route_group(ids, WL.E, 0, ge, gs, ng, es, ed, err)
+        m.quantize_q8_1(x, xq)
+        call()
+    torch.cuda.synchronize()
+    print(json.dumps({"case": f"one layer of window48 at T={T}", "err": int(err.item()),
+                      "groups": int(ng.item())}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--case", action="store_true", help="run the single-layer profiling case instead")
+    ap.add_argument("--case-t", type=int, default=4)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-layers", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.case:
+        run_case(args)
+        return
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            torch.distributed.init_process_group("nccl")
+        line = run_ours(args, rank, world)
+        if world > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
