@@ -74,6 +74,7 @@ extern "C" {
 #define MOE_E_CAP (-4)   /* cap_groups / cap_entries / n_experts not positive, or too large */
 #define MOE_E_CUDA (-5)  /* a CUDA runtime call failed (launch, attribute, device query) */
 #define MOE_E_ALIGN (-6) /* a host-checkable pointer is not suitably aligned */
+#define MOE_E_SCRATCH (-7) /* the call needs more scratch than the library's static buffer holds */
 
 /* ---- device-side error bits, OR-ed into *err */
 #define MOE_ERR_NGROUPS 1   /* *n_groups < 0 or > cap_groups (clamped) */
@@ -180,6 +181,29 @@ typedef struct moe_expert_call {
 } moe_expert_call;
 
 int moe_expert_grouped(const moe_expert_call* call, cudaStream_t stream);
+
+/* Allocation-free variant of moe_expert_grouped (the pages have no counterpart; this is a
+ * library convenience).
+ *
+ * Some callers cannot allocate device memory for the call's scratch: an engine that reserves all
+ * of its device memory up front and forbids allocation afterwards, a plugin running inside a host
+ * framework that owns every allocation, or a latency-critical path that cannot afford the
+ * implicit device synchronisation of cudaMalloc/cudaFree. This entry point takes the same
+ * arguments as moe_expert_grouped but ignores call->gu and call->hq: the gate/up rows and the
+ * q8_1 h rows live in one buffer of MOE_STATIC_SCRATCH_BYTES bytes that the library declares as
+ * static device memory, so nothing is allocated at call time. Every GPU that loads the library
+ * holds that buffer until the process exits.
+ *  - Limit: cap_entries * (2*n_ff*4 + (n_ff/32)*36) bytes (each part rounded up to 256) must not
+ *    exceed MOE_STATIC_SCRATCH_BYTES, else MOE_E_SCRATCH is returned and nothing is launched
+ *    (e.g. 32 entries at n_ff 768 need about 0.2 MB; 256 entries at n_ff 1536 about 3.6 MB).
+ *  - The first call on each device looks up the buffer's device address (once per device, with
+ *    that device current); make that first call before any stream capture on the device.
+ *  - Every call shares the one buffer and it keeps the previous call's contents; the call writes
+ *    every scratch row it later reads, so nothing needs clearing, but calls that overlap on the
+ *    GPU (other streams, other threads) race on the buffer and must be serialised by the caller.
+ */
+#define MOE_STATIC_SCRATCH_BYTES (4u << 20)
+int moe_expert_grouped_static(const moe_expert_call* call, cudaStream_t stream);
 
 /* Test hook: the per-32-block integer sums of `rows` consecutive rows of one blob (row bytes
  * apart) against one q8_1 row xq[K/32], computed by the same device decode and dot-product

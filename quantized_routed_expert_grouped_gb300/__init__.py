@@ -17,11 +17,12 @@ import torch
 __all__ = [
     "Q8_0", "Q4B", "NL4", "CB2", "CB3", "MoeError", "lib", "row_bytes", "strerror",
     "quantize_q8_1", "route_group", "grouped_gu", "swiglu_q8_1", "grouped_down",
-    "expert_grouped", "ExpertCall", "test_block_isum", "ERR_BITS", "F_PDL",
+    "expert_grouped", "ExpertCall", "STATIC_SCRATCH_BYTES", "test_block_isum", "ERR_BITS", "F_PDL",
 ]
 
 Q8_0, Q4B, NL4, CB2, CB3 = 1, 2, 3, 4, 5
 F_PDL = 1
+STATIC_SCRATCH_BYTES = 4 << 20
 ERR_BITS = {1: "NGROUPS", 2: "EXPERT", 4: "START", 8: "ENTRY", 16: "ALIGN", 32: "CODEBOOK",
             64: "TIMEOUT", 128: "ROUTE"}
 
@@ -72,9 +73,10 @@ def lib():
         L.moe_grouped_down.argtypes = [WFmt, _I, _I, _P, _I, _P, _P, _P, _I, _I, _P, _I, _P, _P, _I64, _I64,
                                        _P, _P]
         L.moe_expert_grouped.argtypes = [ctypes.POINTER(ExpertCallC), _P]
+        L.moe_expert_grouped_static.argtypes = [ctypes.POINTER(ExpertCallC), _P]
         L.moe_test_block_isum.argtypes = [WFmt, _I, _P, _I, _P, _P, _P]
         for f in ("moe_quantize_q8_1", "moe_route_group", "moe_grouped_gu", "moe_swiglu_q8_1",
-                  "moe_grouped_down", "moe_expert_grouped", "moe_test_block_isum"):
+                  "moe_grouped_down", "moe_expert_grouped", "moe_expert_grouped_static", "moe_test_block_isum"):
             getattr(L, f).restype = _I
         _LIB = L
     return _LIB
@@ -163,6 +165,11 @@ class ExpertCall:
 
     def __call__(self, stream=None):
         _check(lib().moe_expert_grouped(ctypes.byref(self.c), _stream(stream)))
+
+    def call_static(self, stream=None):
+        """The same call through moe_expert_grouped_static: gu/hq are ignored and the library's
+        static device scratch buffer is used instead (nothing is allocated)."""
+        _check(lib().moe_expert_grouped_static(ctypes.byref(self.c), _stream(stream)))
 
 
 def expert_grouped(*args, stream=None, **kw):

@@ -237,6 +237,7 @@ const char* moe_strerror(int status) {
     case MOE_E_CAP: return "capacity or count not positive or too large";
     case MOE_E_CUDA: return "a CUDA runtime call failed";
     case MOE_E_ALIGN: return "pointer not suitably aligned";
+    case MOE_E_SCRATCH: return "the call needs more scratch than the static buffer (MOE_STATIC_SCRATCH_BYTES) holds";
     }
     return "unknown status";
 }
