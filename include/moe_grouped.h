@@ -27,7 +27,7 @@
  *    MOE_ERR_* bits into *err when err is not NULL; the offending group or entry is skipped (its
  *    rows are not written), *n_groups is clamped to cap_groups. Kernels never trap and never wait
  *    without a time limit.
- *  - Shapes: n_embd and n_ff are multiples of 256.
+ *  - Shapes: n_embd and n_ff are multiples of 256, at most 8192; cap_groups <= 1024.
  *
  * Weight formats (this library's own byte layouts; the pages name real formats but print none).
  * Little-endian, fp16 fields are IEEE binary16. A row of K weights is K/32 blocks (K/256
@@ -93,8 +93,8 @@ typedef struct moe_q8_1 {
     int8_t q[32];
 } moe_q8_1;
 
-/* A weight format: type = MOE_*; codebook = device pointer to the NL4 table (16 int8), the
- * CB2 grid (256x8 int8) or the CB3 grid (256x4 int8); NULL for Q8_0 and Q4B. */
+/* A weight format: type = MOE_*; codebook = device pointer (4-byte aligned) to the NL4 table
+ * (16 int8), the CB2 grid (256x8 int8) or the CB3 grid (256x4 int8); NULL for Q8_0 and Q4B. */
 typedef struct moe_wfmt {
     int32_t type;
     const int8_t* codebook;

@@ -11,7 +11,8 @@ using namespace moe;
 
 namespace {
 
-constexpr int kSmemBudget = 227 * 1024;
+constexpr int kSmemPerSm = 228 * 1024;
+constexpr int kMaxGroups = 1024;
 
 bool cb_type(int t) { return t == MOE_CB2 || t == MOE_CB3; }
 bool valid_type(int t) { return t >= MOE_Q8_0 && t <= MOE_CB3; }
@@ -32,70 +33,64 @@ int sm_count() {
 int check_fmt(const moe_wfmt& f) {
     if (!valid_type(f.type)) return MOE_E_TYPE;
     if ((f.type == MOE_NL4 || cb_type(f.type)) && f.codebook == nullptr) return MOE_E_TYPE;
+    if (reinterpret_cast<uintptr_t>(f.codebook) & 3u) return MOE_E_ALIGN;
     return MOE_OK;
 }
 
 int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
 // Launch geometry and shared-memory layout of one grouped GEMV (K weights per row, `rows`
-// rows per expert), filled into `a` and `p`.
-int plan_gemv(int type, int K, int rows, GemvArgs& a, GemvPlan& p) {
+// rows per expert), filled into `a` and `p`. One CTA per SM: a producer warp and up to 12
+// consumer warps grouped in warp-sets; a set works on one tile (32 rows, lane = row) at a time,
+// its warps splitting the row's 256-weight chunks; as many sets as fit in 12 warps.
+int plan_gemv(int type, int K, int rows, int cap_groups, GemvArgs& a, GemvPlan& p) {
     const int nch = K / 256;
     const int64_t rb = moe_row_bytes(type, K);
-    if (nch <= 0 || rb <= 0 || rows <= 0 || rows % 8) return MOE_E_SHAPE;
-    const int R = cb_type(type) ? 2 : 1;
-    const int maxt = cb_type(type) ? 384 : 512;
+    if (nch <= 0 || nch > 32 || rb <= 0 || rows <= 0 || rows % 8) return MOE_E_SHAPE;
+    if (cap_groups <= 0 || cap_groups > kMaxGroups) return MOE_E_CAP;
+    const bool cb = cb_type(type);
+    const int CPW = (nch + 11) / 12;
+    const int WPS = (nch + CPW - 1) / CPW;
+    const int RT = 32 * rb <= 96 * 1024 ? 32 : 16;
     const int nb = K / 32, nbp = nb + nb / 8;
-    // fixed part of shared memory (everything but the staging ring)
-    auto fixed_bytes = [&](int RT) {
-        int f = cb_type(type) ? 32768 : 0;                     // codebook replicas
-        f += round_up(4 * 2 * nbp * 16, 128);                  // staged activation codes
-        f += round_up(4 * nb * 4, 128) * 2;                    // fp32 scales + aux
-        f += round_up(nch * 4 * RT * 4, 128);                  // partial sums
-        f += 128 + 128;                                        // barriers + misc
-        return f;
-    };
-    for (int QR : {32, 16, 8}) {
-        const int NT = round_up(nch * QR, 32);
-        const int RT = QR * R;
-        const int64_t tile = static_cast<int64_t>(RT) * rb;
-        if (NT > maxt || tile > 72 * 1024) continue;
-        const int stage_bytes = round_up(static_cast<int>(tile) + 16, 128);
-        const int fixed = fixed_bytes(RT);
-        int stages = (kSmemBudget - fixed) / stage_bytes;
-        if (stages > 4) stages = 4;
-        if (stages < 2) continue;
-        p.R = R;
-        p.QR = QR;
-        p.RT = RT;
-        p.NT = NT;
-        p.stages = stages;
-        p.stage_bytes = stage_bytes;
-        // layout: ring | codebook | act codes | dx | aux | partials | barriers | misc
-        int off = stages * stage_bytes;
-        a.off_cb = off;
-        off += cb_type(type) ? 32768 : 0;
-        a.off_actq = off;
-        off += round_up(4 * 2 * nbp * 16, 128);
-        a.off_dx = off;
-        off += round_up(4 * nb * 4, 128);
-        a.off_aux = off;
-        off += round_up(4 * nb * 4, 128);
+    const int actq = round_up(2 * 4 * 2 * nbp * 16, 128), act2 = round_up(2 * 4 * nb * 8, 128);
+    const int grp = round_up(24 * cap_groups + 8 * (cap_groups + 1), 128);
+    const int fixed = (cb ? 32768 : 0) + actq + act2 + grp + 256 + 512;
+    const int stage_bytes = round_up(static_cast<int>(RT * rb) + 16, 128);
+    const int part_bytes = nch * 4 * RT * 4;
+    for (int TP = 12 / WPS > 0 ? 12 / WPS : 1; TP >= 1; --TP) {
+        int stages = (kSmemPerSm - 1024 - fixed) / (stage_bytes + part_bytes);
+        if (stages > 8) stages = 8;
+        if (stages < 2 || stages < TP + 1) continue;
+        int off = cb ? 32768 : 0;  // the codebook sits at offset 0
+        a.off_ring = off;
+        off += stages * stage_bytes;
         a.off_part = off;
-        off += round_up(nch * 4 * RT * 4, 128);
+        off += stages * part_bytes;
+        a.off_actq = off;
+        off += actq;
+        a.off_act2 = off;
+        off += act2;
+        a.off_grp = off;
+        off += grp;
         a.off_bar = off;
-        off += 128;
+        off += 256;
         a.off_misc = off;
-        off += 128;
+        off += 512;
+        p.NT = 32 * (WPS * TP + 1);
         p.smem = off;
         a.K = K;
         a.rows = rows;
         a.row_bytes = static_cast<int>(rb);
         a.nch = nch;
-        a.QR = QR;
+        a.CPW = CPW;
+        a.WPS = WPS;
+        a.TP = TP;
+        a.CW = WPS * TP;
         a.RT = RT;
         a.stages = stages;
         a.stage_bytes = stage_bytes;
+        a.part_bytes = part_bytes;
         a.nb = nb;
         a.nbp = nbp;
         return MOE_OK;
@@ -126,14 +121,14 @@ cudaError_t launch_gemv(int type, const GemvArgs& a, int grid, int NT, int smem,
 // Persistent grid: every SM's resident CTAs, but no more than grid_groups x tiles per group.
 int run_gemv(int type, GemvArgs& a, int grid_groups, cudaStream_t s, bool pdl) {
     GemvPlan p;
-    int rc = plan_gemv(type, a.K, a.rows, a, p);
+    int rc = plan_gemv(type, a.K, a.rows, a.cap_groups, a, p);
     if (rc != MOE_OK) return rc;
     int ctas = 0;
     if (occupancy(type, p.NT, p.smem, &ctas) != cudaSuccess || ctas < 1) return MOE_E_CUDA;
     const int sms = sm_count();
     if (sms <= 0) return MOE_E_CUDA;
     const int gg = grid_groups <= 0 || grid_groups > a.cap_groups ? a.cap_groups : grid_groups;
-    const int64_t tiles = (a.rows + p.RT - 1) / p.RT;
+    const int64_t tiles = (a.rows + a.RT - 1) / a.RT;  // tiles of one group
     int64_t grid = static_cast<int64_t>(gg) * tiles;
     if (grid > static_cast<int64_t>(sms) * ctas) grid = static_cast<int64_t>(sms) * ctas;
     if (grid < 1) grid = 1;

@@ -8,30 +8,38 @@
 // from HBM once per group and applied to all of the group's entries.
 //
 // How (GB300 design, not the pages' kernels):
-//  * Work is the flattened list of (group, 8-row block) pairs of this call, split into one
-//    contiguous, balanced range per CTA of a persistent grid. A CTA walks its range in tiles of
-//    up to RT rows of one expert (contiguous bytes of the blob).
-//  * One thread (tid 0) streams tiles into a ring of shared-memory slots with 1-D bulk copies
-//    (cp.async.bulk, TMA engine) completing on mbarriers; all threads wait with a time limit.
-//  * The group's q8_1 rows (up to 4 entries at a time) are staged once per group in shared
-//    memory as 16-byte halves (conflict-free 128-bit loads, padded every 8 blocks) with the
-//    scale as fp32 and, for the codebook formats, the exact sum of the codes.
-//  * Thread (c, q) owns 256-weight chunk c of R rows q*R..q*R+R-1 of the tile: it decodes each
-//    32-weight block once and applies it to every staged entry with dp4a; its per-(row, entry)
-//    partial goes to shared memory and a fixed-order sum over the chunks gives the output.
-//    The order of every floating-point operation for one (row, entry) depends only on the row's
-//    chunk index, so results do not depend on the grid, the tile size or the other entries.
-//  * CB2/CB3 grids are stored in shared memory in "x-form" x = (g - 1) / 2 (g odd), replicated
-//    per lane ([index][lane] layout: conflict-free lookups). A sign flip of g is then a bit
-//    flip of x (~x = -x - 1, so 2*(~x) + 1 = -g), and sum_i s_i g_i q_i = 2 * dp4a(x ^ mask, q)
-//    + sum_i q_i, with the per-block code sum taken once per staged activation block.
+//  * Persistent grid. The call's work is the list of (group, 8-row block) pairs; each CTA takes
+//    one contiguous range of it, balanced by cost (a row of a group with n entries costs
+//    alpha + n, alpha being the decode's share), computed from the device-side group arrays.
+//  * Warp specialisation. Warp 0 streams tiles (up to 32 rows of one expert: contiguous bytes of
+//    its blob) into a ring of shared-memory slots with 1-D bulk copies (cp.async.bulk, TMA
+//    engine); a slot's "full" mbarrier completes on the copy's byte count and its "empty"
+//    mbarrier when its consumers have released it. Every wait has a time limit.
+//  * The q8_1 rows of the (at most two) groups of a CTA's range are staged once in shared memory
+//    as 16-byte halves with (scale, aux) pairs as float2; all lanes of a warp read the same
+//    block at the same time (broadcast loads).
+//  * Consumer warps form warp-sets; a set owns one tile at a time (lane = row) and its warps
+//    split the rows' 256-weight chunks. A lane decodes each 32-weight block of its row's chunk
+//    once and applies it to every staged entry with dp4a; the chunk partials go to shared memory
+//    and the set's last warp to finish (shared atomic counter after a fence) sums them in chunk
+//    order: no barrier between warps. The order of every floating-point operation for one
+//    (row, entry) depends only on the row's chunks, so results do not depend on the grid, the
+//    tile size or the other entries.
+//  * CB2/CB3 grids are held in shared memory (at offset 0) in "x-form" x = (g - 1) / 2 (g odd),
+//    replicated per lane ([index][lane]: conflict-free lookups). A sign flip of g is a bit flip
+//    of x (2*(~x) + 1 = -g), so sum_i s_i g_i q_i = 2 * dp4a(x ^ mask, q) + sum_i q_i; the
+//    per-block code sum is taken once when the activation row is staged. A sign nibble becomes a
+//    byte mask by one 32x32->64 multiply (bits to byte msbs) and one sign-replicating permute.
 //  * NL4 codes are looked up in the 16-entry table held in four registers with byte permutes
-//    (two 8-entry halves and a per-byte select on the code's top bit).
+//    (two 8-entry halves and a per-byte select on the code's top bit); the staged activation
+//    words are permuted to the permute's byte order.
 //  * No tensor cores: at 1-4 entries per group this is a batched GEMV, bound by HBM bandwidth
 //    and by the integer decode.
 #pragma once
 
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -41,29 +49,55 @@ namespace moe {
 template <int TYPE>
 struct Fmt;
 template <>
-struct Fmt<MOE_Q8_0> { static constexpr int CHUNK = 272, R = 1, MAXT = 512; static constexpr bool CB = false; };
+struct Fmt<MOE_Q8_0> { static constexpr int CHUNK = 272, R = 1, ALPHA = 1; static constexpr bool CB = false; };
 template <>
-struct Fmt<MOE_Q4B> { static constexpr int CHUNK = 160, R = 1, MAXT = 512; static constexpr bool CB = false; };
+struct Fmt<MOE_Q4B> { static constexpr int CHUNK = 160, R = 1, ALPHA = 2; static constexpr bool CB = false; };
 template <>
-struct Fmt<MOE_NL4> { static constexpr int CHUNK = 144, R = 1, MAXT = 512; static constexpr bool CB = false; };
+struct Fmt<MOE_NL4> { static constexpr int CHUNK = 144, R = 1, ALPHA = 5; static constexpr bool CB = false; };
 template <>
 struct Fmt<MOE_CB2> {
-    static constexpr int CHUNK = 70, R = 2, MAXT = 384, NW = 18, IDX = 0, SGN = 8, SUB = 16;
+    static constexpr int CHUNK = 70, R = 2, ALPHA = 4, NW = 18, SGN = 8, SUB = 16;
     static constexpr bool CB = true;
 };
 template <>
 struct Fmt<MOE_CB3> {
-    static constexpr int CHUNK = 102, R = 2, MAXT = 384, NW = 26, IDX = 0, SGN = 16, SUB = 24;
+    static constexpr int CHUNK = 102, R = 2, ALPHA = 5, NW = 26, SGN = 16, SUB = 24;
     static constexpr bool CB = true;
 };
 
+constexpr int kMaxThreads = 416;  // one producer warp + up to 12 consumer warps (<= 128 registers)
+
 __device__ __forceinline__ uint32_t ld32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+__device__ __forceinline__ void named_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
 
 // ---------------------------------------------------------------- per-format decode
 
-// Bytes 0..3 of the 4-bit sign nibble -> 0xFF where the bit is set (bit i -> msb of byte i by one
-// multiply, then a sign-replicating byte permute).
-__device__ __forceinline__ uint32_t sign_mask4(uint32_t nib) { return prmt(nib * 0x10204080u, 0u, 0xBA98u); }
+// Byte mask of sign nibble w of sg (0xFF where the weight is negated). The nibble, isolated,
+// times sum_i 2^(7i+c) (c = 7 for even w, 3 for odd w) puts bit i at the msb of byte (w/2 + i)
+// of the 64-bit product with no carries (copies 7 bits apart, 4 bits wide); a permute with
+// sign replication turns those msbs into the mask.
+template <int w>
+__device__ __forceinline__ uint32_t sign_mask(uint32_t sg) {
+    const uint32_t v = sg & (0xFu << (4 * w));
+    const unsigned long long p =
+        static_cast<unsigned long long>(v) * ((w & 1) ? 0x01020408ull : 0x10204080ull);
+    constexpr uint32_t sel = 0x8888u + 0x1111u * (w >> 1) + 0x3210u;
+    return prmt(static_cast<uint32_t>(p), static_cast<uint32_t>(p >> 32), sel);
+}
+
+// Shared-memory offset (idx << 7) | loff of index byte k of word iw.
+template <int k>
+__device__ __forceinline__ uint32_t cb_off(uint32_t iw, uint32_t loff) {
+    const uint32_t s = k == 0 ? (iw << 7) : (iw >> (8 * k - 7));
+    return (s & 0x7f80u) | loff;
+}
 
 // A CB chunk-row (70 or 102 bytes at an even, possibly not 4-aligned address) held as aligned
 // words plus the byte-permute selector that realigns a field at logical offset L:
@@ -90,45 +124,70 @@ struct CBRow {
 };
 
 // Decode 32-weight sub-block j of a CB chunk-row into 8 words of x-form values with the sign
-// mask applied (w = x ^ mask) and return ls = 2*sub+1. cbt: this lane's codebook replica.
-template <int TYPE>
-__device__ __forceinline__ int cb_decode(const CBRow<TYPE>& row, const int j, const uint8_t* cbt, uint32_t W[8]) {
+// mask applied (w = x ^ mask) and return ls = 2*sub+1. tab: the codebook replicas (smem offset
+// 0); loff: this lane's replica offset.
+template <int TYPE, int j>
+__device__ __forceinline__ int cb_decode(const CBRow<TYPE>& row, const uint8_t* tab, uint32_t loff, uint32_t W[8]) {
     const uint32_t subw = row.w2(Fmt<TYPE>::SUB);
     const int ls = 2 * static_cast<int>((subw >> (8 * (j >> 1) + 4 * (j & 1))) & 15u) + 1;
     const uint32_t sg = row.w2(Fmt<TYPE>::SGN + j);
     if constexpr (TYPE == MOE_CB3) {
         const uint32_t i0 = row.w2(2 * j), i1 = row.w2(2 * j + 1);
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            const uint32_t idx = ((w < 4 ? i0 : i1) >> (8 * (w & 3))) & 0xffu;
-            const uint32_t g = ld32(cbt + (idx << 7));
-            W[w] = g ^ sign_mask4((sg >> (4 * w)) & 15u);
-        }
+        W[0] = ld32(tab + cb_off<0>(i0, loff)) ^ sign_mask<0>(sg);
+        W[1] = ld32(tab + cb_off<1>(i0, loff)) ^ sign_mask<1>(sg);
+        W[2] = ld32(tab + cb_off<2>(i0, loff)) ^ sign_mask<2>(sg);
+        W[3] = ld32(tab + cb_off<3>(i0, loff)) ^ sign_mask<3>(sg);
+        W[4] = ld32(tab + cb_off<0>(i1, loff)) ^ sign_mask<4>(sg);
+        W[5] = ld32(tab + cb_off<1>(i1, loff)) ^ sign_mask<5>(sg);
+        W[6] = ld32(tab + cb_off<2>(i1, loff)) ^ sign_mask<6>(sg);
+        W[7] = ld32(tab + cb_off<3>(i1, loff)) ^ sign_mask<7>(sg);
     } else {
         const uint32_t iw = row.w2(j);
-#pragma unroll
-        for (int gi = 0; gi < 4; ++gi) {
-            const uint32_t idx = (iw >> (8 * gi)) & 0xffu;
-            const uint2 g = *reinterpret_cast<const uint2*>(cbt + (idx << 7));
-            W[2 * gi] = g.x ^ sign_mask4((sg >> (8 * gi)) & 15u);
-            W[2 * gi + 1] = g.y ^ sign_mask4((sg >> (8 * gi + 4)) & 15u);
-        }
+        uint2 g;
+        g = *reinterpret_cast<const uint2*>(tab + cb_off<0>(iw, loff));
+        W[0] = g.x ^ sign_mask<0>(sg);
+        W[1] = g.y ^ sign_mask<1>(sg);
+        g = *reinterpret_cast<const uint2*>(tab + cb_off<1>(iw, loff));
+        W[2] = g.x ^ sign_mask<2>(sg);
+        W[3] = g.y ^ sign_mask<3>(sg);
+        g = *reinterpret_cast<const uint2*>(tab + cb_off<2>(iw, loff));
+        W[4] = g.x ^ sign_mask<4>(sg);
+        W[5] = g.y ^ sign_mask<5>(sg);
+        g = *reinterpret_cast<const uint2*>(tab + cb_off<3>(iw, loff));
+        W[6] = g.x ^ sign_mask<6>(sg);
+        W[7] = g.y ^ sign_mask<7>(sg);
     }
     return ls;
 }
 
-// Block j (32 weights) of a 16-byte-aligned Q8_0 / Q4B / NL4 chunk: 8 weight words matching the
+// NL4: the four 4-bit codes of one byte lane set -> table values, bytes in the order [0, 2, 1, 3].
+// sel: 3-bit codes as a permute selector; msk: 0xFF bytes where the code is >= 8.
+__device__ __forceinline__ uint32_t nl4_lookup(const uint32_t tab[4], uint32_t sel, uint32_t msk) {
+    const uint32_t lo = prmt(tab[0], tab[1], sel), hi = prmt(tab[2], tab[3], sel);
+    return (lo & ~msk) | (hi & msk);
+}
+
+// One 16-byte NL4 code word Q (codes of weights 4k..4k+3 in the low nibbles, 16+4k.. in the high)
+// -> two weight words (byte order [0, 2, 1, 3], matching the staged activations).
+__device__ __forceinline__ void nl4_word(const uint32_t tab[4], uint32_t Q, uint32_t& wlo, uint32_t& whi) {
+    const uint32_t s = Q & 0x77777777u;
+    const uint32_t sl = (s & 0x0f0fu) | ((s >> 12) & 0xf0f0u);
+    const uint32_t sh = ((s >> 4) & 0x0f0fu) | ((s >> 16) & 0xf0f0u);
+    wlo = nl4_lookup(tab, sl, prmt(Q << 4, 0u, 0xB9A8u));
+    whi = nl4_lookup(tab, sh, prmt(Q, 0u, 0xB9A8u));
+}
+
+// Block j (32 weights) of a Q8_0 / Q4B chunk in shared memory: 8 weight words matching the
 // staged activation words, the weight scale d and (Q4B) the minimum m.
-template <int TYPE>
-__device__ __forceinline__ void blk_decode(const uint8_t* chunk, const int j, const uint32_t tab[4], uint32_t W[8],
-                                           float& d, float& m) {
+template <int TYPE, int j>
+__device__ __forceinline__ void blk_decode_smem(const uint8_t* chunk, uint32_t W[8], float& d, float& m) {
     if constexpr (TYPE == MOE_Q8_0) {
-        const int L = 34 * j;  // j even: L % 4 == 0; j odd: L % 4 == 2
+        constexpr int L = 34 * j;  // j even: L % 4 == 0; j odd: L % 4 == 2
         const uint8_t* p = chunk + (L & ~3);
         uint32_t r[9];
 #pragma unroll
         for (int i = 0; i < 9; ++i) r[i] = ld32(p + 4 * i);
-        if ((j & 1) == 0) {
+        if constexpr ((j & 1) == 0) {
             d = h2f_bits(r[0]);
 #pragma unroll
             for (int k = 0; k < 8; ++k) W[k] = prmt(r[k], r[k + 1], 0x5432u);
@@ -138,7 +197,7 @@ __device__ __forceinline__ void blk_decode(const uint8_t* chunk, const int j, co
             for (int k = 0; k < 8; ++k) W[k] = r[k + 1];
         }
         m = 0.0f;
-    } else if constexpr (TYPE == MOE_Q4B) {
+    } else {  // Q4B: 20-byte blocks, always 4-aligned
         const uint8_t* p = chunk + 20 * j;
         const uint32_t dm = ld32(p);
         d = h2f_bits(dm);
@@ -149,38 +208,29 @@ __device__ __forceinline__ void blk_decode(const uint8_t* chunk, const int j, co
             W[k] = qs & 0x0f0f0f0fu;
             W[4 + k] = (qs >> 4) & 0x0f0f0f0fu;
         }
-    } else {  // NL4: weight bytes come out in the order [0, 2, 1, 3] of each word (the staged
-              // activation words are permuted the same way)
-        const int L = 18 * j;
-        const uint8_t* p = chunk + (L & ~3);
-        uint32_t r[5];
-#pragma unroll
-        for (int i = 0; i < 5; ++i) r[i] = ld32(p + 4 * i);
-        uint32_t qs[4];
-        if ((j & 1) == 0) {
-            d = h2f_bits(r[0]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) qs[k] = prmt(r[k], r[k + 1], 0x5432u);
-        } else {
-            d = h2f_bits(r[0] >> 16);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) qs[k] = r[k + 1];
-        }
-        m = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t Q = qs[k];
-            const uint32_t sl = (Q & 0x0707u) | ((Q >> 12) & 0x7070u);          // low codes & 7
-            const uint32_t sh = ((Q >> 4) & 0x0707u) | ((Q >> 16) & 0x7070u);   // high codes & 7
-            const uint32_t ml = prmt(Q << 4, 0u, 0xB9A8u);                      // low codes >= 8
-            const uint32_t mh = prmt(Q, 0u, 0xB9A8u);                           // high codes >= 8
-            W[k] = (prmt(tab[0], tab[1], sl) & ~ml) | (prmt(tab[2], tab[3], sl) & ml);
-            W[4 + k] = (prmt(tab[0], tab[1], sh) & ~mh) | (prmt(tab[2], tab[3], sh) & mh);
-        }
     }
 }
 
-// ---------------------------------------------------------------- shared staging
+// Block j of an NL4 chunk held in registers (36 words, 16-byte aligned chunk).
+template <int j>
+__device__ __forceinline__ void nl4_decode(const uint32_t raw[36], const uint32_t tab[4], uint32_t W[8], float& d) {
+    constexpr int L = 18 * j;
+    constexpr int i = L >> 2;
+    uint32_t qs[4];
+    if constexpr ((j & 1) == 0) {
+        d = h2f_bits(raw[i]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) qs[k] = prmt(raw[i + k], raw[i + k + 1], 0x5432u);
+    } else {
+        d = h2f_bits(raw[i] >> 16);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) qs[k] = raw[i + 1 + k];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) nl4_word(tab, qs[k], W[k], W[4 + k]);
+}
+
+// ---------------------------------------------------------------- work split
 
 struct Tile {
     int g, row0, nrows;
@@ -195,8 +245,8 @@ __device__ __forceinline__ Tile next_tile(long long& cur, long long end, int rbp
     return Tile{g, off * 8, static_cast<int>(n) * 8};
 }
 
-// Group g's expert and entry range; false if the group is skipped (invalid data reported once
-// by the calling thread when `report`, or simply empty).
+// Group g's expert and entry range; false if the group is skipped (invalid data reported by
+// the calling thread when `report`, or simply empty).
 __device__ __forceinline__ bool group_ok(const GemvArgs& a, int g, int& x, int& e0, int& e1, bool report) {
     x = a.grp_expert[g];
     e0 = a.grp_start[g];
@@ -217,58 +267,76 @@ __device__ __forceinline__ bool group_ok(const GemvArgs& a, int g, int& x, int& 
     return true;
 }
 
-// Producer (thread 0): find the next tile of a valid group in [cur, end) and start its copy
-// into ring slot `issued % stages`. Returns false when the range is exhausted.
-__device__ __forceinline__ bool produce(const GemvArgs& a, uint8_t* smem, uint64_t* bars, long long& cur,
-                                        long long end, int& issued) {
-    const int rbpg = a.rows >> 3;
-    while (cur < end) {
-        const Tile t = next_tile(cur, end, rbpg, a.RT >> 3);
-        int x, e0, e1;
-        if (!group_ok(a, t.g, x, e0, e1, false)) continue;
-        const int s = issued % a.stages;
-        const uint32_t bytes = static_cast<uint32_t>(t.nrows) * static_cast<uint32_t>(a.row_bytes);
-        const uint8_t* src = static_cast<const uint8_t*>(a.w[x]) + static_cast<size_t>(t.row0) * a.row_bytes;
-        mbar_arrive_expect_tx(&bars[s], bytes);
-        bulk_g2s(smem + static_cast<size_t>(s) * a.stage_bytes, src, bytes, &bars[s]);
-        ++issued;
-        return true;
+// Per-group facts cached in shared memory for the whole launch: expert, entry range, cost per
+// 8-row block (0 for a skipped group), and the inclusive prefix of the group costs.
+struct GroupInfo {
+    const uint8_t* ptr;
+    int x, e0, e1, cost;
+};
+
+// Flattened (group, 8-row block) index at which the cumulative cost reaches `target`
+// (binary search over the cost prefix cum[0..G]).
+__device__ __forceinline__ long long locate(const GroupInfo* gi, const long long* cum, int G, int rbpg,
+                                            long long target) {
+    if (target >= cum[G]) return static_cast<long long>(G) * rbpg;
+    int lo = 0, hi = G - 1;  // first g with cum[g+1] > target
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (cum[mid + 1] > target) hi = mid;
+        else lo = mid + 1;
     }
-    return false;
+    return static_cast<long long>(lo) * rbpg + (target - cum[lo]) / gi[lo].cost;
 }
 
-// The codebook in shared memory: CB3 256 x 32 lane replicas of 4 bytes, CB2 256 x 16 replicas of
-// 8 bytes, both in x-form and both 32 KB with entry idx at offset idx*128.
+// ---------------------------------------------------------------- shared staging
+
+// The codebook in shared memory at offset 0: CB3 256 x 32 lane replicas of 4 bytes, CB2 256 x 16
+// replicas of 8 bytes, both in x-form and both 32 KB with entry idx at offset idx*128.
 template <int TYPE>
-__device__ __forceinline__ void stage_codebook(const GemvArgs& a, uint8_t* smem, int tid, int NT) {
+__device__ __forceinline__ void stage_codebook(const GemvArgs& a, uint8_t* smem, int t, int nt) {
     if constexpr (Fmt<TYPE>::CB) {
-        uint8_t* cb = smem + a.off_cb;
+        // one 4-byte grid word per thread and iteration (all loads independent), converted to
+        // x-form bytewise and written to its 32 (CB3) or 16 (CB2, two words per entry) replicas
+        constexpr int kWords = TYPE == MOE_CB2 ? 512 : 256;
+        const uint32_t* cbw = reinterpret_cast<const uint32_t*>(a.codebook);
         bool even = false;
-        for (int i = tid; i < 256 * 8; i += NT) {
-            const int idx = i >> 3, part = i & 7;
-            uint32_t v[2];
+        for (int i = t; i < kWords; i += nt) {
+            const uint32_t g = __ldg(cbw + i);
+            even |= (g & 0x01010101u) != 0x01010101u;
+            uint32_t v = 0;
 #pragma unroll
-            for (int h = 0; h < (TYPE == MOE_CB2 ? 2 : 1); ++h) {
-                uint32_t w = 0;
-#pragma unroll
-                for (int bb = 0; bb < 4; ++bb) {
-                    const int g = a.codebook[idx * (TYPE == MOE_CB2 ? 8 : 4) + 4 * h + bb];
-                    even |= (g & 1) == 0;
-                    w |= (static_cast<uint32_t>((g - 1) >> 1) & 0xffu) << (8 * bb);
-                }
-                v[h] = w;
+            for (int bb = 0; bb < 4; ++bb) {
+                const int x = static_cast<int8_t>(g >> (8 * bb));
+                v |= (static_cast<uint32_t>((x - 1) >> 1) & 0xffu) << (8 * bb);
             }
-            uint4 u;
-            if constexpr (TYPE == MOE_CB2) u = make_uint4(v[0], v[1], v[0], v[1]);
-            else u = make_uint4(v[0], v[0], v[0], v[0]);
-            *reinterpret_cast<uint4*>(cb + idx * 128 + part * 16) = u;
+            if constexpr (TYPE == MOE_CB3) {
+                uint4* dst = reinterpret_cast<uint4*>(smem + i * 128);
+                const uint4 u = make_uint4(v, v, v, v);
+#pragma unroll
+                for (int part = 0; part < 8; ++part) dst[part] = u;
+            } else {  // word h of entry idx goes to bytes 4h..4h+3 of every 8-byte replica
+                const int idx = i >> 1, h = i & 1;
+                uint32_t* dst = reinterpret_cast<uint32_t*>(smem + idx * 128) + h;
+#pragma unroll
+                for (int rep = 0; rep < 16; ++rep) dst[2 * rep] = v;
+            }
         }
         if (even) set_err(a.err, MOE_ERR_CODEBOOK);
     }
 }
 
-// Entry bookkeeping for a batch of up to 4 entries (thread 0): misc[4+s] ok, [8+s] activation
-// row, [12+s] output row.
+template <int TYPE>
+__device__ __forceinline__ void load_table(const GemvArgs& a, uint32_t tab[4]) {
+    if constexpr (TYPE == MOE_NL4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tab[k] = __ldg(reinterpret_cast<const uint32_t*>(a.codebook) + k);
+    } else {
+        tab[0] = tab[1] = tab[2] = tab[3] = 0;
+    }
+}
+
+// Entry bookkeeping for a batch of up to 4 entries (one thread) in misc block `ent` (16 ints):
+// [4+s] ok, [8+s] activation row, [12+s] output row.
 __device__ __forceinline__ void setup_entries(const GemvArgs& a, int* misc, int b0, int ne) {
     for (int s = 0; s < kMaxEntriesPerPass; ++s) {
         int ok = 0, in = 0, o = 0;
@@ -285,12 +353,14 @@ __device__ __forceinline__ void setup_entries(const GemvArgs& a, int* misc, int 
     }
 }
 
+// q8_1 rows of `ne` entries -> codes as 16-byte halves, (d, aux) as float2: aux = exact code sum
+// (CB formats), s (Q4B) or 0.
 template <int TYPE>
-__device__ __forceinline__ void stage_act(const GemvArgs& a, uint8_t* smem, const int* misc, int ne, int tid, int NT) {
-    int4* q = reinterpret_cast<int4*>(smem + a.off_actq);
-    float* dx = reinterpret_cast<float*>(smem + a.off_dx);
-    int* aux = reinterpret_cast<int*>(smem + a.off_aux);
-    for (int i = tid; i < ne * a.nb; i += NT) {
+__device__ __forceinline__ void stage_act(const GemvArgs& a, uint8_t* smem, const int* misc, int ne, int t, int nt,
+                                          int buf = 0) {
+    int4* q = reinterpret_cast<int4*>(smem + a.off_actq) + buf * (kMaxEntriesPerPass * 2 * a.nbp);
+    float2* q2 = reinterpret_cast<float2*>(smem + a.off_act2) + buf * (kMaxEntriesPerPass * a.nb);
+    for (int i = t; i < ne * a.nb; i += nt) {
         const int s = i / a.nb, b = i - s * a.nb, bp = b + (b >> 3);
         uint32_t w[9];
         if (misc[4 + s]) {
@@ -307,231 +377,365 @@ __device__ __forceinline__ void stage_act(const GemvArgs& a, uint8_t* smem, cons
         }
         q[(s * 2 + 0) * a.nbp + bp] = make_int4(w[1], w[2], w[3], w[4]);
         q[(s * 2 + 1) * a.nbp + bp] = make_int4(w[5], w[6], w[7], w[8]);
-        dx[s * a.nb + b] = h2f_bits(w[0]);
+        float aux = 0.0f;
         if constexpr (Fmt<TYPE>::CB) {
             int S = 0;
 #pragma unroll
             for (int k = 1; k < 9; ++k) S = dp4a(w[k], 0x01010101u, S);
-            aux[s * a.nb + b] = S;
+            aux = __int_as_float(S);
         } else if constexpr (TYPE == MOE_Q4B) {
-            reinterpret_cast<float*>(aux)[s * a.nb + b] = h2f_bits(w[0] >> 16);
+            aux = h2f_bits(w[0] >> 16);
         }
+        q2[s * a.nb + b] = make_float2(h2f_bits(w[0]), aux);
     }
 }
 
-// ---------------------------------------------------------------- compute
-
 template <int NE>
 __device__ __forceinline__ void load_act(const GemvArgs& a, const uint8_t* smem, int b, uint32_t A[NE][8], float dx[NE],
-                                         int aux[NE]) {
-    const int4* q = reinterpret_cast<const int4*>(smem + a.off_actq);
-    const float* dxs = reinterpret_cast<const float*>(smem + a.off_dx);
-    const int* auxs = reinterpret_cast<const int*>(smem + a.off_aux);
+                                         float aux[NE], int buf = 0) {
+    const int4* q = reinterpret_cast<const int4*>(smem + a.off_actq) + buf * (kMaxEntriesPerPass * 2 * a.nbp);
+    const float2* q2 = reinterpret_cast<const float2*>(smem + a.off_act2) + buf * (kMaxEntriesPerPass * a.nb);
     const int bp = b + (b >> 3);
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
         const int4 lo = q[(e * 2 + 0) * a.nbp + bp], hi = q[(e * 2 + 1) * a.nbp + bp];
         A[e][0] = lo.x; A[e][1] = lo.y; A[e][2] = lo.z; A[e][3] = lo.w;
         A[e][4] = hi.x; A[e][5] = hi.y; A[e][6] = hi.z; A[e][7] = hi.w;
-        dx[e] = dxs[e * a.nb + b];
-        aux[e] = auxs[e * a.nb + b];
+        const float2 v = q2[e * a.nb + b];
+        dx[e] = v.x;
+        aux[e] = v.y;
     }
 }
 
-// Thread (c, q): chunk c of rows q*R .. q*R+R-1 of the tile; partials to part[(c*4+e)*RT + row].
+// ---------------------------------------------------------------- compute
+
+// ---------------------------------------------------------------- compute
+
+__device__ __forceinline__ int dot8(const uint32_t W[8], const uint32_t A[8]) {
+    int d = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) d = dp4a(W[w], A[w], d);
+    return d;
+}
+
+// One lane's row of chunk c (256 weights) against NE staged entries: chunk partials acc[e].
+// All lanes of a warp read the same activation block at the same time (broadcast loads).
+template <int TYPE, int NE, int j>
+__device__ __forceinline__ void cb_block(const GemvArgs& a, const uint8_t* smem, const CBRow<TYPE>& row, int c,
+                                         uint32_t loff, int buf, float acc[NE]) {
+    uint32_t A[NE][8];
+    float dx[NE], sq[NE];
+    load_act<NE>(a, smem, c * 8 + j, A, dx, sq, buf);
+    uint32_t W[8];
+    const int ls = cb_decode<TYPE, j>(row, smem, loff, W);
+#pragma unroll
+    for (int e = 0; e < NE; ++e) {
+        const int isum = 2 * dot8(W, A[e]) + __float_as_int(sq[e]);
+        acc[e] = fmaf(static_cast<float>(ls * isum), dx[e], acc[e]);
+    }
+}
+
+template <int TYPE, int NE, int j>
+__device__ __forceinline__ void plain_block(const GemvArgs& a, const uint8_t* smem, const uint8_t* chunk,
+                                            const uint32_t* raw, const uint32_t tab[4], int c, int buf, float acc[NE]) {
+    uint32_t A[NE][8];
+    float dx[NE], aux[NE];
+    load_act<NE>(a, smem, c * 8 + j, A, dx, aux, buf);
+    uint32_t W[8];
+    float dw, mw = 0.0f;
+    if constexpr (TYPE == MOE_NL4) nl4_decode<j>(raw, tab, W, dw);
+    else blk_decode_smem<TYPE, j>(chunk, W, dw, mw);
+#pragma unroll
+    for (int e = 0; e < NE; ++e) {
+        acc[e] = fmaf(__fmul_rn(dw, dx[e]), static_cast<float>(dot8(W, A[e])), acc[e]);
+        if constexpr (TYPE == MOE_Q4B) acc[e] = fmaf(mw, aux[e], acc[e]);
+    }
+}
+
 template <int TYPE, int NE>
-__device__ __forceinline__ void compute_tile(const GemvArgs& a, const uint8_t* tile, const uint8_t* smem, int c, int q,
-                                             int nrows, int lane, const uint32_t tab[4], float* part) {
-    constexpr int R = Fmt<TYPE>::R;
-    float acc[R][NE];
+__device__ __forceinline__ void lane_chunk(const GemvArgs& a, const uint8_t* smem, const uint8_t* tile, int row, int c,
+                                           uint32_t loff, const uint32_t tab[4], int buf, float acc[NE]) {
 #pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int e = 0; e < NE; ++e) acc[r][e] = 0.0f;
-
+    for (int e = 0; e < NE; ++e) acc[e] = 0.0f;
+    const uint8_t* chunk = tile + row * a.row_bytes + c * Fmt<TYPE>::CHUNK;
     if constexpr (Fmt<TYPE>::CB) {
-        CBRow<TYPE> rows[R];
-        float D[R];
+        CBRow<TYPE> rr;
+        rr.load(chunk);
+        const float D = rr.D();
+        cb_block<TYPE, NE, 0>(a, smem, rr, c, loff, buf, acc);
+        cb_block<TYPE, NE, 1>(a, smem, rr, c, loff, buf, acc);
+        cb_block<TYPE, NE, 2>(a, smem, rr, c, loff, buf, acc);
+        cb_block<TYPE, NE, 3>(a, smem, rr, c, loff, buf, acc);
+        cb_block<TYPE, NE, 4>(a, smem, rr, c, loff, buf, acc);
+        cb_block<TYPE, NE, 5>(a, smem, rr, c, loff, buf, acc);
+        cb_block<TYPE, NE, 6>(a, smem, rr, c, loff, buf, acc);
+        cb_block<TYPE, NE, 7>(a, smem, rr, c, loff, buf, acc);
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int row = q * R + r;
-            if (row < nrows) rows[r].load(tile + row * a.row_bytes + c * Fmt<TYPE>::CHUNK);
-            else rows[r].zero();
-            D[r] = rows[r].D();
-        }
-        const uint8_t* cbt = smem + a.off_cb + (TYPE == MOE_CB3 ? lane * 4 : (lane & 15) * 8);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            uint32_t A[NE][8];
-            float dx[NE];
-            int sq[NE];
-            load_act<NE>(a, smem, c * 8 + j, A, dx, sq);
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                uint32_t W[8];
-                const int ls = cb_decode<TYPE>(rows[r], j, cbt, W);
-#pragma unroll
-                for (int e = 0; e < NE; ++e) {
-                    int d = 0;
-#pragma unroll
-                    for (int w = 0; w < 8; ++w) d = dp4a(W[w], A[e][w], d);
-                    const int isum = 2 * d + sq[e];
-                    acc[r][e] = fmaf(static_cast<float>(ls * isum), dx[e], acc[r][e]);
-                }
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int e = 0; e < NE; ++e) acc[r][e] = __fmul_rn(D[r], acc[r][e]);
+        for (int e = 0; e < NE; ++e) acc[e] = __fmul_rn(D, acc[e]);
     } else {
-        const int row = q;  // R == 1
-        if (row < nrows) {
-            const uint8_t* chunk = tile + row * a.row_bytes + c * Fmt<TYPE>::CHUNK;
+        uint32_t raw[TYPE == MOE_NL4 ? 36 : 1];
+        if constexpr (TYPE == MOE_NL4) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                uint32_t A[NE][8];
-                float dx[NE];
-                int aux[NE];
-                load_act<NE>(a, smem, c * 8 + j, A, dx, aux);
-                uint32_t W[8];
-                float dw, mw;
-                blk_decode<TYPE>(chunk, j, tab, W, dw, mw);
-#pragma unroll
-                for (int e = 0; e < NE; ++e) {
-                    int d = 0;
-#pragma unroll
-                    for (int w = 0; w < 8; ++w) d = dp4a(W[w], A[e][w], d);
-                    acc[0][e] = fmaf(__fmul_rn(dw, dx[e]), static_cast<float>(d), acc[0][e]);
-                    if constexpr (TYPE == MOE_Q4B) acc[0][e] = fmaf(mw, __int_as_float(aux[e]), acc[0][e]);
-                }
+            for (int k = 0; k < 9; ++k) {
+                const uint4 v = *reinterpret_cast<const uint4*>(chunk + 16 * k);
+                raw[4 * k] = v.x; raw[4 * k + 1] = v.y; raw[4 * k + 2] = v.z; raw[4 * k + 3] = v.w;
             }
         }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const int row = q * R + r;
-        if (row < nrows) {
-#pragma unroll
-            for (int e = 0; e < NE; ++e) part[(c * kMaxEntriesPerPass + e) * a.RT + row] = acc[r][e];
-        }
+        plain_block<TYPE, NE, 0>(a, smem, chunk, raw, tab, c, buf, acc);
+        plain_block<TYPE, NE, 1>(a, smem, chunk, raw, tab, c, buf, acc);
+        plain_block<TYPE, NE, 2>(a, smem, chunk, raw, tab, c, buf, acc);
+        plain_block<TYPE, NE, 3>(a, smem, chunk, raw, tab, c, buf, acc);
+        plain_block<TYPE, NE, 4>(a, smem, chunk, raw, tab, c, buf, acc);
+        plain_block<TYPE, NE, 5>(a, smem, chunk, raw, tab, c, buf, acc);
+        plain_block<TYPE, NE, 6>(a, smem, chunk, raw, tab, c, buf, acc);
+        plain_block<TYPE, NE, 7>(a, smem, chunk, raw, tab, c, buf, acc);
     }
 }
 
-// Fixed-order sum over the chunks, written to the entries' output rows.
-__device__ __forceinline__ void reduce_write(const GemvArgs& a, const float* part, const int* misc, const Tile& t,
-                                             int ne, int tid, int NT) {
-    for (int i = tid; i < ne * t.nrows; i += NT) {
-        const int s = i / t.nrows, row = i - s * t.nrows;
-        if (!misc[4 + s]) continue;
-        float v = 0.0f;
-        for (int c = 0; c < a.nch; ++c) v = __fadd_rn(v, part[(c * kMaxEntriesPerPass + s) * a.RT + row]);
-        a.out[static_cast<int64_t>(misc[12 + s]) * a.out_stride + t.row0 + row] = v;
+// The warp's chunks (c = wi, wi + WPS, ...) of the tile's rows (lane = row) -> chunk partials
+// part[(c*4 + e)*RT + row].
+template <int TYPE, int NE>
+__device__ __forceinline__ void warp_chunks(const GemvArgs& a, const uint8_t* smem, const uint8_t* tile, float* part,
+                                            int wi, int lane, uint32_t loff, const uint32_t tab[4], int buf) {
+    for (int c = wi; c < a.nch; c += a.WPS) {
+        float acc[NE];
+        lane_chunk<TYPE, NE>(a, smem, tile, lane, c, loff, tab, buf, acc);
+#pragma unroll
+        for (int e = 0; e < NE; ++e) part[(c * kMaxEntriesPerPass + e) * a.RT + lane] = acc[e];
     }
 }
 
 template <int TYPE>
-__device__ __forceinline__ void load_table(const GemvArgs& a, uint32_t tab[4]) {
-    if constexpr (TYPE == MOE_NL4) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            uint32_t w = 0;
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb) w |= (static_cast<uint32_t>(a.codebook[4 * k + bb]) & 0xffu) << (8 * bb);
-            tab[k] = w;
-        }
-    } else {
-        tab[0] = tab[1] = tab[2] = tab[3] = 0;
+__device__ __forceinline__ void compute_batch(const GemvArgs& a, const uint8_t* smem, const uint8_t* tile, float* part,
+                                              int ne, int wi, int lane, int nrows, uint32_t loff, const uint32_t tab[4],
+                                              int buf) {
+    if (lane >= nrows) return;
+    // batches of 3 entries run the 4-entry code; the fourth result is never read
+    if (ne == 1) warp_chunks<TYPE, 1>(a, smem, tile, part, wi, lane, loff, tab, buf);
+    else if (ne == 2) warp_chunks<TYPE, 2>(a, smem, tile, part, wi, lane, loff, tab, buf);
+    else warp_chunks<TYPE, 4>(a, smem, tile, part, wi, lane, loff, tab, buf);
+}
+
+// Fixed-order sum over the chunks (c = 0 .. nch-1) of each (row, entry), written to the entry's
+// output row.
+__device__ __forceinline__ void reduce_write(const GemvArgs& a, const float* part, const int* ment, const Tile& t,
+                                             int ne, int lane) {
+    if (lane >= t.nrows) return;
+    for (int e = 0; e < ne; ++e) {
+        if (!ment[4 + e]) continue;
+        float s = part[e * a.RT + lane];
+        for (int c = 1; c < a.nch; ++c) s = __fadd_rn(s, part[(c * kMaxEntriesPerPass + e) * a.RT + lane]);
+        a.out[static_cast<int64_t>(ment[12 + e]) * a.out_stride + t.row0 + lane] = s;
     }
 }
 
 template <int TYPE>
-__global__ void __launch_bounds__(Fmt<TYPE>::MAXT, 1) gemv_kernel(const GemvArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int tid = threadIdx.x, NT = blockDim.x, lane = tid & 31;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.off_bar);
+__global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NT = blockDim.x;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.off_bar);
+    uint64_t* empty = full + a.stages;
+    // misc: [0] tiles issued, [1] abort flag, [32..47] / [48..63] entry blocks of act buffers 0 / 1,
+    // [64 + s] arrivals at ring slot s (the last warp of a tile sums its chunk partials)
     int* misc = reinterpret_cast<int*>(smem + a.off_misc);
-    float* part = reinterpret_cast<float*>(smem + a.off_part);
+    GroupInfo* gi = reinterpret_cast<GroupInfo*>(smem + a.off_grp);
+    long long* cum = reinterpret_cast<long long*>(gi + a.cap_groups);
+    const int S = a.stages;
+    const int rbpg = a.rows >> 3, rt8 = a.RT >> 3;
 
-    if (tid < a.stages) mbar_init(&bars[tid], 1);
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], a.WPS + 1);
+            misc[64 + s] = 0;
+        }
+        misc[0] = 0;
+        misc[1] = 0;
+    }
     fence_barrier_init();
-    __syncthreads();
-
+    // static data first (before the dependency wait): the codebook replicas and the NL4 table
+    if (warp > 0) stage_codebook<TYPE>(a, smem, tid - 32, NT - 32);
+    uint32_t tab[4];
+    load_table<TYPE>(a, tab);
     if (!a.prefetch_before_wait) pdl_wait();
     int G = *a.n_groups;
     if (G < 0 || G > a.cap_groups) {
         if (blockIdx.x == 0 && tid == 0) set_err(a.err, MOE_ERR_NGROUPS);
         G = G < 0 ? 0 : a.cap_groups;
     }
-    const int rbpg = a.rows >> 3;
-    const long long total = static_cast<long long>(G) * rbpg;
-    const long long rb0 = total * blockIdx.x / gridDim.x, rb1 = total * (blockIdx.x + 1) / gridDim.x;
+    // the group table, one group per thread, then the prefix of the costs (warp 0)
+    for (int g = tid; g < G; g += NT) {
+        int x, e0, e1;
+        const bool ok = group_ok(a, g, x, e0, e1, blockIdx.x == 0);
+        gi[g] = GroupInfo{ok ? static_cast<const uint8_t*>(a.w[x]) : nullptr, x, e0, e1, ok ? a.alpha + (e1 - e0) : 0};
+    }
+    __syncthreads();
+    if (warp == 0) {
+        long long run = 0;
+        if (lane == 0) cum[0] = 0;
+        for (int base = 0; base < G; base += 32) {
+            const int g = base + lane;
+            long long v = g < G ? static_cast<long long>(gi[g].cost) * rbpg : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long y = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += y;
+            }
+            if (g < G) cum[g + 1] = run + v;
+            run += __shfl_sync(0xffffffffu, v, 31);
+        }
+    }
+    __syncthreads();
+    const long long tot = cum[G];
+    const long long rb0 = locate(gi, cum, G, rbpg, tot * blockIdx.x / gridDim.x);
+    const long long rb1 = locate(gi, cum, G, rbpg, tot * (blockIdx.x + 1) / gridDim.x);
 
+    // producer: the first S tiles may start before the dependency wait (down kernel)
     long long pcur = rb0;
     int issued = 0;
+    auto produce_one = [&](bool wait_empty) -> int {  // 1 issued, 0 range exhausted, -1 timeout
+        while (pcur < rb1) {
+            const Tile t = next_tile(pcur, rb1, rbpg, rt8);
+            const GroupInfo g = gi[t.g];
+            if (g.cost == 0) continue;
+            const int s = issued % S;
+            if (wait_empty && issued >= S) {
+                if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>(issued / S - 1) & 1u)) return -1;
+            }
+            const uint32_t bytes = static_cast<uint32_t>(t.nrows) * static_cast<uint32_t>(a.row_bytes);
+            mbar_arrive_expect_tx(&full[s], bytes);
+            bulk_g2s(smem + a.off_ring + static_cast<size_t>(s) * a.stage_bytes,
+                     g.ptr + static_cast<size_t>(t.row0) * a.row_bytes, bytes, &full[s]);
+            ++issued;
+            *reinterpret_cast<volatile int*>(misc) = issued;
+            return 1;
+        }
+        return 0;
+    };
     if (tid == 0)
-        for (int s = 0; s < a.stages; ++s)
-            if (!produce(a, smem, bars, pcur, rb1, issued)) break;
+        for (int s = 0; s < S; ++s)
+            if (produce_one(false) != 1) break;
     if (a.prefetch_before_wait) pdl_wait();
     pdl_trigger();
     if (rb0 == rb1) return;
 
-    stage_codebook<TYPE>(a, smem, tid, NT);
-    uint32_t tab[4];
-    load_table<TYPE>(a, tab);
+    if (warp == 0) {
+        if (lane == 0) {
+            for (;;) {
+                if (*reinterpret_cast<volatile int*>(misc + 1)) break;
+                const int rc = produce_one(true);
+                if (rc == 0) break;
+                if (rc < 0) {
+                    set_err(a.err, MOE_ERR_TIMEOUT);
+                    *reinterpret_cast<volatile int*>(misc + 1) = 1;
+                    break;
+                }
+            }
+        }
+        return;
+    }
 
-    const int c = tid / a.QR, q = tid - (tid / a.QR) * a.QR;
-    const bool active = c < a.nch;
+    // consumers: warp-set `set` takes the CTA's tiles set, set + TP, ...; within a set, warp wi
+    // takes chunks wi, wi + WPS, ... of every row of the tile (lane = row)
+    const int cw = warp - 1;
+    const int set = cw / a.WPS, wi = cw - set * a.WPS;
+    const int ct = tid - 32, cnt = a.CW * 32;
+    const uint32_t loff = TYPE == MOE_CB3 ? lane * 4u : (lane & 15u) * 8u;
+
+    // A range spanning at most two groups of at most 4 entries each (the common case) has both
+    // groups' activations staged once, here, and every warp-set runs freely; otherwise warp-set 0
+    // alone walks the range and restages at every group (or 4-entry batch) change.
+    const int gA = static_cast<int>(rb0 / rbpg), gB = static_cast<int>((rb1 - 1) / rbpg);
+    const int neA = gi[gA].e1 - gi[gA].e0, neB = gi[gB].e1 - gi[gB].e0;
+    const bool fast = gB - gA <= 1 && (gi[gA].cost == 0 || neA <= kMaxEntriesPerPass) &&
+                      (gi[gB].cost == 0 || neB <= kMaxEntriesPerPass);
+    if (fast) {
+        if (ct == 0) {
+            if (gi[gA].cost) setup_entries(a, misc + 32, gi[gA].e0, neA);
+            if (gB != gA && gi[gB].cost) setup_entries(a, misc + 48, gi[gB].e0, neB);
+        }
+        named_sync(1, cnt);
+        if (gi[gA].cost) stage_act<TYPE>(a, smem, misc + 32, neA, ct, cnt, 0);
+        if (gB != gA && gi[gB].cost) stage_act<TYPE>(a, smem, misc + 48, neB, ct, cnt, 1);
+        named_sync(1, cnt);
+    } else if (set != 0) {
+        return;
+    }
+    const int TPe = fast ? a.TP : 1;
+    const int scnt = a.WPS * 32, st = ct - set * scnt;  // thread index within the set
+
     long long ccur = rb0;
     int k = 0, cur_g = -1, cur_b0 = -1;
+    bool aborted = false;
     while (ccur < rb1) {
-        const Tile t = next_tile(ccur, rb1, rbpg, a.RT >> 3);
-        int x, e0, e1;
-        if (!group_ok(a, t.g, x, e0, e1, tid == 0)) continue;
-        const int slot = k % a.stages;
-        const uint32_t parity = static_cast<uint32_t>(k / a.stages) & 1u;
-        const uint8_t* tile = smem + static_cast<size_t>(slot) * a.stage_bytes;
-        bool waited = false;
-        for (int b0 = e0; b0 < e1; b0 += kMaxEntriesPerPass) {
-            const int ne = e1 - b0 < kMaxEntriesPerPass ? e1 - b0 : kMaxEntriesPerPass;
-            if (t.g != cur_g || b0 != cur_b0) {
-                __syncthreads();
-                if (tid == 0) setup_entries(a, misc, b0, ne);
-                __syncthreads();
-                stage_act<TYPE>(a, smem, misc, ne, tid, NT);
+        const Tile t = next_tile(ccur, rb1, rbpg, rt8);
+        const GroupInfo g = gi[t.g];
+        if (g.cost == 0) continue;
+        const int kk = k++;
+        if (kk % TPe != set) continue;
+        const int slot = kk % S;
+        const uint32_t parity = static_cast<uint32_t>(kk / S) & 1u;
+        const uint8_t* tile = smem + a.off_ring + static_cast<size_t>(slot) * a.stage_bytes;
+        float* part = reinterpret_cast<float*>(smem + a.off_part + static_cast<size_t>(slot) * a.part_bytes);
+        if (!aborted && !mbar_wait_bounded(&full[slot], parity)) {
+            aborted = true;
+            set_err(a.err, MOE_ERR_TIMEOUT);
+            *reinterpret_cast<volatile int*>(misc + 1) = 1;
+        }
+        if (*reinterpret_cast<volatile int*>(misc + 1)) aborted = true;
+        // entry batches: one for a group of up to 4 entries (always in fast mode)
+        for (int b0 = g.e0; b0 < g.e1; b0 += kMaxEntriesPerPass) {
+            const int ne = g.e1 - b0 < kMaxEntriesPerPass ? g.e1 - b0 : kMaxEntriesPerPass;
+            const int buf = fast && t.g != gA ? 1 : 0;
+            const int* ment = misc + 32 + 16 * buf;
+            if (!fast && (t.g != cur_g || b0 != cur_b0)) {
+                named_sync(1, scnt);
+                if (st == 0) setup_entries(a, misc + 32, b0, ne);
+                named_sync(1, scnt);
+                stage_act<TYPE>(a, smem, misc + 32, ne, st, scnt, 0);
+                named_sync(1, scnt);
                 cur_g = t.g;
                 cur_b0 = b0;
             }
-            bool late = false;
-            if (!waited) {
-                late = !mbar_wait_bounded(&bars[slot], parity);
-                waited = true;
-            }
-            if (__syncthreads_or(late)) {
-                // a staged tile never arrived: report, wait (bounded) for the copies still in
-                // flight into this CTA's shared memory, and leave
-                if (tid == 0) {
-                    set_err(a.err, MOE_ERR_TIMEOUT);
-                    for (int kk = k; kk < issued; ++kk)
-                        mbar_wait_bounded(&bars[kk % a.stages], static_cast<uint32_t>(kk / a.stages) & 1u);
+            if (!aborted) compute_batch<TYPE>(a, smem, tile, part, ne, wi, lane, t.nrows, loff, tab, buf);
+            if (fast) {
+                // release the weights, then the set's last warp sums the chunk partials
+                __syncwarp();
+                __threadfence_block();
+                int last = 0;
+                if (lane == 0) {
+                    mbar_arrive(&empty[slot]);
+                    last = atomicAdd(&misc[64 + slot], 1) == a.WPS - 1;
                 }
-                __syncthreads();
-                return;
-            }
-            if (active) {
-                switch (ne) {
-                case 1: compute_tile<TYPE, 1>(a, tile, smem, c, q, t.nrows, lane, tab, part); break;
-                case 2: compute_tile<TYPE, 2>(a, tile, smem, c, q, t.nrows, lane, tab, part); break;
-                case 3: compute_tile<TYPE, 3>(a, tile, smem, c, q, t.nrows, lane, tab, part); break;
-                default: compute_tile<TYPE, 4>(a, tile, smem, c, q, t.nrows, lane, tab, part); break;
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence_block();
+                    if (!aborted) reduce_write(a, part, ment, t, ne, lane);
+                    __syncwarp();
+                    if (lane == 0) {
+                        misc[64 + slot] = 0;
+                        mbar_arrive(&empty[slot]);
+                    }
                 }
+            } else {
+                named_sync(1, scnt);
+                if (wi == 0 && !aborted) reduce_write(a, part, ment, t, ne, lane);
+                named_sync(1, scnt);
             }
-            __syncthreads();
-            reduce_write(a, part, misc, t, ne, tid, NT);
         }
-        __syncthreads();
-        if (tid == 0) produce(a, smem, bars, pcur, rb1, issued);
-        ++k;
+        if (!fast) {
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&empty[slot]);
+                if (wi == 0) mbar_arrive(&empty[slot]);
+            }
+        }
+    }
+    if (aborted && ct == 0) {
+        // wait (bounded) for the copies still in flight into this CTA's shared memory
+        const int n = *reinterpret_cast<volatile int*>(misc);
+        for (int q = n - S > 0 ? n - S : 0; q < n; ++q)
+            mbar_wait_bounded(&full[q % S], static_cast<uint32_t>(q / S) & 1u);
     }
 }
 
@@ -539,7 +743,7 @@ __global__ void __launch_bounds__(Fmt<TYPE>::MAXT, 1) gemv_kernel(const GemvArgs
 // and dot-product code (one thread per (row, chunk), the blob read straight from global memory).
 template <int TYPE>
 __global__ void __launch_bounds__(256) isum_kernel(const GemvArgs a, const uint8_t* blob, int rows, int32_t* isum) {
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, NT = blockDim.x, lane = tid & 31;
     int* misc = reinterpret_cast<int*>(smem + a.off_misc);
     if (tid == 0) {
@@ -556,38 +760,62 @@ __global__ void __launch_bounds__(256) isum_kernel(const GemvArgs a, const uint8
     if (i >= rows * a.nch) return;
     const int r = i / a.nch, c = i - r * a.nch;
     const uint8_t* chunk = blob + static_cast<size_t>(r) * a.row_bytes + c * Fmt<TYPE>::CHUNK;
-#pragma unroll 1
-    for (int j = 0; j < 8; ++j) {
-        uint32_t A[1][8];
-        float dx[1];
-        int aux[1];
-        load_act<1>(a, smem, c * 8 + j, A, dx, aux);
-        uint32_t W[8];
-        int v;
-        if constexpr (Fmt<TYPE>::CB) {
-            CBRow<TYPE> row;
-            row.load(chunk);
-            cb_decode<TYPE>(row, j, smem + a.off_cb + (TYPE == MOE_CB3 ? lane * 4 : (lane & 15) * 8), W);
+    const uint32_t loff = TYPE == MOE_CB3 ? lane * 4u : (lane & 15u) * 8u;
+    int32_t out[8];
+    if constexpr (Fmt<TYPE>::CB) {
+        CBRow<TYPE> row;
+        row.load(chunk);
+        auto one = [&](auto jc) {
+            constexpr int j = decltype(jc)::value;
+            uint32_t A[1][8];
+            float dx[1], aux[1];
+            load_act<1>(a, smem, c * 8 + j, A, dx, aux);
+            uint32_t W[8];
+            cb_decode<TYPE, j>(row, smem, loff, W);
             int d = 0;
 #pragma unroll
             for (int w = 0; w < 8; ++w) d = dp4a(W[w], A[0][w], d);
-            v = 2 * d + aux[0];
-        } else {
-            float dw, mw;
-            blk_decode<TYPE>(chunk, j, tab, W, dw, mw);
-            int d = 0;
+            out[j] = 2 * d + __float_as_int(aux[0]);
+        };
+        one(std::integral_constant<int, 0>{}); one(std::integral_constant<int, 1>{});
+        one(std::integral_constant<int, 2>{}); one(std::integral_constant<int, 3>{});
+        one(std::integral_constant<int, 4>{}); one(std::integral_constant<int, 5>{});
+        one(std::integral_constant<int, 6>{}); one(std::integral_constant<int, 7>{});
+    } else {
+        uint32_t raw[36];
+        if constexpr (TYPE == MOE_NL4) {
 #pragma unroll
-            for (int w = 0; w < 8; ++w) d = dp4a(W[w], A[0][w], d);
-            v = d;
+            for (int k = 0; k < 36; ++k) raw[k] = ld32(chunk + 4 * k);
         }
-        isum[static_cast<size_t>(r) * a.nb + c * 8 + j] = v;
+        auto one = [&](auto jc) {
+            constexpr int j = decltype(jc)::value;
+            uint32_t A[1][8];
+            float dx[1], aux[1];
+            load_act<1>(a, smem, c * 8 + j, A, dx, aux);
+            uint32_t W[8];
+            float dw, mw;
+            if constexpr (TYPE == MOE_NL4) nl4_decode<j>(raw, tab, W, dw);
+            else blk_decode_smem<TYPE, j>(chunk, W, dw, mw);
+            int d = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) d = dp4a(W[w], A[0][w], d);
+            out[j] = d;
+        };
+        one(std::integral_constant<int, 0>{}); one(std::integral_constant<int, 1>{});
+        one(std::integral_constant<int, 2>{}); one(std::integral_constant<int, 3>{});
+        one(std::integral_constant<int, 4>{}); one(std::integral_constant<int, 5>{});
+        one(std::integral_constant<int, 6>{}); one(std::integral_constant<int, 7>{});
     }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) isum[static_cast<size_t>(r) * a.nb + c * 8 + j] = out[j];
 }
 
 // ---------------------------------------------------------------- per-format entry points
 
 template <int TYPE>
-cudaError_t launch_gemv_t(const GemvArgs& a, int grid, int NT, int smem, cudaStream_t s, bool pdl) {
+cudaError_t launch_gemv_t(const GemvArgs& args, int grid, int NT, int smem, cudaStream_t s, bool pdl) {
+    GemvArgs a = args;
+    a.alpha = Fmt<TYPE>::ALPHA;
     cudaError_t e = cudaFuncSetAttribute(gemv_kernel<TYPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_kernel(gemv_kernel<TYPE>, dim3(grid), dim3(NT), static_cast<size_t>(smem), s, pdl, a);
@@ -613,17 +841,13 @@ cudaError_t launch_isum_t(const int8_t* codebook, int K, const void* blob, int r
     a.act = xq;
     a.n_act_rows = 1;
     a.out_rows = 1;
-    int off = 0;
-    a.off_cb = off;
-    off += Fmt<TYPE>::CB ? 32768 : 0;
+    int off = Fmt<TYPE>::CB ? 32768 : 0;  // codebook at offset 0
     a.off_actq = off;
     off += 2 * a.nbp * 16;
-    a.off_dx = off;
-    off += a.nb * 4;
-    a.off_aux = off;
-    off += a.nb * 4;
+    a.off_act2 = off;
+    off += a.nb * 8;
     a.off_misc = off;
-    off += 64;
+    off += 128;
     cudaError_t e = cudaFuncSetAttribute(isum_kernel<TYPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, off);
     if (e != cudaSuccess) return e;
     const int n = rows * a.nch;

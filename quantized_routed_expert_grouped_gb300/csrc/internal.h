@@ -31,14 +31,18 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 struct GemvArgs {
     const void* const* w;  // [n_experts] blob pointers
     int n_experts;
-    int K;          // weights per row
-    int rows;       // rows per expert
-    int row_bytes;  // bytes per row
-    int nch;        // 256-weight chunks per row
-    int QR;         // row groups per tile (threads per chunk column)
-    int RT;         // maximum rows per tile (QR * rows per thread)
-    int stages;     // staging ring depth
+    int K;            // weights per row
+    int rows;         // rows per expert
+    int row_bytes;    // bytes per row
+    int nch;          // 256-weight chunks per row
+    int CPW;          // chunks per consumer warp and tile
+    int WPS;          // consumer warps per warp-set (one tile per set at a time) = ceil(nch / CPW)
+    int TP;           // warp-sets per CTA (tiles in flight in compute)
+    int CW;           // consumer warps per CTA = WPS * TP (plus one producer warp)
+    int RT;           // rows per tile (32, or 16 for very long rows): lane = row
+    int stages;       // staging ring depth
     int stage_bytes;  // bytes per ring slot (tile + slack, multiple of 128)
+    int alpha;        // decode cost of a row relative to one entry's dot products (balancing)
     const int32_t* grp_expert;
     const int32_t* grp_start;
     const int32_t* n_groups;
@@ -54,14 +58,16 @@ struct GemvArgs {
     int32_t* err;
     const int8_t* codebook;
     int prefetch_before_wait;  // weight tiles may be requested before griddepcontrol.wait
-    // dynamic shared-memory layout (byte offsets)
-    int off_bar, off_actq, off_dx, off_aux, off_part, off_cb, off_misc;
+    // dynamic shared-memory layout (byte offsets; a CB codebook, when present, is at offset 0;
+    // two activation buffers of kMaxEntriesPerPass entries; the group table holds cap_groups)
+    int off_ring, off_part, off_actq, off_act2, off_bar, off_misc, off_grp;
+    int part_bytes;  // per-slot partial sums: nch x 4 entries x RT floats
     int nb;   // activation blocks per row (K/32)
     int nbp;  // padded block slots per activation half-row
 };
 
 struct GemvPlan {
-    int R, QR, RT, NT, stages, stage_bytes, smem, ctas_per_sm;
+    int NT, smem;
 };
 
 cudaError_t launch_quantize_q8_1(const float* x, int64_t rows, int64_t cols, moe_q8_1* xq, cudaStream_t s,
