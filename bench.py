@@ -6,6 +6,12 @@ synthetic bytes), window sizes T = 1, 2, 3, 4. Per layer the graph runs the whol
 routing/grouping, activation q8_1, grouped gate/up, fused SwiGLU + q8_1, grouped down, chained
 with programmatic dependent launch; every kernel waits for the previous layer before reading.
 
+The gate/up pool is held in the CB3X slot layout, transcoded once at load time from the CB3 pool
+(the same integers; load-time re-encoding as in #3455 "GP100 (sm_60): 4-bit slots for resident
+IQ2_S / IQ3_XXS / IQ3_S gate/up experts"); the native-layout window (CB3 read directly) is timed
+too and reported in "native_layout". Bandwidth figures count the CB3 format's bytes (algorithmic
+bytes); the slot layout streams 4/3 of that for gate/up.
+
 One step = one launch of each of the four window graphs (T = 1..4). value = mean microseconds
 per window over the four T (lower is better); per-T microseconds and weight-stream bandwidth are
 in "per_T". Every window reads >= 1 GB of weights, far more than L2 (129 MB), so no flush is
@@ -34,6 +40,7 @@ import synth  # noqa: E402
 
 WL = synth.WORKLOADS["window48"]
 GU_T, DN_T = WL.pairs[0]
+XT = synth.CB3X  # slot layout the gate/up pool is transcoded to at load
 TS = (1, 2, 3, 4)
 METRIC = "us_per_verify_window_48L"
 
@@ -105,7 +112,7 @@ class Clocks:
 class Window:
     """Device state of one T: inputs, routing outputs, scratch and the captured 48-layer graph."""
 
-    def __init__(self, m, T, tab_gu, tab_dn, cb_gu, cb_dn, dev):
+    def __init__(self, m, T, tab_gu, tab_dn, cb_gu, cb_dn, dev, gu_type=GU_T):
         self.T = T
         L, n = WL.layers, T * WL.k
         i32 = dict(dtype=torch.int32, device=dev)
@@ -124,7 +131,8 @@ class Window:
         self.hq = torch.zeros((n, WL.F // 32, 36), dtype=torch.uint8, device=dev)
         self.out = torch.zeros((L, n, WL.N), dtype=torch.float32, device=dev)
         self.err = torch.zeros(1, **i32)
-        self.calls = [m.ExpertCall(GU_T, cb_gu, DN_T, cb_dn, WL.N, WL.F, tab_gu[l], tab_dn[l], WL.E, self.ge[l],
+        self.gu_type = gu_type
+        self.calls = [m.ExpertCall(gu_type, cb_gu, DN_T, cb_dn, WL.N, WL.F, tab_gu[l], tab_dn[l], WL.E, self.ge[l],
                                    self.gs[l], self.ng[l], n, 0, n, self.xq[l], self.es[l], self.ed[l], self.gu,
                                    self.hq, self.out[l], self.err, m.F_PDL) for l in range(L)]
         self.m = m
@@ -174,14 +182,26 @@ def run_ours(args, rank, world):
     tab_dn = [tab(pool_dn, l) for l in range(WL.layers)]
     cb_gu = torch.from_numpy(synth.codebook(GU_T, WL.seed * 7 + 1).ravel().copy()).to(dev)
     cb_dn = torch.from_numpy(synth.codebook(DN_T, WL.seed * 7 + 2).ravel().copy()).to(dev)
+    # load-time transcoding of the gate/up pool into the slot layout
+    xb = synth.blob_bytes(XT, 2 * WL.F, WL.N)
+    pool_gx = torch.empty((WL.layers, WL.E, xb), dtype=torch.uint8, device=dev)
+    tab_gx = [tab(pool_gx, l) for l in range(WL.layers)]
+    terr = torch.zeros(1, dtype=torch.int32, device=dev)
+    for l in range(WL.layers):
+        m.transcode_cb(GU_T, cb_gu, XT, WL.N, 2 * WL.F, tab_gu[l], tab_gx[l], terr)
+    torch.cuda.synchronize()
+    if int(terr.item()):
+        raise RuntimeError(f"transcoding error bits {int(terr.item())}")
     setup_s = time.time() - t0
 
-    wins = {T: Window(m, T, tab_gu, tab_dn, cb_gu, cb_dn, dev) for T in TS}
-    for w in wins.values():
+    wins = {T: Window(m, T, tab_gx, tab_dn, None, cb_dn, dev, gu_type=XT) for T in TS}
+    natv = {T: Window(m, T, tab_gu, tab_dn, cb_gu, cb_dn, dev) for T in TS}
+    for w in list(wins.values()) + list(natv.values()):
         w.capture()
     torch.cuda.synchronize()
-    if int(wins[1].err.item()):
-        raise RuntimeError(f"device error bits {int(wins[1].err.item())}")
+    for w in list(wins.values()) + list(natv.values()):
+        if int(w.err.item()):
+            raise RuntimeError(f"device error bits {int(w.err.item())}")
 
     s = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -223,6 +243,26 @@ def run_ours(args, rank, world):
                       "frac_of_measured_hbm": round(bytes_t[T][0] / (us_t[T] * 1e-6) / 1e9 / hbm_peak, 4),
                       "groups_per_layer": round(float(np.mean(bytes_t[T][2])), 2)} for T in TS}
 
+    # ---- the native layout (CB3 read directly), timed the same way after the headline run
+    nat_t = {T: [] for T in TS}
+    for _ in range(args.warmup):
+        for T in TS:
+            natv[T].graph.replay()
+    for _ in range(args.steps):
+        for T in TS:
+            a, b = ev(), ev()
+            a.record(s)
+            natv[T].graph.replay()
+            b.record(s)
+            nat_t[T].append((a, b))
+    torch.cuda.synchronize()
+    native = {str(T): {"us": round(float(np.median([a.elapsed_time(b) * 1e3 for a, b in nat_t[T]])), 2)}
+              for T in TS}
+    for T in TS:
+        us = native[str(T)]["us"]
+        native[str(T)]["GBps"] = round(bytes_t[T][0] / (us * 1e-6) / 1e9, 1)
+        native[str(T)]["frac_of_measured_hbm"] = round(bytes_t[T][0] / (us * 1e-6) / 1e9 / hbm_peak, 4)
+
     # ---- dominant kernel (grouped gate/up) timed on its own, T = 4, all 48 layers per launch set
     roof = gate_up_roofline(m, wins[4], bytes_t[4], hbm_peak, peak_kind, s)
 
@@ -236,9 +276,11 @@ def run_ours(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "int8 dp4a + fp32", "data": "synthetic",
         "config": {"workload": "window48: 48 layers x 128 experts, top-8, n_embd 2560, n_ff 768, CB3 gate/up + "
                                "NL4 down (16.4 GB pool), T=1..4, one CUDA graph per T",
+                   "layout": "gate/up held as CB3X slots (CB3 transcoded at load, same integers); down NL4",
                    "l2": "inputs larger than L2 (>= 1 GB of weights per window), no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "per_T": per_T, "roofline": roof, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+        "per_T": per_T, "native_layout": {"gate_up": "CB3 (read directly)", "per_T": native},
+        "roofline": roof, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
         "setup_s": round(setup_s, 1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -250,24 +292,27 @@ def gate_up_roofline(m, w, bytes_t, hbm_peak, peak_kind, s):
     """The grouped gate/up kernel launched alone for the 48 layers of the T = 4 window (inputs
     already routed and quantized), CUDA events on the launching stream."""
     for l in range(WL.layers):
-        m.grouped_gu(GU_T, w.calls[l]._keep[0], WL.N, WL.F, w.calls[l]._keep[2], WL.E, w.ge[l], w.gs[l], w.ng[l],
-                     w.T * WL.k, 0, w.xq[l], w.es[l], w.T * WL.k, w.gu, w.err, stream=s)
+        m.grouped_gu(w.gu_type, w.calls[l]._keep[0], WL.N, WL.F, w.calls[l]._keep[2], WL.E, w.ge[l], w.gs[l],
+                     w.ng[l], w.T * WL.k, 0, w.xq[l], w.es[l], w.T * WL.k, w.gu, w.err, stream=s)
     torch.cuda.synchronize()
     reps = 5
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(s)
     for _ in range(reps):
         for l in range(WL.layers):
-            m.grouped_gu(GU_T, w.calls[l]._keep[0], WL.N, WL.F, w.calls[l]._keep[2], WL.E, w.ge[l], w.gs[l],
+            m.grouped_gu(w.gu_type, w.calls[l]._keep[0], WL.N, WL.F, w.calls[l]._keep[2], WL.E, w.ge[l], w.gs[l],
                          w.ng[l], w.T * WL.k, 0, w.xq[l], w.es[l], w.T * WL.k, w.gu, w.err, stream=s)
     b.record(s)
     torch.cuda.synchronize()
     dur_s = a.elapsed_time(b) * 1e-3 / (reps * WL.layers)
     per_launch = bytes_t[1] / WL.layers
     ach = per_launch / dur_s / 1e9
-    return {"kernel": "grouped gate/up (CB3, T=4)", "bound": "hbm", "achieved": round(ach, 1),
-            "peak": hbm_peak, "unit": "GB/s", "frac": round(ach / hbm_peak, 4), "traffic": None,
-            "peak_kind": peak_kind, "bytes_per_launch": int(per_launch), "us_per_launch": round(dur_s * 1e6, 2)}
+    streamed = per_launch * synth.blob_bytes(w.gu_type, 2 * WL.F, WL.N) / synth.blob_bytes(GU_T, 2 * WL.F, WL.N)
+    return {"kernel": f"grouped gate/up ({synth.NAMES[w.gu_type]} slots of CB3, T=4)", "bound": "hbm",
+            "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
+            "traffic": None, "peak_kind": peak_kind, "bytes_per_launch": int(per_launch),
+            "streamed_bytes_per_launch": int(streamed), "streamed_GBps": round(streamed / dur_s / 1e9, 1),
+            "us_per_launch": round(dur_s * 1e6, 2)}
 
 
 def end_to_end(wins, args, s, world, dev):
@@ -396,7 +441,13 @@ def run_case(args):
     gu = torch.zeros((n, 2 * WL.F), dtype=torch.float32, device=dev)
     hq = torch.zeros((n, WL.F // 32, 36), dtype=torch.uint8, device=dev)
     out = torch.zeros((n, WL.N), dtype=torch.float32, device=dev)
-    call = m.ExpertCall(GU_T, cb_gu, DN_T, cb_dn, WL.N, WL.F, tab(pool_gu), tab(pool_dn), WL.E, ge, gs, ng, n, 0, n,
+    gu_type, cbg, tg = GU_T, cb_gu, tab(pool_gu)
+    if args.case_slot:
+        pool_gx = torch.empty((WL.E, synth.blob_bytes(XT, 2 * WL.F, WL.N)), dtype=torch.uint8, device=dev)
+        tx = tab(pool_gx)
+        m.transcode_cb(GU_T, cb_gu, XT, WL.N, 2 * WL.F, tg, tx, err)
+        gu_type, cbg, tg = XT, None, tx
+    call = m.ExpertCall(gu_type, cbg, DN_T, cb_dn, WL.N, WL.F, tg, tab(pool_dn), WL.E, ge, gs, ng, n, 0, n,
                         xq, es, ed, gu, hq, out, err, m.F_PDL)
     for _ in range(args.steps):
         m.route_group(ids, WL.E, 0, ge, gs, ng, es, ed, err)
@@ -411,6 +462,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", action="store_true", help="run the single-layer profiling case instead")
     ap.add_argument("--case-t", type=int, default=4)
+    ap.add_argument("--case-slot", action="store_true", help="profiling case with the gate/up pool in slot layout")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)

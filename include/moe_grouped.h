@@ -43,6 +43,15 @@
  *   CB sub-block j (32 weights): ls = 2*((sub[j/2] >> 4*(j%2)) & 15) + 1, w = D*ls*(+-grid).
  *   CB grids must hold odd values only (the kernels rely on it; an even entry sets
  *   MOE_ERR_CODEBOOK).
+ * Transcoded slot layouts (load-time re-encodings of CB2/CB3 by moe_transcode_cb, same integers,
+ * decode without lookups; the idea of #3455 "GP100 (sm_60): 4-bit slots for resident IQ2_S /
+ * IQ3_XXS / IQ3_S gate/up experts", "Problem and result"): each weight's signed odd value
+ * v = +-grid is stored as u = (v-1)/2 + bias (v = 2*(u-bias) + 1). A row of K weights is K/256
+ * code chunks, then K/256 scale records of 8 bytes (u16 D, u16 0, u8 sub[4]):
+ *   MOE_CB3X (136 B / 256 w): 4-bit codes, bias 8 (|v| <= 15); in 32-weight sub-block j
+ *        (16 bytes): low nibble of byte i = weight i, high nibble = weight 16+i.
+ *   MOE_CB2X (72 B / 256 w): 2-bit codes, bias 2 (|v| <= 3); in sub-block j (8 bytes):
+ *        bits 2p..2p+1 of byte i = weight 8p+i.
  * Gate/up blob of an expert: n_ff gate rows then n_ff up rows, each of n_embd weights.
  * Down blob of an expert: n_embd rows of n_ff weights. Blob pointers must be 16-byte aligned.
  *
@@ -65,6 +74,8 @@ extern "C" {
 #define MOE_NL4 3
 #define MOE_CB2 4
 #define MOE_CB3 5
+#define MOE_CB3X 6
+#define MOE_CB2X 7
 
 /* ---- host-visible status codes */
 #define MOE_OK 0
@@ -99,6 +110,16 @@ typedef struct moe_wfmt {
     int32_t type;
     const int8_t* codebook;
 } moe_wfmt;
+
+/* Load-time transcoding of CB2/CB3 blobs into a slot layout (MOE_CB3X or MOE_CB2X). For every
+ * blob b < n_blobs: dst_blobs[b] (rows x row_bytes(dst_type, K)) = the slot form of
+ * src_blobs[b] (rows x row_bytes(src.type, K)). src_blobs / dst_blobs: device arrays of device
+ * pointers (16-byte aligned blobs). A value outside the slot's range (|v| > 15 for CB3X, > 3 for
+ * CB2X) sets MOE_ERR_CODEBOOK; check *err before using the result. The integer dot products and
+ * scales of the slot form equal the source's exactly. */
+int moe_transcode_cb(moe_wfmt src, int dst_type, int K, int rows, int n_blobs,
+                     const void* const* src_blobs, void* const* dst_blobs, int32_t* err,
+                     cudaStream_t stream);
 
 /* Bytes of one row of K weights in format `type` (0 if K is not valid for it). Host only. */
 int64_t moe_row_bytes(int type, int K);

@@ -19,8 +19,8 @@ _BUILD = os.path.join(_HERE, "_build")
 _LOCK = threading.Lock()
 _LIBS: dict = {}
 
-Q8_0, Q4B, NL4, CB2, CB3 = 1, 2, 3, 4, 5
-TYPE_NAMES = {"Q8_0": Q8_0, "Q4B": Q4B, "NL4": NL4, "CB2": CB2, "CB3": CB3}
+Q8_0, Q4B, NL4, CB2, CB3, CB3X, CB2X = 1, 2, 3, 4, 5, 6, 7
+TYPE_NAMES = {"Q8_0": Q8_0, "Q4B": Q4B, "NL4": NL4, "CB2": CB2, "CB3": CB3, "CB3X": CB3X, "CB2X": CB2X}
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -66,6 +66,8 @@ def _setup(lib):
     lib.orc_grouped_gemv.argtypes = [_I, _P, _I, _I, _P, _I, _P, _P, _I, _P, _P, _P, _P, _I64]
     lib.orc_grouped_gemv.restype = _I
     lib.orc_swiglu_q8_1.argtypes = [_P, _I, _I, _I, _P]
+    lib.orc_transcode_row.argtypes = [_I, _P, _I, _P, _I, _P]
+    lib.orc_transcode_row.restype = _I
     lib.orc_route_group.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P]
     lib.orc_route_group.restype = _I
     return lib
@@ -150,6 +152,23 @@ class Oracle:
         xq_row = np.ascontiguousarray(xq_row, dtype=np.uint8)
         cb = self._cb(cb)
         return float(self.lib.orc_row_dot(typ, _ptr(row), K, _ptr(cb), _ptr(xq_row)))
+
+    def transcode_row(self, src_type, row, K, cb, dst_type):
+        row = np.ascontiguousarray(row, dtype=np.uint8)
+        cb = self._cb(cb)
+        out = np.zeros(self.row_bytes(dst_type, K), dtype=np.uint8)
+        rc = self.lib.orc_transcode_row(src_type, _ptr(row), K, _ptr(cb), dst_type, _ptr(out))
+        return out, rc
+
+    def transcode_blob(self, src_type, blob, K, rows, cb, dst_type):
+        rb_s, rb_d = self.row_bytes(src_type, K), self.row_bytes(dst_type, K)
+        out = np.zeros(rows * rb_d, dtype=np.uint8)
+        bad = 0
+        for r in range(rows):
+            o, rc = self.transcode_row(src_type, blob[r * rb_s:(r + 1) * rb_s], K, cb, dst_type)
+            out[r * rb_d:(r + 1) * rb_d] = o
+            bad |= rc
+        return out, bad
 
     # ---- grouped steps
     def grouped_gemv(self, typ, K, rows, blobs, grp_expert, grp_start, n_groups, act,

@@ -157,8 +157,35 @@ int64_t orc_row_bytes(int type, int K) {
     case ORC_NL4: return (int64_t)(K / 32) * 18;
     case ORC_CB2: return K % 256 ? 0 : (int64_t)(K / 256) * 70;
     case ORC_CB3: return K % 256 ? 0 : (int64_t)(K / 256) * 102;
+    case ORC_CB3X: return K % 256 ? 0 : (int64_t)(K / 256) * (128 + 8);
+    case ORC_CB2X: return K % 256 ? 0 : (int64_t)(K / 256) * (64 + 8);
     }
     return 0;
+}
+
+/* ---- transcoded slots: codes of the K weights, then one 8-byte scale record per 256 weights */
+
+static int slot_bits(int type) { return type == ORC_CB3X ? 4 : 2; }
+static int slot_bias(int type) { return type == ORC_CB3X ? 8 : 2; }
+
+/* Code u of weight n of a slot row. */
+static int slot_code(int type, const uint8_t* row, int n) {
+    int c = n / 256, j = (n % 256) / 32, i = n % 32;
+    if (type == ORC_CB3X) {
+        const uint8_t* sb = row + c * 128 + j * 16;
+#ifndef ORC_PLANT_SLOT_ORDER
+        return i < 16 ? (sb[i] & 15) : (sb[i - 16] >> 4);
+#else
+        return (sb[i / 2] >> (4 * (i & 1))) & 15;
+#endif
+    }
+    const uint8_t* sb = row + c * 64 + j * 8;
+    return (sb[i % 8] >> (2 * (i / 8))) & 3;
+}
+
+static const uint8_t* slot_scale(int type, const uint8_t* row, int K, int n) {
+    int code_bytes = type == ORC_CB3X ? 128 : 64;
+    return row + (K / 256) * code_bytes + (n / 256) * 8;
 }
 
 /* 4-bit code j (0..31) of a 16-byte nibble array. */
@@ -218,6 +245,8 @@ void orc_int_weights(int type, const uint8_t* row, int K, const int8_t* cb, int3
         case ORC_NL4: v[n] = cb[nib_code(row + 18 * b + 2, i)]; break;
         case ORC_CB2: v[n] = cb_value(type, row + 70 * (n / 256), cb, n % 256); break;
         case ORC_CB3: v[n] = cb_value(type, row + 102 * (n / 256), cb, n % 256); break;
+        case ORC_CB3X:
+        case ORC_CB2X: v[n] = 2 * (slot_code(type, row, n) - slot_bias(type)) + 1; break;
         }
     }
 }
@@ -237,6 +266,12 @@ void orc_dequant_row(int type, const uint8_t* row, int K, const int8_t* cb, doub
         case ORC_CB3: {
             const uint8_t* sb = row + (type == ORC_CB2 ? 70 : 102) * (n / 256);
             w[n] = (double)orc_h2f(rd16(sb)) * cb_ls(cb_sub(type, sb), (n % 256) / 32) * v[n];
+            break;
+        }
+        case ORC_CB3X:
+        case ORC_CB2X: {
+            const uint8_t* sc = slot_scale(type, row, K, n);
+            w[n] = (double)orc_h2f(rd16(sc)) * cb_ls(sc + 4, (n % 256) / 32) * v[n];
             break;
         }
         }
@@ -282,10 +317,46 @@ double orc_row_dot(int type, const uint8_t* row, int K, const int8_t* cb, const 
             acc += (double)orc_h2f(rd16(sb)) * dx * ((double)cb_ls(cb_sub(type, sb), b % 8) * isum[b]);
             break;
         }
+        case ORC_CB3X:
+        case ORC_CB2X: {
+            const uint8_t* sc = slot_scale(type, row, K, 32 * b);
+            acc += (double)orc_h2f(rd16(sc)) * dx * ((double)cb_ls(sc + 4, b % 8) * isum[b]);
+            break;
+        }
         }
     }
     free(isum);
     return acc;
+}
+
+int orc_transcode_row(int src_type, const uint8_t* src, int K, const int8_t* cb, int dst_type, uint8_t* dst) {
+    int bits = slot_bits(dst_type), bias = slot_bias(dst_type), lim = (1 << bits) - 1, bad = 0;
+    int code_bytes = dst_type == ORC_CB3X ? 128 : 64;
+    int32_t* v = (int32_t*)malloc(sizeof(int32_t) * (size_t)K);
+    orc_int_weights(src_type, src, K, cb, v);
+    memset(dst, 0, (size_t)orc_row_bytes(dst_type, K));
+    for (int n = 0; n < K; n++) {
+        int u = (v[n] - 1) / 2 + bias; /* v odd: exact */
+        if ((v[n] & 1) == 0 || u < 0 || u > lim) { bad = -1; u = 0; }
+        int c = n / 256, j = (n % 256) / 32, i = n % 32;
+        if (dst_type == ORC_CB3X) {
+            uint8_t* sb = dst + c * 128 + j * 16;
+            if (i < 16) sb[i] |= (uint8_t)u;
+            else sb[i - 16] |= (uint8_t)(u << 4);
+        } else {
+            uint8_t* sb = dst + c * 64 + j * 8;
+            sb[i % 8] |= (uint8_t)(u << (2 * (i / 8)));
+        }
+    }
+    for (int c = 0; c < K / 256; c++) {
+        const uint8_t* sb = src + (src_type == ORC_CB2 ? 70 : 102) * c;
+        uint8_t* sc = dst + (K / 256) * code_bytes + 8 * c;
+        sc[0] = sb[0];
+        sc[1] = sb[1];
+        memcpy(sc + 4, cb_sub(src_type, sb), 4);
+    }
+    free(v);
+    return bad;
 }
 
 /* ------------------------------------------------------------------ grouped steps */

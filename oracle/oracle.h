@@ -24,7 +24,15 @@
  *       weight n: group i = n/4, p = n%4: +-grid3[idx[i]][p], bit n%8 of sign[n/8] negates
  *   CB2/CB3 sub-block j (32 weights): sub_j = (sub[j>>1] >> 4*(j&1)) & 15, ls_j = 2*sub_j+1,
  *       w = D * ls_j * (+-grid value)
- * A row of K weights is K/32 blocks (K/256 super-blocks) packed without padding.
+ * Transcoded slot layouts (load-time re-encodings of CB2/CB3 holding the same integers): each
+ * weight's signed odd value v = +-grid is stored as u = (v - 1)/2 + bias, so v = 2*(u - bias) + 1.
+ * A row of K weights is K/256 code chunks followed by K/256 scale records of 8 bytes
+ * (u16 D, u16 0, u8 sub[4]):
+ *   CB3X: 128 B of 4-bit codes per 256 weights, bias 8 (|v| <= 15). In 32-weight sub-block j
+ *         (16 bytes): byte i, low nibble = weight i, high nibble = weight 16 + i.
+ *   CB2X:  64 B of 2-bit codes per 256 weights, bias 2 (|v| <= 3). In sub-block j (8 bytes):
+ *         bits 2p..2p+1 of byte i = weight 8p + i.
+ * Rows of the native formats are K/32 blocks (K/256 super-blocks) packed without padding.
  */
 #ifndef MOE_ORACLE_H
 #define MOE_ORACLE_H
@@ -34,7 +42,7 @@
 extern "C" {
 #endif
 
-enum { ORC_Q8_0 = 1, ORC_Q4B = 2, ORC_NL4 = 3, ORC_CB2 = 4, ORC_CB3 = 5 };
+enum { ORC_Q8_0 = 1, ORC_Q4B = 2, ORC_NL4 = 3, ORC_CB2 = 4, ORC_CB3 = 5, ORC_CB3X = 6, ORC_CB2X = 7 };
 
 /* IEEE binary16 <-> binary32, round to nearest even (subnormals kept). */
 float orc_h2f(uint16_t h);
@@ -50,6 +58,10 @@ int64_t orc_row_bytes(int type, int K);
 
 /* q8_1 of n values (n % 32 == 0): out receives n/32 blocks of 36 bytes. */
 void orc_quantize_q8_1(const float* x, int64_t n, uint8_t* out);
+
+/* Transcode one row of CB2/CB3 (src_type) into the slot layout dst_type (CB3X or CB2X).
+ * Returns 0, or -1 when a value does not fit the slot's code range (row left unspecified). */
+int orc_transcode_row(int src_type, const uint8_t* src, int K, const int8_t* cb, int dst_type, uint8_t* dst);
 
 /* Dequantize one row to fp64 (w[K]); cb is the codebook (CB2 256x8, CB3 256x4, NL4 16). */
 void orc_dequant_row(int type, const uint8_t* row, int K, const int8_t* cb, double* w);

@@ -15,12 +15,12 @@ import os
 import torch
 
 __all__ = [
-    "Q8_0", "Q4B", "NL4", "CB2", "CB3", "MoeError", "lib", "row_bytes", "strerror",
+    "Q8_0", "Q4B", "NL4", "CB2", "CB3", "CB3X", "CB2X", "MoeError", "transcode_cb", "lib", "row_bytes", "strerror",
     "quantize_q8_1", "route_group", "grouped_gu", "swiglu_q8_1", "grouped_down",
     "expert_grouped", "ExpertCall", "STATIC_SCRATCH_BYTES", "test_block_isum", "ERR_BITS", "F_PDL",
 ]
 
-Q8_0, Q4B, NL4, CB2, CB3 = 1, 2, 3, 4, 5
+Q8_0, Q4B, NL4, CB2, CB3, CB3X, CB2X = 1, 2, 3, 4, 5, 6, 7
 F_PDL = 1
 STATIC_SCRATCH_BYTES = 4 << 20
 ERR_BITS = {1: "NGROUPS", 2: "EXPERT", 4: "START", 8: "ENTRY", 16: "ALIGN", 32: "CODEBOOK",
@@ -75,8 +75,10 @@ def lib():
         L.moe_expert_grouped.argtypes = [ctypes.POINTER(ExpertCallC), _P]
         L.moe_expert_grouped_static.argtypes = [ctypes.POINTER(ExpertCallC), _P]
         L.moe_test_block_isum.argtypes = [WFmt, _I, _P, _I, _P, _P, _P]
+        L.moe_transcode_cb.argtypes = [WFmt, _I, _I, _I, _I, _P, _P, _P, _P]
         for f in ("moe_quantize_q8_1", "moe_route_group", "moe_grouped_gu", "moe_swiglu_q8_1",
-                  "moe_grouped_down", "moe_expert_grouped", "moe_expert_grouped_static", "moe_test_block_isum"):
+                  "moe_grouped_down", "moe_expert_grouped", "moe_expert_grouped_static", "moe_test_block_isum",
+                  "moe_transcode_cb"):
             getattr(L, f).restype = _I
         _LIB = L
     return _LIB
@@ -174,6 +176,12 @@ class ExpertCall:
 
 def expert_grouped(*args, stream=None, **kw):
     ExpertCall(*args, **kw)(stream)
+
+
+def transcode_cb(src_type, codebook, dst_type, K, rows, src_table, dst_table, err=None, stream=None):
+    """Load-time transcoding of CB2/CB3 blobs (device pointer tables) into slot layouts."""
+    _check(lib().moe_transcode_cb(_fmt(src_type, codebook), dst_type, K, rows, src_table.shape[0], _dp(src_table),
+                                  _dp(dst_table), _dp(err), _stream(stream)))
 
 
 def test_block_isum(typ, codebook, K, blob, rows, xq_row, isum, stream=None):

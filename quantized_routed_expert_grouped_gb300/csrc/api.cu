@@ -15,7 +15,7 @@ constexpr int kSmemPerSm = 228 * 1024;
 constexpr int kMaxGroups = 1024;
 
 bool cb_type(int t) { return t == MOE_CB2 || t == MOE_CB3; }
-bool valid_type(int t) { return t >= MOE_Q8_0 && t <= MOE_CB3; }
+bool valid_type(int t) { return t >= MOE_Q8_0 && t <= MOE_CB2X; }
 
 int sm_count() {
     int dev = 0;
@@ -40,16 +40,24 @@ int check_fmt(const moe_wfmt& f) {
 int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
 // Launch geometry and shared-memory layout of one grouped GEMV (K weights per row, `rows`
-// rows per expert), filled into `a` and `p`. One CTA per SM: a producer warp and up to 12
+// rows per expert), filled into `a` and `p`. One CTA per SM: a producer warp and up to 15
 // consumer warps grouped in warp-sets; a set works on one tile (32 rows, lane = row) at a time,
-// its warps splitting the row's 256-weight chunks; as many sets as fit in 12 warps.
+// its warps splitting the row's 256-weight chunks; as many sets as fit in 15 warps.
 int plan_gemv(int type, int K, int rows, int cap_groups, GemvArgs& a, GemvPlan& p) {
     const int nch = K / 256;
     const int64_t rb = moe_row_bytes(type, K);
     if (nch <= 0 || nch > 32 || rb <= 0 || rows <= 0 || rows % 8) return MOE_E_SHAPE;
     if (cap_groups <= 0 || cap_groups > kMaxGroups) return MOE_E_CAP;
     const bool cb = cb_type(type);
-    const int CPW = (nch + 11) / 12;
+    // chunks per warp: the smallest that gives the most consumer warps (at most 15; warp-sets
+    // of WPS = ceil(nch / CPW) warps, TP = 15 / WPS sets)
+    int CPW = 1, best = 0;
+    for (int cpw = 1; cpw <= nch; ++cpw) {
+        const int wps = (nch + cpw - 1) / cpw;
+        if (wps > 15) continue;
+        const int cw = wps * (15 / wps);
+        if (cw > best) { best = cw; CPW = cpw; }
+    }
     const int WPS = (nch + CPW - 1) / CPW;
     const int RT = 32 * rb <= 96 * 1024 ? 32 : 16;
     const int nb = K / 32, nbp = nb + nb / 8;
@@ -58,7 +66,7 @@ int plan_gemv(int type, int K, int rows, int cap_groups, GemvArgs& a, GemvPlan& 
     const int fixed = (cb ? 32768 : 0) + actq + act2 + grp + 256 + 512;
     const int stage_bytes = round_up(static_cast<int>(RT * rb) + 16, 128);
     const int part_bytes = nch * 4 * RT * 4;
-    for (int TP = 12 / WPS > 0 ? 12 / WPS : 1; TP >= 1; --TP) {
+    for (int TP = 15 / WPS > 0 ? 15 / WPS : 1; TP >= 1; --TP) {
         int stages = (kSmemPerSm - 1024 - fixed) / (stage_bytes + part_bytes);
         if (stages > 8) stages = 8;
         if (stages < 2 || stages < TP + 1) continue;
@@ -104,6 +112,8 @@ cudaError_t occupancy(int type, int NT, int smem, int* ctas) {
     case MOE_Q4B: return gemv_occupancy_q4b(NT, smem, ctas);
     case MOE_NL4: return gemv_occupancy_nl4(NT, smem, ctas);
     case MOE_CB2: return gemv_occupancy_cb2(NT, smem, ctas);
+    case MOE_CB3X: return gemv_occupancy_cb3x(NT, smem, ctas);
+    case MOE_CB2X: return gemv_occupancy_cb2x(NT, smem, ctas);
     default: return gemv_occupancy_cb3(NT, smem, ctas);
     }
 }
@@ -114,6 +124,8 @@ cudaError_t launch_gemv(int type, const GemvArgs& a, int grid, int NT, int smem,
     case MOE_Q4B: return launch_gemv_q4b(a, grid, NT, smem, s, pdl);
     case MOE_NL4: return launch_gemv_nl4(a, grid, NT, smem, s, pdl);
     case MOE_CB2: return launch_gemv_cb2(a, grid, NT, smem, s, pdl);
+    case MOE_CB3X: return launch_gemv_cb3x(a, grid, NT, smem, s, pdl);
+    case MOE_CB2X: return launch_gemv_cb2x(a, grid, NT, smem, s, pdl);
     default: return launch_gemv_cb3(a, grid, NT, smem, s, pdl);
     }
 }
@@ -219,6 +231,8 @@ int64_t moe_row_bytes(int type, int K) {
     case MOE_NL4: return static_cast<int64_t>(K / 32) * 18;
     case MOE_CB2: return K % 256 ? 0 : static_cast<int64_t>(K / 256) * 70;
     case MOE_CB3: return K % 256 ? 0 : static_cast<int64_t>(K / 256) * 102;
+    case MOE_CB3X: return K % 256 ? 0 : static_cast<int64_t>(K / 256) * (128 + 8);
+    case MOE_CB2X: return K % 256 ? 0 : static_cast<int64_t>(K / 256) * (64 + 8);
     }
     return 0;
 }
@@ -308,6 +322,19 @@ int moe_expert_grouped(const moe_expert_call* c, cudaStream_t stream) {
                      c->out_rows, c->out_row_stride, c->err, stream, pdl, pdl);
 }
 
+int moe_transcode_cb(moe_wfmt src, int dst_type, int K, int rows, int n_blobs, const void* const* src_blobs,
+                     void* const* dst_blobs, int32_t* err, cudaStream_t stream) {
+    if (!cb_type(src.type) || (dst_type != MOE_CB3X && dst_type != MOE_CB2X)) return MOE_E_TYPE;
+    int rc = check_fmt(src);
+    if (rc) return rc;
+    if (!src_blobs || !dst_blobs) return MOE_E_NULL;
+    if (K <= 0 || K % 256 || rows <= 0 || n_blobs <= 0) return MOE_E_SHAPE;
+    return launch_transcode_cb(src.type, src.codebook, dst_type, K, rows, n_blobs, src_blobs, dst_blobs, err,
+                               stream) == cudaSuccess
+               ? MOE_OK
+               : MOE_E_CUDA;
+}
+
 int moe_test_block_isum(moe_wfmt fmt, int K, const void* blob, int rows, const moe_q8_1* xq, int32_t* isum,
                         cudaStream_t stream) {
     int rc = check_fmt(fmt);
@@ -320,6 +347,8 @@ int moe_test_block_isum(moe_wfmt fmt, int K, const void* blob, int rows, const m
     case MOE_Q4B: e = launch_isum_q4b(fmt.codebook, K, blob, rows, xq, isum, stream); break;
     case MOE_NL4: e = launch_isum_nl4(fmt.codebook, K, blob, rows, xq, isum, stream); break;
     case MOE_CB2: e = launch_isum_cb2(fmt.codebook, K, blob, rows, xq, isum, stream); break;
+    case MOE_CB3X: e = launch_isum_cb3x(fmt.codebook, K, blob, rows, xq, isum, stream); break;
+    case MOE_CB2X: e = launch_isum_cb2x(fmt.codebook, K, blob, rows, xq, isum, stream); break;
     default: e = launch_isum_cb3(fmt.codebook, K, blob, rows, xq, isum, stream); break;
     }
     return e == cudaSuccess ? MOE_OK : MOE_E_CUDA;

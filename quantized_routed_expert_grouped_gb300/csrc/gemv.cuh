@@ -46,26 +46,49 @@
 
 namespace moe {
 
+// CHUNK: bytes of one 256-weight chunk (for the slot layouts: its codes; the 8-byte scale
+// records follow all of a row's codes). CB: native codebook format (grid staged in shared
+// memory). SLOT: transcoded slot layout (BIAS: code bias). ALPHA: decode cost of a row relative to
+// one entry's dot products (work balancing).
 template <int TYPE>
 struct Fmt;
 template <>
-struct Fmt<MOE_Q8_0> { static constexpr int CHUNK = 272, R = 1, ALPHA = 1; static constexpr bool CB = false; };
+struct Fmt<MOE_Q8_0> {
+    static constexpr int CHUNK = 272, ALPHA = 1;
+    static constexpr bool CB = false, SLOT = false;
+};
 template <>
-struct Fmt<MOE_Q4B> { static constexpr int CHUNK = 160, R = 1, ALPHA = 2; static constexpr bool CB = false; };
+struct Fmt<MOE_Q4B> {
+    static constexpr int CHUNK = 160, ALPHA = 2;
+    static constexpr bool CB = false, SLOT = false;
+};
 template <>
-struct Fmt<MOE_NL4> { static constexpr int CHUNK = 144, R = 1, ALPHA = 5; static constexpr bool CB = false; };
+struct Fmt<MOE_NL4> {
+    static constexpr int CHUNK = 144, ALPHA = 5;
+    static constexpr bool CB = false, SLOT = false;
+};
 template <>
 struct Fmt<MOE_CB2> {
-    static constexpr int CHUNK = 70, R = 2, ALPHA = 4, NW = 18, SGN = 8, SUB = 16;
-    static constexpr bool CB = true;
+    static constexpr int CHUNK = 70, ALPHA = 4, NW = 18, SGN = 8, SUB = 16;
+    static constexpr bool CB = true, SLOT = false;
 };
 template <>
 struct Fmt<MOE_CB3> {
-    static constexpr int CHUNK = 102, R = 2, ALPHA = 5, NW = 26, SGN = 16, SUB = 24;
-    static constexpr bool CB = true;
+    static constexpr int CHUNK = 102, ALPHA = 5, NW = 26, SGN = 16, SUB = 24;
+    static constexpr bool CB = true, SLOT = false;
+};
+template <>
+struct Fmt<MOE_CB3X> {
+    static constexpr int CHUNK = 128, ALPHA = 1, BIAS = 8;
+    static constexpr bool CB = false, SLOT = true;
+};
+template <>
+struct Fmt<MOE_CB2X> {
+    static constexpr int CHUNK = 64, ALPHA = 1, BIAS = 2;
+    static constexpr bool CB = false, SLOT = true;
 };
 
-constexpr int kMaxThreads = 416;  // one producer warp + up to 12 consumer warps (<= 128 registers)
+constexpr int kMaxThreads = 512;  // one producer warp + up to 15 consumer warps (<= 128 registers)
 
 __device__ __forceinline__ uint32_t ld32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
@@ -230,6 +253,26 @@ __device__ __forceinline__ void nl4_decode(const uint32_t raw[36], const uint32_
     for (int k = 0; k < 4; ++k) nl4_word(tab, qs[k], W[k], W[4 + k]);
 }
 
+// Sub-block j (32 weights) of a slot chunk: codes -> 8 words of biased values u (one code per
+// byte), matching the staged activation words. q: the sub-block's code words (4 for 4-bit
+// codes, 2 for 2-bit codes).
+template <int TYPE>
+__device__ __forceinline__ void slot_decode(const uint32_t* q, uint32_t W[8]) {
+    if constexpr (TYPE == MOE_CB3X) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            W[k] = q[k] & 0x0f0f0f0fu;
+            W[4 + k] = (q[k] >> 4) & 0x0f0f0f0fu;
+        }
+    } else {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            W[2 * p] = (q[0] >> (2 * p)) & 0x03030303u;
+            W[2 * p + 1] = (q[1] >> (2 * p)) & 0x03030303u;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- work split
 
 struct Tile {
@@ -378,10 +421,12 @@ __device__ __forceinline__ void stage_act(const GemvArgs& a, uint8_t* smem, cons
         q[(s * 2 + 0) * a.nbp + bp] = make_int4(w[1], w[2], w[3], w[4]);
         q[(s * 2 + 1) * a.nbp + bp] = make_int4(w[5], w[6], w[7], w[8]);
         float aux = 0.0f;
-        if constexpr (Fmt<TYPE>::CB) {
+        if constexpr (Fmt<TYPE>::CB || Fmt<TYPE>::SLOT) {
             int S = 0;
 #pragma unroll
             for (int k = 1; k < 9; ++k) S = dp4a(w[k], 0x01010101u, S);
+            // CB: sum s g q = 2 dot(x ^ mask, q) + S; slots: = 2 dot(u, q) - (2 bias - 1) S
+            if constexpr (Fmt<TYPE>::SLOT) S *= -(2 * Fmt<TYPE>::BIAS - 1);
             aux = __int_as_float(S);
         } else if constexpr (TYPE == MOE_Q4B) {
             aux = h2f_bits(w[0] >> 16);
@@ -411,11 +456,15 @@ __device__ __forceinline__ void load_act(const GemvArgs& a, const uint8_t* smem,
 
 // ---------------------------------------------------------------- compute
 
+// Two independent dp4a chains (even and odd words) halve the dependent latency.
 __device__ __forceinline__ int dot8(const uint32_t W[8], const uint32_t A[8]) {
-    int d = 0;
+    int d0 = 0, d1 = 0;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) d = dp4a(W[w], A[w], d);
-    return d;
+    for (int w = 0; w < 8; w += 2) {
+        d0 = dp4a(W[w], A[w], d0);
+        d1 = dp4a(W[w + 1], A[w + 1], d1);
+    }
+    return d0 + d1;
 }
 
 // One lane's row of chunk c (256 weights) against NE staged entries: chunk partials acc[e].
@@ -452,13 +501,73 @@ __device__ __forceinline__ void plain_block(const GemvArgs& a, const uint8_t* sm
     }
 }
 
+template <int TYPE, int NE, int j>
+__device__ __forceinline__ void slot_block(const GemvArgs& a, const uint8_t* smem, const uint32_t* q, uint32_t subw,
+                                           int c, int buf, float acc[NE]) {
+    uint32_t A[NE][8];
+    float dx[NE], aux[NE];
+    load_act<NE>(a, smem, c * 8 + j, A, dx, aux, buf);
+    uint32_t W[8];
+    slot_decode<TYPE>(q, W);
+    const int ls = 2 * static_cast<int>((subw >> (8 * (j >> 1) + 4 * (j & 1))) & 15u) + 1;
+#pragma unroll
+    for (int e = 0; e < NE; ++e) {
+        const int isum = 2 * dot8(W, A[e]) + __float_as_int(aux[e]);
+        acc[e] = fmaf(static_cast<float>(ls * isum), dx[e], acc[e]);
+    }
+}
+
+// The code words of 16 bytes at p (16-byte aligned when `al16`, else 8-byte aligned).
+__device__ __forceinline__ void ld16(const uint8_t* p, bool al16, uint32_t q[4]) {
+    if (al16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p);
+        q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
+    } else {
+        const uint2 v0 = *reinterpret_cast<const uint2*>(p), v1 = *reinterpret_cast<const uint2*>(p + 8);
+        q[0] = v0.x; q[1] = v0.y; q[2] = v1.x; q[3] = v1.y;
+    }
+}
+
+template <int TYPE, int NE>
+__device__ __forceinline__ void slot_chunk(const GemvArgs& a, const uint8_t* smem, const uint8_t* rowp, int c, int buf,
+                                           float acc[NE]) {
+    const uint2 sc = *reinterpret_cast<const uint2*>(rowp + a.nch * Fmt<TYPE>::CHUNK + c * 8);
+    const float D = h2f_bits(sc.x);
+    const uint8_t* codes = rowp + c * Fmt<TYPE>::CHUNK;
+    const bool al16 = (a.row_bytes & 15) == 0;
+    uint32_t q[4];
+    if constexpr (TYPE == MOE_CB3X) {  // 16 bytes per sub-block
+        ld16(codes + 0, al16, q); slot_block<TYPE, NE, 0>(a, smem, q, sc.y, c, buf, acc);
+        ld16(codes + 16, al16, q); slot_block<TYPE, NE, 1>(a, smem, q, sc.y, c, buf, acc);
+        ld16(codes + 32, al16, q); slot_block<TYPE, NE, 2>(a, smem, q, sc.y, c, buf, acc);
+        ld16(codes + 48, al16, q); slot_block<TYPE, NE, 3>(a, smem, q, sc.y, c, buf, acc);
+        ld16(codes + 64, al16, q); slot_block<TYPE, NE, 4>(a, smem, q, sc.y, c, buf, acc);
+        ld16(codes + 80, al16, q); slot_block<TYPE, NE, 5>(a, smem, q, sc.y, c, buf, acc);
+        ld16(codes + 96, al16, q); slot_block<TYPE, NE, 6>(a, smem, q, sc.y, c, buf, acc);
+        ld16(codes + 112, al16, q); slot_block<TYPE, NE, 7>(a, smem, q, sc.y, c, buf, acc);
+    } else {  // 8 bytes per sub-block: two sub-blocks per 16-byte load
+        ld16(codes + 0, al16, q); slot_block<TYPE, NE, 0>(a, smem, q, sc.y, c, buf, acc);
+        slot_block<TYPE, NE, 1>(a, smem, q + 2, sc.y, c, buf, acc);
+        ld16(codes + 16, al16, q); slot_block<TYPE, NE, 2>(a, smem, q, sc.y, c, buf, acc);
+        slot_block<TYPE, NE, 3>(a, smem, q + 2, sc.y, c, buf, acc);
+        ld16(codes + 32, al16, q); slot_block<TYPE, NE, 4>(a, smem, q, sc.y, c, buf, acc);
+        slot_block<TYPE, NE, 5>(a, smem, q + 2, sc.y, c, buf, acc);
+        ld16(codes + 48, al16, q); slot_block<TYPE, NE, 6>(a, smem, q, sc.y, c, buf, acc);
+        slot_block<TYPE, NE, 7>(a, smem, q + 2, sc.y, c, buf, acc);
+    }
+#pragma unroll
+    for (int e = 0; e < NE; ++e) acc[e] = __fmul_rn(D, acc[e]);
+}
+
 template <int TYPE, int NE>
 __device__ __forceinline__ void lane_chunk(const GemvArgs& a, const uint8_t* smem, const uint8_t* tile, int row, int c,
                                            uint32_t loff, const uint32_t tab[4], int buf, float acc[NE]) {
 #pragma unroll
     for (int e = 0; e < NE; ++e) acc[e] = 0.0f;
     const uint8_t* chunk = tile + row * a.row_bytes + c * Fmt<TYPE>::CHUNK;
-    if constexpr (Fmt<TYPE>::CB) {
+    if constexpr (Fmt<TYPE>::SLOT) {
+        slot_chunk<TYPE, NE>(a, smem, tile + row * a.row_bytes, c, buf, acc);
+    } else if constexpr (Fmt<TYPE>::CB) {
         CBRow<TYPE> rr;
         rr.load(chunk);
         const float D = rr.D();
@@ -762,7 +871,22 @@ __global__ void __launch_bounds__(256) isum_kernel(const GemvArgs a, const uint8
     const uint8_t* chunk = blob + static_cast<size_t>(r) * a.row_bytes + c * Fmt<TYPE>::CHUNK;
     const uint32_t loff = TYPE == MOE_CB3 ? lane * 4u : (lane & 15u) * 8u;
     int32_t out[8];
-    if constexpr (Fmt<TYPE>::CB) {
+    if constexpr (Fmt<TYPE>::SLOT) {
+        const uint8_t* rowp = blob + static_cast<size_t>(r) * a.row_bytes;
+        const uint8_t* codes = rowp + c * Fmt<TYPE>::CHUNK;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            constexpr int qb = TYPE == MOE_CB3X ? 16 : 8;
+            uint32_t q[4];
+            for (int k = 0; k < qb / 4; ++k) q[k] = ld32(codes + j * qb + 4 * k);
+            uint32_t A[1][8];
+            float dx[1], aux[1];
+            load_act<1>(a, smem, c * 8 + j, A, dx, aux);
+            uint32_t W[8];
+            slot_decode<TYPE>(q, W);
+            out[j] = 2 * dot8(W, A[0]) + __float_as_int(aux[0]);
+        }
+    } else if constexpr (Fmt<TYPE>::CB) {
         CBRow<TYPE> row;
         row.load(chunk);
         auto one = [&](auto jc) {
@@ -836,7 +960,7 @@ cudaError_t launch_isum_t(const int8_t* codebook, int K, const void* blob, int r
     a.nch = K / 256;
     a.nb = K / 32;
     a.nbp = a.nb + a.nb / 8;
-    a.row_bytes = static_cast<int>(a.nch * Fmt<TYPE>::CHUNK);
+    a.row_bytes = static_cast<int>(a.nch * (Fmt<TYPE>::CHUNK + (Fmt<TYPE>::SLOT ? 8 : 0)));
     a.codebook = codebook;
     a.act = xq;
     a.n_act_rows = 1;

@@ -79,6 +79,9 @@ cudaError_t launch_route_group(const int32_t* topk_ids, int T, int k, int n_expe
                                int32_t* grp_expert, int32_t* grp_start, int32_t* n_groups, int32_t* ent_src,
                                int32_t* ent_dst, int32_t* err, cudaStream_t s);
 
+cudaError_t launch_transcode_cb(int src_type, const int8_t* codebook, int dst_type, int K, int rows, int n_blobs,
+                                const void* const* src_blobs, void* const* dst_blobs, int32_t* err, cudaStream_t s);
+
 // Per-format grouped GEMV and test-hook launchers (one translation unit per format).
 #define MOE_DECLARE_FORMAT(NAME)                                                                       \
     cudaError_t launch_gemv_##NAME(const GemvArgs& a, int grid, int NT, int smem, cudaStream_t s, bool pdl); \
@@ -90,6 +93,8 @@ MOE_DECLARE_FORMAT(q4b)
 MOE_DECLARE_FORMAT(nl4)
 MOE_DECLARE_FORMAT(cb2)
 MOE_DECLARE_FORMAT(cb3)
+MOE_DECLARE_FORMAT(cb3x)
+MOE_DECLARE_FORMAT(cb2x)
 #undef MOE_DECLARE_FORMAT
 
 }  // namespace moe

@@ -18,8 +18,8 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-Q8_0, Q4B, NL4, CB2, CB3 = 1, 2, 3, 4, 5
-NAMES = {Q8_0: "Q8_0", Q4B: "Q4B", NL4: "NL4", CB2: "CB2", CB3: "CB3"}
+Q8_0, Q4B, NL4, CB2, CB3, CB3X, CB2X = 1, 2, 3, 4, 5, 6, 7
+NAMES = {Q8_0: "Q8_0", Q4B: "Q4B", NL4: "NL4", CB2: "CB2", CB3: "CB3", CB3X: "CB3X", CB2X: "CB2X"}
 BY_NAME = {v: k for k, v in NAMES.items()}
 
 # (bytes per unit, weights per unit, [(field offset, distribution)]) per format
@@ -33,7 +33,14 @@ _UNIT = {
 _DIST = {"d": (1e-3, 1e-2), "m": (-0.08, -0.008)}
 
 
+# bytes per 256 weights of the transcoded slot layouts (codes + 8-byte scale record)
+_SLOT = {CB3X: 136, CB2X: 72}
+
+
 def row_bytes(typ: int, K: int) -> int:
+    if typ in _SLOT:
+        assert K % 256 == 0
+        return K // 256 * _SLOT[typ]
     ub, uw, _ = _UNIT[typ]
     assert K % uw == 0
     return K // uw * ub

@@ -6,7 +6,7 @@ from the CUDA path.
 """
 from __future__ import annotations
 
-from dataclasses import dataclass
+from dataclasses import dataclass, replace
 
 import numpy as np
 import torch
@@ -64,6 +64,19 @@ def make_layer(wl: synth.Workload, pair, T: int, layer: int = 0, device="cuda", 
     ids = synth.routing(T, wl.k, E, wl.seed * 1000 + layer * 10 + T + 5)
     return Layer(wl, gu_t, dn_t, T, layer, key_gu, key_dn, pool_gu, pool_dn, pointer_table(pool_gu),
                  pointer_table(pool_dn), cb_gu, cb_dn, dev(cb_gu), dev(cb_dn), x, ids)
+
+
+def transcoded(m, L: Layer, dst_type: int, device="cuda") -> Layer:
+    """A copy of layer L whose gate/up pool is the GPU's load-time transcoding of L's CB2/CB3 pool
+    into the slot layout dst_type (the oracle keeps using L's native blobs: same integers)."""
+    wl = L.wl
+    rows = 2 * wl.F
+    out = torch.zeros((L.pool_gu.shape[0], rows * synth.row_bytes(dst_type, wl.N)), dtype=torch.uint8, device=device)
+    tab = pointer_table(out)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    m.transcode_cb(L.gu_t, L.cb_gu_d, dst_type, wl.N, rows, L.tab_gu, tab, err)
+    assert int(err.item()) == 0
+    return replace(L, gu_t=dst_type, pool_gu=out, tab_gu=tab, cb_gu_d=None)
 
 
 def host_blobs(L: Layer, experts, role: str):

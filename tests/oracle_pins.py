@@ -21,7 +21,7 @@ from __future__ import annotations
 
 import numpy as np
 
-Q8_0, Q4B, NL4, CB2, CB3 = 1, 2, 3, 4, 5
+Q8_0, Q4B, NL4, CB2, CB3, CB3X, CB2X = 1, 2, 3, 4, 5, 6, 7
 
 
 def _h(v):
@@ -269,6 +269,54 @@ def check_formats_bruteforce(o):
             assert np.array_equal(isum, (v.reshape(-1, 32) * q).sum(axis=1))
 
 
+# ------------------------------------------------------------------ transcoded slot layouts
+
+def check_slots(o):
+    """Load-time slot layouts hold exactly the native integers and scales (round trip through
+    the native decode), in the documented byte positions (hand-worked), and refuse values that
+    do not fit."""
+    rng = np.random.Generator(np.random.PCG64(29))
+    K = 512
+    for src, dst in ((CB3, CB3X), (CB2, CB2X), (CB2, CB3X)):
+        cb = _cb_for(src, rng)
+        for _ in range(4):
+            row = _random_row(src, K, rng)
+            t, rc = o.transcode_row(src, row, K, cb, dst)
+            assert rc == 0 and len(t) == o.row_bytes(dst, K)
+            assert np.array_equal(o.int_weights(dst, t, K), o.int_weights(src, row, K, cb)), (src, dst)
+            assert np.array_equal(o.dequant_row(dst, t, K), o.dequant_row(src, row, K, cb))
+            x = rng.standard_normal((1, K)).astype(np.float32)
+            xq = o.quantize_q8_1(x)[0]
+            assert np.array_equal(o.block_isum(dst, t, K, xq), o.block_isum(src, row, K, xq, cb))
+            assert o.row_dot(dst, t, K, xq) == o.row_dot(src, row, K, xq, cb)
+    # hand-worked CB3X bytes: CB3 weights 0..3 = +1 -3 +5 +7, weight 16 = -15, weight 17 = +15
+    g3 = np.ones((256, 4), np.int8); g3[7] = [1, 3, 5, 7]; g3[9] = [15, 15, 1, 1]
+    sb = np.zeros(102, np.uint8)
+    _wr16(sb, 0, _h(0.5))
+    sb[2 + 0] = 7; sb[66 + 0] = 0x02          # weight 1 negated
+    sb[2 + 4] = 9; sb[66 + 2] = 0x01          # group 4 = weights 16..19, weight 16 negated
+    sb[98:102] = [0x21, 0x43, 0x65, 0x87]
+    t, rc = o.transcode_row(CB3, sb, 256, g3, CB3X)
+    assert rc == 0
+    # u = (v-1)/2 + 8: +1 -> 8, -3 -> 6, +5 -> 10, +7 -> 11, -15 -> 0, +15 -> 15, +1 -> 8
+    assert list(t[0:4]) == [8 | (0 << 4), 6 | (15 << 4), 10 | (8 << 4), 11 | (8 << 4)], list(t[0:4])
+    assert list(t[128:136]) == [sb[0], sb[1], 0, 0, 0x21, 0x43, 0x65, 0x87]
+    # hand-worked CB2X bytes: CB2 group 0 = weights 0..7 from grid2[5] = [3,-3,1,-1,3,3,-1,1]
+    g2 = np.ones((256, 8), np.int8); g2[5] = [3, -3, 1, -1, 3, 3, -1, 1]
+    sb = np.zeros(70, np.uint8)
+    sb[2 + 0] = 5; sb[34 + 0] = 0x80          # weight 7 negated -> -1
+    t, rc = o.transcode_row(CB2, sb, 256, g2, CB2X)
+    assert rc == 0
+    # u = (v-1)/2 + 2: 3 -> 3, -3 -> 0, 1 -> 2, -1 -> 1; weights 0..7 sit in bits 0-1 of bytes 0..7
+    assert [int(v) & 3 for v in t[0:8]] == [3, 0, 2, 1, 3, 3, 1, 1], [int(v) & 3 for v in t[0:8]]
+    assert [(int(v) >> 2) & 3 for v in t[0:8]] == [2] * 8  # weights 8..15: grid row 0, all +1 -> u = 2
+    # out-of-range values are refused
+    g_big = g3.copy(); g_big[7] = [17, 3, 5, 7]
+    sb2 = np.zeros(102, np.uint8); sb2[2] = 7
+    assert o.transcode_row(CB3, sb2, 256, g_big, CB3X)[1] == -1
+    assert o.transcode_row(CB2, sb, 256, np.full((256, 8), 5, np.int8), CB2X)[1] == -1
+
+
 # ------------------------------------------------------------------ grouping
 
 def check_route_hand(o):
@@ -365,5 +413,5 @@ def check_swiglu_q8_1(o):
 
 
 ALL_CHECKS = [check_f16, check_exp, check_silu, check_q8_1, check_formats_hand, check_formats_onehot,
-              check_formats_bruteforce, check_route_hand, check_route_invariants, check_grouped_invariants,
+              check_formats_bruteforce, check_slots, check_route_hand, check_route_invariants, check_grouped_invariants,
               check_swiglu_q8_1]

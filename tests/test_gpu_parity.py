@@ -38,12 +38,17 @@ def test_quantize_q8_1_bitexact(m, orc):
 
 # ------------------------------------------------------------------ a2/a4 integer block sums
 
-@pytest.mark.parametrize("typ", [synth.Q8_0, synth.Q4B, synth.NL4, synth.CB2, synth.CB3])
+@pytest.mark.parametrize("typ", [synth.Q8_0, synth.Q4B, synth.NL4, synth.CB2, synth.CB3, synth.CB3X, synth.CB2X])
 @pytest.mark.parametrize("K", [256, 768, 2560])
 def test_block_isum_bitexact(m, orc, typ, K):
     rows = 24
-    blob = synth.weight_blobs(typ, rows, K, 1, synth.derive_key(typ, K), "cpu")[0]
-    cb = synth.codebook(typ, K + typ)
+    src = {synth.CB3X: synth.CB3, synth.CB2X: synth.CB2}.get(typ, typ)
+    blob = synth.weight_blobs(src, rows, K, 1, synth.derive_key(src, K), "cpu")[0]
+    cb = synth.codebook(src, K + src)
+    if src != typ:  # slot layouts: the oracle's own transcoding of the native blob
+        t, rc = orc.transcode_blob(src, blob.numpy(), K, rows, cb, typ)
+        assert rc == 0
+        blob, cb = torch.from_numpy(t), None
     x = synth.activations(1, K, K * 3 + typ, outliers=0.01)
     xq = orc.quantize_q8_1(x)
     pad = torch.zeros(blob.numel() + 64, dtype=torch.uint8)
@@ -57,6 +62,32 @@ def test_block_isum_bitexact(m, orc, typ, K):
     for r in range(rows):
         want = orc.block_isum(typ, b[r * rb:(r + 1) * rb], K, xq[0], cb)
         assert np.array_equal(got[r], want), (r, np.nonzero(got[r] != want))
+
+
+# ------------------------------------------------------------------ load-time transcoding
+
+@pytest.mark.parametrize("src,dst,K", [(synth.CB3, synth.CB3X, 2560), (synth.CB2, synth.CB2X, 768),
+                                       (synth.CB2, synth.CB3X, 512), (synth.CB3, synth.CB3X, 768)])
+def test_transcode_bitexact(m, orc, src, dst, K):
+    rows, nb = 16, 3
+    blobs = synth.weight_blobs(src, rows, K, nb, synth.derive_key(src, dst, K), "cuda")
+    cb = synth.codebook(src, 5 + K)
+    cbd = torch.from_numpy(np.ascontiguousarray(cb).ravel()).cuda()
+    out = torch.zeros((nb, rows * synth.row_bytes(dst, K)),
+                      dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.transcode_cb(src, cbd, dst, K, rows, H.pointer_table(blobs), H.pointer_table(out), err)
+    got = out.cpu().numpy()
+    assert int(err.item()) == 0
+    for b in range(nb):
+        want, rc = orc.transcode_blob(src, blobs[b].cpu().numpy(), K, rows, cb, dst)
+        assert rc == 0 and np.array_equal(got[b], want), b
+    # a grid value outside the slot's range is reported
+    bad = cb.copy()
+    bad.ravel()[0] = 17 if dst == synth.CB3X else 5
+    m.transcode_cb(src, torch.from_numpy(np.ascontiguousarray(bad).ravel()).cuda(), dst, K, rows,
+                   H.pointer_table(blobs), H.pointer_table(out), err)
+    assert int(err.item()) & 32
 
 
 # ------------------------------------------------------------------ a0: routing
@@ -131,14 +162,18 @@ def _stage_inputs(orc, L, r):
     return xq, hq
 
 
-CASES = [("tiny", (synth.Q8_0, synth.Q8_0), 1), ("verify", (synth.CB2, synth.NL4), 4),
-         ("window48", (synth.CB3, synth.NL4), 1), ("window48", (synth.CB3, synth.NL4), 3)]
+# (workload, (gate/up, down), T, slot layout the gate/up pool is transcoded to or None)
+CASES = [("tiny", (synth.Q8_0, synth.Q8_0), 1, None), ("verify", (synth.CB2, synth.NL4), 4, None),
+         ("window48", (synth.CB3, synth.NL4), 1, None), ("window48", (synth.CB3, synth.NL4), 3, None),
+         ("window48", (synth.CB3, synth.NL4), 4, synth.CB3X), ("verify", (synth.CB2, synth.NL4), 4, synth.CB2X)]
+CASE_IDS = [f"{c[0]}-T{c[2]}" + (f"-{synth.NAMES[c[3]]}" if c[3] else "") for c in CASES]
 
 
-@pytest.mark.parametrize("wname,pair,T", CASES, ids=[f"{c[0]}-T{c[2]}" for c in CASES])
-def test_grouped_stages(m, orc, wname, pair, T):
+@pytest.mark.parametrize("wname,pair,T,xt", CASES, ids=CASE_IDS)
+def test_grouped_stages(m, orc, wname, pair, T, xt):
     wl = synth.WORKLOADS[wname]
-    L = H.make_layer(wl, pair, T)
+    L0 = H.make_layer(wl, pair, T)
+    L = H.transcoded(m, L0, xt) if xt else L0
     r = orc.route_group(L.ids, wl.E)
     G, n = r["n_groups"], T * wl.k
     B = H.make_bufs(L)
@@ -148,10 +183,10 @@ def test_grouped_stages(m, orc, wname, pair, T):
     xq_d = torch.from_numpy(xq).cuda()
     m.grouped_gu(L.gu_t, L.cb_gu_d, wl.N, wl.F, L.tab_gu, wl.E, B.grp_expert, B.grp_start, B.n_groups,
                  B.cap_groups, 0, xq_d, B.ent_src, B.cap_entries, B.gu, B.err)
-    gub = H.host_blobs(L, r["grp_expert"], "gu")
+    gub = H.host_blobs(L0, r["grp_expert"], "gu")
     ref = np.full((n, 2 * wl.F), np.nan)
-    orc.grouped_gemv(L.gu_t, wl.N, 2 * wl.F, gub, r["grp_expert"], r["grp_start"], G, xq, ent_in=r["ent_src"],
-                     out=ref, cb=L.cb_gu)
+    orc.grouped_gemv(L0.gu_t, wl.N, 2 * wl.F, gub, r["grp_expert"], r["grp_start"], G, xq, ent_in=r["ent_src"],
+                     out=ref, cb=L0.cb_gu)
     got = B.gu.cpu().numpy()
     assert H.rel_err(got, ref) <= TOL
     # down on oracle-made hq, scattered destinations
@@ -177,11 +212,12 @@ def _e2e(m, orc, L, grid_groups=0, flags=1):
     return B
 
 
-@pytest.mark.parametrize("wname,pair,T", CASES, ids=[f"{c[0]}-T{c[2]}" for c in CASES])
-def test_expert_grouped_end_to_end(m, orc, wname, pair, T):
+@pytest.mark.parametrize("wname,pair,T,xt", CASES, ids=CASE_IDS)
+def test_expert_grouped_end_to_end(m, orc, wname, pair, T, xt):
     wl = synth.WORKLOADS[wname]
-    L = H.make_layer(wl, pair, T)
-    ref = H.oracle_call(orc, L)
+    L0 = H.make_layer(wl, pair, T)
+    L = H.transcoded(m, L0, xt) if xt else L0
+    ref = H.oracle_call(orc, L0)
     B = _e2e(m, orc, L)
     assert int(B.err.item()) == 0
     assert np.array_equal(B.xq.cpu().numpy(), ref["xq"])

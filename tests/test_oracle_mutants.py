@@ -16,6 +16,7 @@ PLANTS = {
     "ORC_PLANT_Q4B_MIN": "Q4B minimum term dropped",
     "ORC_PLANT_ROUTE_ORDER": "entries of a group ordered by slot first",
     "ORC_PLANT_ENTRY_ROW": "gate/up reads the entry index instead of its token row",
+    "ORC_PLANT_SLOT_ORDER": "4-bit slot codes read interleaved",
 }
 
 
