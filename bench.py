@@ -265,6 +265,7 @@ def run_ours(args, rank, world):
 
     # ---- dominant kernel (grouped gate/up) timed on its own, T = 4, all 48 layers per launch set
     roof = gate_up_roofline(m, wins[4], bytes_t[4], hbm_peak, peak_kind, s)
+    breakdown = {f"T{T}": step_breakdown(m, wins[T], s) for T in (1, 4)}
 
     # ---- end to end: pinned host inputs -> device, the window graphs, outputs -> host
     e2e = end_to_end(wins, args, s, world, dev)
@@ -280,7 +281,7 @@ def run_ours(args, rank, world):
                    "l2": "inputs larger than L2 (>= 1 GB of weights per window), no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "per_T": per_T, "native_layout": {"gate_up": "CB3 (read directly)", "per_T": native},
-        "roofline": roof, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+        "roofline": roof, "step_us_per_layer_alone": breakdown, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
         "setup_s": round(setup_s, 1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -313,6 +314,47 @@ def gate_up_roofline(m, w, bytes_t, hbm_peak, peak_kind, s):
             "traffic": None, "peak_kind": peak_kind, "bytes_per_launch": int(per_launch),
             "streamed_bytes_per_launch": int(streamed), "streamed_GBps": round(streamed / dur_s / 1e9, 1),
             "us_per_launch": round(dur_s * 1e6, 2)}
+
+
+def step_breakdown(m, w, s, reps=5):
+    """Each step of the window alone: a CUDA graph of that step's 48 launches (no PDL), replayed
+    with CUDA events on the launching stream: GPU microseconds per launch. The per-layer sum
+    exceeds the window time / 48 because the window graph chains kernels with programmatic
+    dependent launch."""
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    n = w.T * WL.k
+    s = None  # launch on the current stream (the capture stream inside torch.cuda.graph)
+    steps = {
+        "route": lambda l: m.route_group(w.ids[l], WL.E, 0, w.ge[l], w.gs[l], w.ng[l], w.es[l], w.ed[l], w.err,
+                                         stream=s),
+        "quantize": lambda l: m.quantize_q8_1(w.x[l], w.xq[l], stream=s),
+        "gate_up": lambda l: m.grouped_gu(w.gu_type, w.calls[l]._keep[0], WL.N, WL.F, w.calls[l]._keep[2], WL.E,
+                                          w.ge[l], w.gs[l], w.ng[l], n, 0, w.xq[l], w.es[l], n, w.gu, w.err,
+                                          stream=s),
+        "swiglu_q8_1": lambda l: m.swiglu_q8_1(w.gu, WL.F, w.gs[l], w.ng[l], n, n, w.hq, w.err, stream=s),
+        "down": lambda l: m.grouped_down(DN_T, w.calls[l]._keep[1], WL.N, WL.F, w.calls[l]._keep[3], WL.E, w.ge[l],
+                                         w.gs[l], w.ng[l], n, 0, w.hq, n, w.ed[l], w.out[l], w.err, stream=s),
+    }
+    out = {}
+    for name, f in steps.items():
+        for l in range(WL.layers):
+            f(l)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            for l in range(WL.layers):
+                f(l)
+        g.replay()
+        torch.cuda.synchronize()
+        cur = torch.cuda.current_stream()
+        a, b = ev(), ev()
+        a.record(cur)
+        for _ in range(reps):
+            g.replay()
+        b.record(cur)
+        torch.cuda.synchronize()
+        out[name] = round(a.elapsed_time(b) * 1e3 / (reps * WL.layers), 2)
+    return out
 
 
 def end_to_end(wins, args, s, world, dev):

@@ -27,7 +27,8 @@
  *    MOE_ERR_* bits into *err when err is not NULL; the offending group or entry is skipped (its
  *    rows are not written), *n_groups is clamped to cap_groups. Kernels never trap and never wait
  *    without a time limit.
- *  - Shapes: n_embd and n_ff are multiples of 256, at most 8192; cap_groups <= 1024.
+ *  - Shapes: n_embd and n_ff are multiples of 256, at most 8192; cap_groups <= 1024,
+ *    cap_entries <= 4096.
  *
  * Weight formats (this library's own byte layouts; the pages name real formats but print none).
  * Little-endian, fp16 fields are IEEE binary16. A row of K weights is K/32 blocks (K/256

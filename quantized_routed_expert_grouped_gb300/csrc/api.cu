@@ -13,6 +13,7 @@ namespace {
 
 constexpr int kSmemPerSm = 228 * 1024;
 constexpr int kMaxGroups = 1024;
+constexpr int kMaxEntries = 4096;
 
 bool cb_type(int t) { return t == MOE_CB2 || t == MOE_CB3; }
 bool valid_type(int t) { return t >= MOE_Q8_0 && t <= MOE_CB2X; }
@@ -43,11 +44,12 @@ int round_up(int v, int m) { return (v + m - 1) / m * m; }
 // rows per expert), filled into `a` and `p`. One CTA per SM: a producer warp and up to 15
 // consumer warps grouped in warp-sets; a set works on one tile (32 rows, lane = row) at a time,
 // its warps splitting the row's 256-weight chunks; as many sets as fit in 15 warps.
-int plan_gemv(int type, int K, int rows, int cap_groups, GemvArgs& a, GemvPlan& p) {
+int plan_gemv(int type, int K, int rows, int cap_groups, int cap_entries, int n_act_rows, GemvArgs& a,
+              GemvPlan& p) {
     const int nch = K / 256;
     const int64_t rb = moe_row_bytes(type, K);
     if (nch <= 0 || nch > 32 || rb <= 0 || rows <= 0 || rows % 8) return MOE_E_SHAPE;
-    if (cap_groups <= 0 || cap_groups > kMaxGroups) return MOE_E_CAP;
+    if (cap_groups <= 0 || cap_groups > kMaxGroups || cap_entries <= 0 || cap_entries > kMaxEntries) return MOE_E_CAP;
     const bool cb = cb_type(type);
     // chunks per warp: the smallest that gives the most consumer warps (at most 15; warp-sets
     // of WPS = ceil(nch / CPW) warps, TP = 15 / WPS sets)
@@ -61,9 +63,13 @@ int plan_gemv(int type, int K, int rows, int cap_groups, GemvArgs& a, GemvPlan& 
     const int WPS = (nch + CPW - 1) / CPW;
     const int RT = 32 * rb <= 96 * 1024 ? 32 : 16;
     const int nb = K / 32, nbp = nb + nb / 8;
-    const int actq = round_up(2 * 4 * 2 * nbp * 16, 128), act2 = round_up(2 * 4 * nb * 8, 128);
+    // activation rows: the whole matrix when it fits in 64 KB, else two 4-entry buffers
+    const int act_row = 2 * nbp * 16 + nb * 8;
+    const int act_cap = n_act_rows > 8 && n_act_rows * act_row <= 64 * 1024 ? n_act_rows : 8;
+    const int actq = round_up(act_cap * 2 * nbp * 16, 128), act2 = round_up(act_cap * nb * 8, 128);
     const int grp = round_up(24 * cap_groups + 8 * (cap_groups + 1), 128);
-    const int fixed = (cb ? 32768 : 0) + actq + act2 + grp + 256 + 512;
+    const int entb = round_up(8 * cap_entries, 128);
+    const int fixed = (cb ? 32768 : 0) + actq + act2 + grp + entb + 256 + 512;
     const int stage_bytes = round_up(static_cast<int>(RT * rb) + 16, 128);
     const int part_bytes = nch * 4 * RT * 4;
     for (int TP = 15 / WPS > 0 ? 15 / WPS : 1; TP >= 1; --TP) {
@@ -81,6 +87,8 @@ int plan_gemv(int type, int K, int rows, int cap_groups, GemvArgs& a, GemvPlan& 
         off += act2;
         a.off_grp = off;
         off += grp;
+        a.off_ent = off;
+        off += entb;
         a.off_bar = off;
         off += 256;
         a.off_misc = off;
@@ -101,6 +109,7 @@ int plan_gemv(int type, int K, int rows, int cap_groups, GemvArgs& a, GemvPlan& 
         a.part_bytes = part_bytes;
         a.nb = nb;
         a.nbp = nbp;
+        a.act_cap = act_cap;
         return MOE_OK;
     }
     return MOE_E_SHAPE;
@@ -133,7 +142,7 @@ cudaError_t launch_gemv(int type, const GemvArgs& a, int grid, int NT, int smem,
 // Persistent grid: every SM's resident CTAs, but no more than grid_groups x tiles per group.
 int run_gemv(int type, GemvArgs& a, int grid_groups, cudaStream_t s, bool pdl) {
     GemvPlan p;
-    int rc = plan_gemv(type, a.K, a.rows, a.cap_groups, a, p);
+    int rc = plan_gemv(type, a.K, a.rows, a.cap_groups, a.cap_entries, a.n_act_rows, a, p);
     if (rc != MOE_OK) return rc;
     int ctas = 0;
     if (occupancy(type, p.NT, p.smem, &ctas) != cudaSuccess || ctas < 1) return MOE_E_CUDA;

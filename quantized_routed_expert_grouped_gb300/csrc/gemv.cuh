@@ -288,28 +288,6 @@ __device__ __forceinline__ Tile next_tile(long long& cur, long long end, int rbp
     return Tile{g, off * 8, static_cast<int>(n) * 8};
 }
 
-// Group g's expert and entry range; false if the group is skipped (invalid data reported by
-// the calling thread when `report`, or simply empty).
-__device__ __forceinline__ bool group_ok(const GemvArgs& a, int g, int& x, int& e0, int& e1, bool report) {
-    x = a.grp_expert[g];
-    e0 = a.grp_start[g];
-    e1 = a.grp_start[g + 1];
-    if (x < 0 || x >= a.n_experts) {
-        if (report) set_err(a.err, MOE_ERR_EXPERT);
-        return false;
-    }
-    if (e0 < 0 || e1 < e0 || e1 > a.cap_entries) {
-        if (report) set_err(a.err, MOE_ERR_START);
-        return false;
-    }
-    if (e1 == e0) return false;
-    if (reinterpret_cast<uintptr_t>(a.w[x]) & 15u) {
-        if (report) set_err(a.err, MOE_ERR_ALIGN);
-        return false;
-    }
-    return true;
-}
-
 // Per-group facts cached in shared memory for the whole launch: expert, entry range, cost per
 // 8-row block (0 for a skipped group), and the inclusive prefix of the group costs.
 struct GroupInfo {
@@ -378,75 +356,75 @@ __device__ __forceinline__ void load_table(const GemvArgs& a, uint32_t tab[4]) {
     }
 }
 
-// Entry bookkeeping for a batch of up to 4 entries (one thread) in misc block `ent` (16 ints):
-// [4+s] ok, [8+s] activation row, [12+s] output row.
-__device__ __forceinline__ void setup_entries(const GemvArgs& a, int* misc, int b0, int ne) {
-    for (int s = 0; s < kMaxEntriesPerPass; ++s) {
-        int ok = 0, in = 0, o = 0;
-        if (s < ne) {
-            const int e = b0 + s;
-            in = a.ent_in ? a.ent_in[e] : e;
-            o = a.ent_out ? a.ent_out[e] : e;
-            ok = in >= 0 && in < a.n_act_rows && o >= 0 && o < a.out_rows;
-            if (!ok) set_err(a.err, MOE_ERR_ENTRY);
-        }
-        misc[4 + s] = ok;
-        misc[8 + s] = in;
-        misc[12 + s] = o;
+// Staged activations: slot i of the shared-memory act region holds one q8_1 row as 16-byte code
+// halves (q[(i*2 + h)*nbp + bp], bp = b + b/8: conflict-free 128-bit loads) and (d, aux) pairs
+// (q2[i*nb + b]); aux = exact code sum S times the format's factor (CB: S, slots: -(2 bias - 1) S),
+// s (Q4B) or 0. Row `src` < 0 stages zeros.
+template <int TYPE>
+__device__ __forceinline__ void stage_block(const GemvArgs& a, uint8_t* smem, int slot, int src, int b) {
+    int4* q = reinterpret_cast<int4*>(smem + a.off_actq);
+    float2* q2 = reinterpret_cast<float2*>(smem + a.off_act2);
+    const int bp = b + (b >> 3);
+    uint32_t w[9];
+    if (src >= 0) {
+        const uint32_t* p = reinterpret_cast<const uint32_t*>(a.act + static_cast<int64_t>(src) * a.nb + b);
+#pragma unroll
+        for (int k = 0; k < 9; ++k) w[k] = __ldg(p + k);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 9; ++k) w[k] = 0;
+    }
+    if constexpr (TYPE == MOE_NL4) {
+#pragma unroll
+        for (int k = 1; k < 9; ++k) w[k] = prmt(w[k], 0u, 0x3120u);
+    }
+    q[(slot * 2 + 0) * a.nbp + bp] = make_int4(w[1], w[2], w[3], w[4]);
+    q[(slot * 2 + 1) * a.nbp + bp] = make_int4(w[5], w[6], w[7], w[8]);
+    float aux = 0.0f;
+    if constexpr (Fmt<TYPE>::CB || Fmt<TYPE>::SLOT) {
+        int S = 0;
+#pragma unroll
+        for (int k = 1; k < 9; ++k) S = dp4a(w[k], 0x01010101u, S);
+        // CB: sum s g q = 2 dot(x ^ mask, q) + S; slots: = 2 dot(u, q) - (2 bias - 1) S
+        if constexpr (Fmt<TYPE>::SLOT) S *= -(2 * Fmt<TYPE>::BIAS - 1);
+        aux = __int_as_float(S);
+    } else if constexpr (TYPE == MOE_Q4B) {
+        aux = h2f_bits(w[0] >> 16);
+    }
+    q2[slot * a.nb + b] = make_float2(h2f_bits(w[0]), aux);
+}
+
+// All n rows of the activation matrix into slots 0..n-1.
+template <int TYPE>
+__device__ __forceinline__ void stage_all(const GemvArgs& a, uint8_t* smem, int n, int t, int nt) {
+    for (int i = t; i < n * a.nb; i += nt) {
+        const int r = i / a.nb;
+        stage_block<TYPE>(a, smem, r, r, i - r * a.nb);
     }
 }
 
-// q8_1 rows of `ne` entries -> codes as 16-byte halves, (d, aux) as float2: aux = exact code sum
-// (CB formats), s (Q4B) or 0.
+// The activation rows of entries e0 .. e0+ne-1 (ent[e].x, -1 when invalid) into slots slot0 ...
 template <int TYPE>
-__device__ __forceinline__ void stage_act(const GemvArgs& a, uint8_t* smem, const int* misc, int ne, int t, int nt,
-                                          int buf = 0) {
-    int4* q = reinterpret_cast<int4*>(smem + a.off_actq) + buf * (kMaxEntriesPerPass * 2 * a.nbp);
-    float2* q2 = reinterpret_cast<float2*>(smem + a.off_act2) + buf * (kMaxEntriesPerPass * a.nb);
+__device__ __forceinline__ void stage_entries(const GemvArgs& a, uint8_t* smem, const int2* ent, int e0, int ne,
+                                              int slot0, int t, int nt) {
     for (int i = t; i < ne * a.nb; i += nt) {
-        const int s = i / a.nb, b = i - s * a.nb, bp = b + (b >> 3);
-        uint32_t w[9];
-        if (misc[4 + s]) {
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(a.act + static_cast<int64_t>(misc[8 + s]) * a.nb + b);
-#pragma unroll
-            for (int k = 0; k < 9; ++k) w[k] = __ldg(src + k);
-        } else {
-#pragma unroll
-            for (int k = 0; k < 9; ++k) w[k] = 0;
-        }
-        if constexpr (TYPE == MOE_NL4) {
-#pragma unroll
-            for (int k = 1; k < 9; ++k) w[k] = prmt(w[k], 0u, 0x3120u);
-        }
-        q[(s * 2 + 0) * a.nbp + bp] = make_int4(w[1], w[2], w[3], w[4]);
-        q[(s * 2 + 1) * a.nbp + bp] = make_int4(w[5], w[6], w[7], w[8]);
-        float aux = 0.0f;
-        if constexpr (Fmt<TYPE>::CB || Fmt<TYPE>::SLOT) {
-            int S = 0;
-#pragma unroll
-            for (int k = 1; k < 9; ++k) S = dp4a(w[k], 0x01010101u, S);
-            // CB: sum s g q = 2 dot(x ^ mask, q) + S; slots: = 2 dot(u, q) - (2 bias - 1) S
-            if constexpr (Fmt<TYPE>::SLOT) S *= -(2 * Fmt<TYPE>::BIAS - 1);
-            aux = __int_as_float(S);
-        } else if constexpr (TYPE == MOE_Q4B) {
-            aux = h2f_bits(w[0] >> 16);
-        }
-        q2[s * a.nb + b] = make_float2(h2f_bits(w[0]), aux);
+        const int s = i / a.nb;
+        stage_block<TYPE>(a, smem, slot0 + s, ent[e0 + s].x, i - s * a.nb);
     }
 }
 
 template <int NE>
-__device__ __forceinline__ void load_act(const GemvArgs& a, const uint8_t* smem, int b, uint32_t A[NE][8], float dx[NE],
-                                         float aux[NE], int buf = 0) {
-    const int4* q = reinterpret_cast<const int4*>(smem + a.off_actq) + buf * (kMaxEntriesPerPass * 2 * a.nbp);
-    const float2* q2 = reinterpret_cast<const float2*>(smem + a.off_act2) + buf * (kMaxEntriesPerPass * a.nb);
+__device__ __forceinline__ void load_act(const GemvArgs& a, const uint8_t* smem, int b, const int slots[NE],
+                                         uint32_t A[NE][8], float dx[NE], float aux[NE]) {
+    const int4* q = reinterpret_cast<const int4*>(smem + a.off_actq);
+    const float2* q2 = reinterpret_cast<const float2*>(smem + a.off_act2);
     const int bp = b + (b >> 3);
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
-        const int4 lo = q[(e * 2 + 0) * a.nbp + bp], hi = q[(e * 2 + 1) * a.nbp + bp];
+        const int4 lo = q[(slots[e] * 2 + 0) * a.nbp + bp], hi = q[(slots[e] * 2 + 1) * a.nbp + bp];
         A[e][0] = lo.x; A[e][1] = lo.y; A[e][2] = lo.z; A[e][3] = lo.w;
         A[e][4] = hi.x; A[e][5] = hi.y; A[e][6] = hi.z; A[e][7] = hi.w;
-        const float2 v = q2[e * a.nb + b];
+        const float2 v = q2[slots[e] * a.nb + b];
         dx[e] = v.x;
         aux[e] = v.y;
     }
@@ -471,10 +449,10 @@ __device__ __forceinline__ int dot8(const uint32_t W[8], const uint32_t A[8]) {
 // All lanes of a warp read the same activation block at the same time (broadcast loads).
 template <int TYPE, int NE, int j>
 __device__ __forceinline__ void cb_block(const GemvArgs& a, const uint8_t* smem, const CBRow<TYPE>& row, int c,
-                                         uint32_t loff, int buf, float acc[NE]) {
+                                         uint32_t loff, const int* slots, float acc[NE]) {
     uint32_t A[NE][8];
     float dx[NE], sq[NE];
-    load_act<NE>(a, smem, c * 8 + j, A, dx, sq, buf);
+    load_act<NE>(a, smem, c * 8 + j, slots, A, dx, sq);
     uint32_t W[8];
     const int ls = cb_decode<TYPE, j>(row, smem, loff, W);
 #pragma unroll
@@ -486,10 +464,11 @@ __device__ __forceinline__ void cb_block(const GemvArgs& a, const uint8_t* smem,
 
 template <int TYPE, int NE, int j>
 __device__ __forceinline__ void plain_block(const GemvArgs& a, const uint8_t* smem, const uint8_t* chunk,
-                                            const uint32_t* raw, const uint32_t tab[4], int c, int buf, float acc[NE]) {
+                                            const uint32_t* raw, const uint32_t tab[4], int c, const int* slots,
+                                            float acc[NE]) {
     uint32_t A[NE][8];
     float dx[NE], aux[NE];
-    load_act<NE>(a, smem, c * 8 + j, A, dx, aux, buf);
+    load_act<NE>(a, smem, c * 8 + j, slots, A, dx, aux);
     uint32_t W[8];
     float dw, mw = 0.0f;
     if constexpr (TYPE == MOE_NL4) nl4_decode<j>(raw, tab, W, dw);
@@ -503,10 +482,10 @@ __device__ __forceinline__ void plain_block(const GemvArgs& a, const uint8_t* sm
 
 template <int TYPE, int NE, int j>
 __device__ __forceinline__ void slot_block(const GemvArgs& a, const uint8_t* smem, const uint32_t* q, uint32_t subw,
-                                           int c, int buf, float acc[NE]) {
+                                           int c, const int* slots, float acc[NE]) {
     uint32_t A[NE][8];
     float dx[NE], aux[NE];
-    load_act<NE>(a, smem, c * 8 + j, A, dx, aux, buf);
+    load_act<NE>(a, smem, c * 8 + j, slots, A, dx, aux);
     uint32_t W[8];
     slot_decode<TYPE>(q, W);
     const int ls = 2 * static_cast<int>((subw >> (8 * (j >> 1) + 4 * (j & 1))) & 15u) + 1;
@@ -529,31 +508,31 @@ __device__ __forceinline__ void ld16(const uint8_t* p, bool al16, uint32_t q[4])
 }
 
 template <int TYPE, int NE>
-__device__ __forceinline__ void slot_chunk(const GemvArgs& a, const uint8_t* smem, const uint8_t* rowp, int c, int buf,
-                                           float acc[NE]) {
+__device__ __forceinline__ void slot_chunk(const GemvArgs& a, const uint8_t* smem, const uint8_t* rowp, int c,
+                                           const int* slots, float acc[NE]) {
     const uint2 sc = *reinterpret_cast<const uint2*>(rowp + a.nch * Fmt<TYPE>::CHUNK + c * 8);
     const float D = h2f_bits(sc.x);
     const uint8_t* codes = rowp + c * Fmt<TYPE>::CHUNK;
     const bool al16 = (a.row_bytes & 15) == 0;
     uint32_t q[4];
     if constexpr (TYPE == MOE_CB3X) {  // 16 bytes per sub-block
-        ld16(codes + 0, al16, q); slot_block<TYPE, NE, 0>(a, smem, q, sc.y, c, buf, acc);
-        ld16(codes + 16, al16, q); slot_block<TYPE, NE, 1>(a, smem, q, sc.y, c, buf, acc);
-        ld16(codes + 32, al16, q); slot_block<TYPE, NE, 2>(a, smem, q, sc.y, c, buf, acc);
-        ld16(codes + 48, al16, q); slot_block<TYPE, NE, 3>(a, smem, q, sc.y, c, buf, acc);
-        ld16(codes + 64, al16, q); slot_block<TYPE, NE, 4>(a, smem, q, sc.y, c, buf, acc);
-        ld16(codes + 80, al16, q); slot_block<TYPE, NE, 5>(a, smem, q, sc.y, c, buf, acc);
-        ld16(codes + 96, al16, q); slot_block<TYPE, NE, 6>(a, smem, q, sc.y, c, buf, acc);
-        ld16(codes + 112, al16, q); slot_block<TYPE, NE, 7>(a, smem, q, sc.y, c, buf, acc);
+        ld16(codes + 0, al16, q); slot_block<TYPE, NE, 0>(a, smem, q, sc.y, c, slots, acc);
+        ld16(codes + 16, al16, q); slot_block<TYPE, NE, 1>(a, smem, q, sc.y, c, slots, acc);
+        ld16(codes + 32, al16, q); slot_block<TYPE, NE, 2>(a, smem, q, sc.y, c, slots, acc);
+        ld16(codes + 48, al16, q); slot_block<TYPE, NE, 3>(a, smem, q, sc.y, c, slots, acc);
+        ld16(codes + 64, al16, q); slot_block<TYPE, NE, 4>(a, smem, q, sc.y, c, slots, acc);
+        ld16(codes + 80, al16, q); slot_block<TYPE, NE, 5>(a, smem, q, sc.y, c, slots, acc);
+        ld16(codes + 96, al16, q); slot_block<TYPE, NE, 6>(a, smem, q, sc.y, c, slots, acc);
+        ld16(codes + 112, al16, q); slot_block<TYPE, NE, 7>(a, smem, q, sc.y, c, slots, acc);
     } else {  // 8 bytes per sub-block: two sub-blocks per 16-byte load
-        ld16(codes + 0, al16, q); slot_block<TYPE, NE, 0>(a, smem, q, sc.y, c, buf, acc);
-        slot_block<TYPE, NE, 1>(a, smem, q + 2, sc.y, c, buf, acc);
-        ld16(codes + 16, al16, q); slot_block<TYPE, NE, 2>(a, smem, q, sc.y, c, buf, acc);
-        slot_block<TYPE, NE, 3>(a, smem, q + 2, sc.y, c, buf, acc);
-        ld16(codes + 32, al16, q); slot_block<TYPE, NE, 4>(a, smem, q, sc.y, c, buf, acc);
-        slot_block<TYPE, NE, 5>(a, smem, q + 2, sc.y, c, buf, acc);
-        ld16(codes + 48, al16, q); slot_block<TYPE, NE, 6>(a, smem, q, sc.y, c, buf, acc);
-        slot_block<TYPE, NE, 7>(a, smem, q + 2, sc.y, c, buf, acc);
+        ld16(codes + 0, al16, q); slot_block<TYPE, NE, 0>(a, smem, q, sc.y, c, slots, acc);
+        slot_block<TYPE, NE, 1>(a, smem, q + 2, sc.y, c, slots, acc);
+        ld16(codes + 16, al16, q); slot_block<TYPE, NE, 2>(a, smem, q, sc.y, c, slots, acc);
+        slot_block<TYPE, NE, 3>(a, smem, q + 2, sc.y, c, slots, acc);
+        ld16(codes + 32, al16, q); slot_block<TYPE, NE, 4>(a, smem, q, sc.y, c, slots, acc);
+        slot_block<TYPE, NE, 5>(a, smem, q + 2, sc.y, c, slots, acc);
+        ld16(codes + 48, al16, q); slot_block<TYPE, NE, 6>(a, smem, q, sc.y, c, slots, acc);
+        slot_block<TYPE, NE, 7>(a, smem, q + 2, sc.y, c, slots, acc);
     }
 #pragma unroll
     for (int e = 0; e < NE; ++e) acc[e] = __fmul_rn(D, acc[e]);
@@ -561,24 +540,24 @@ __device__ __forceinline__ void slot_chunk(const GemvArgs& a, const uint8_t* sme
 
 template <int TYPE, int NE>
 __device__ __forceinline__ void lane_chunk(const GemvArgs& a, const uint8_t* smem, const uint8_t* tile, int row, int c,
-                                           uint32_t loff, const uint32_t tab[4], int buf, float acc[NE]) {
+                                           uint32_t loff, const uint32_t tab[4], const int* slots, float acc[NE]) {
 #pragma unroll
     for (int e = 0; e < NE; ++e) acc[e] = 0.0f;
     const uint8_t* chunk = tile + row * a.row_bytes + c * Fmt<TYPE>::CHUNK;
     if constexpr (Fmt<TYPE>::SLOT) {
-        slot_chunk<TYPE, NE>(a, smem, tile + row * a.row_bytes, c, buf, acc);
+        slot_chunk<TYPE, NE>(a, smem, tile + row * a.row_bytes, c, slots, acc);
     } else if constexpr (Fmt<TYPE>::CB) {
         CBRow<TYPE> rr;
         rr.load(chunk);
         const float D = rr.D();
-        cb_block<TYPE, NE, 0>(a, smem, rr, c, loff, buf, acc);
-        cb_block<TYPE, NE, 1>(a, smem, rr, c, loff, buf, acc);
-        cb_block<TYPE, NE, 2>(a, smem, rr, c, loff, buf, acc);
-        cb_block<TYPE, NE, 3>(a, smem, rr, c, loff, buf, acc);
-        cb_block<TYPE, NE, 4>(a, smem, rr, c, loff, buf, acc);
-        cb_block<TYPE, NE, 5>(a, smem, rr, c, loff, buf, acc);
-        cb_block<TYPE, NE, 6>(a, smem, rr, c, loff, buf, acc);
-        cb_block<TYPE, NE, 7>(a, smem, rr, c, loff, buf, acc);
+        cb_block<TYPE, NE, 0>(a, smem, rr, c, loff, slots, acc);
+        cb_block<TYPE, NE, 1>(a, smem, rr, c, loff, slots, acc);
+        cb_block<TYPE, NE, 2>(a, smem, rr, c, loff, slots, acc);
+        cb_block<TYPE, NE, 3>(a, smem, rr, c, loff, slots, acc);
+        cb_block<TYPE, NE, 4>(a, smem, rr, c, loff, slots, acc);
+        cb_block<TYPE, NE, 5>(a, smem, rr, c, loff, slots, acc);
+        cb_block<TYPE, NE, 6>(a, smem, rr, c, loff, slots, acc);
+        cb_block<TYPE, NE, 7>(a, smem, rr, c, loff, slots, acc);
 #pragma unroll
         for (int e = 0; e < NE; ++e) acc[e] = __fmul_rn(D, acc[e]);
     } else {
@@ -590,14 +569,14 @@ __device__ __forceinline__ void lane_chunk(const GemvArgs& a, const uint8_t* sme
                 raw[4 * k] = v.x; raw[4 * k + 1] = v.y; raw[4 * k + 2] = v.z; raw[4 * k + 3] = v.w;
             }
         }
-        plain_block<TYPE, NE, 0>(a, smem, chunk, raw, tab, c, buf, acc);
-        plain_block<TYPE, NE, 1>(a, smem, chunk, raw, tab, c, buf, acc);
-        plain_block<TYPE, NE, 2>(a, smem, chunk, raw, tab, c, buf, acc);
-        plain_block<TYPE, NE, 3>(a, smem, chunk, raw, tab, c, buf, acc);
-        plain_block<TYPE, NE, 4>(a, smem, chunk, raw, tab, c, buf, acc);
-        plain_block<TYPE, NE, 5>(a, smem, chunk, raw, tab, c, buf, acc);
-        plain_block<TYPE, NE, 6>(a, smem, chunk, raw, tab, c, buf, acc);
-        plain_block<TYPE, NE, 7>(a, smem, chunk, raw, tab, c, buf, acc);
+        plain_block<TYPE, NE, 0>(a, smem, chunk, raw, tab, c, slots, acc);
+        plain_block<TYPE, NE, 1>(a, smem, chunk, raw, tab, c, slots, acc);
+        plain_block<TYPE, NE, 2>(a, smem, chunk, raw, tab, c, slots, acc);
+        plain_block<TYPE, NE, 3>(a, smem, chunk, raw, tab, c, slots, acc);
+        plain_block<TYPE, NE, 4>(a, smem, chunk, raw, tab, c, slots, acc);
+        plain_block<TYPE, NE, 5>(a, smem, chunk, raw, tab, c, slots, acc);
+        plain_block<TYPE, NE, 6>(a, smem, chunk, raw, tab, c, slots, acc);
+        plain_block<TYPE, NE, 7>(a, smem, chunk, raw, tab, c, slots, acc);
     }
 }
 
@@ -605,10 +584,10 @@ __device__ __forceinline__ void lane_chunk(const GemvArgs& a, const uint8_t* sme
 // part[(c*4 + e)*RT + row].
 template <int TYPE, int NE>
 __device__ __forceinline__ void warp_chunks(const GemvArgs& a, const uint8_t* smem, const uint8_t* tile, float* part,
-                                            int wi, int lane, uint32_t loff, const uint32_t tab[4], int buf) {
+                                            int wi, int lane, uint32_t loff, const uint32_t tab[4], const int* slots) {
     for (int c = wi; c < a.nch; c += a.WPS) {
         float acc[NE];
-        lane_chunk<TYPE, NE>(a, smem, tile, lane, c, loff, tab, buf, acc);
+        lane_chunk<TYPE, NE>(a, smem, tile, lane, c, loff, tab, slots, acc);
 #pragma unroll
         for (int e = 0; e < NE; ++e) part[(c * kMaxEntriesPerPass + e) * a.RT + lane] = acc[e];
     }
@@ -617,24 +596,26 @@ __device__ __forceinline__ void warp_chunks(const GemvArgs& a, const uint8_t* sm
 template <int TYPE>
 __device__ __forceinline__ void compute_batch(const GemvArgs& a, const uint8_t* smem, const uint8_t* tile, float* part,
                                               int ne, int wi, int lane, int nrows, uint32_t loff, const uint32_t tab[4],
-                                              int buf) {
+                                              const int slots[4]) {
     if (lane >= nrows) return;
-    // batches of 3 entries run the 4-entry code; the fourth result is never read
-    if (ne == 1) warp_chunks<TYPE, 1>(a, smem, tile, part, wi, lane, loff, tab, buf);
-    else if (ne == 2) warp_chunks<TYPE, 2>(a, smem, tile, part, wi, lane, loff, tab, buf);
-    else warp_chunks<TYPE, 4>(a, smem, tile, part, wi, lane, loff, tab, buf);
+    // batches of 3 entries run the 4-entry code (the fourth slot repeats the third; its result
+    // is never read)
+    if (ne == 1) warp_chunks<TYPE, 1>(a, smem, tile, part, wi, lane, loff, tab, slots);
+    else if (ne == 2) warp_chunks<TYPE, 2>(a, smem, tile, part, wi, lane, loff, tab, slots);
+    else warp_chunks<TYPE, 4>(a, smem, tile, part, wi, lane, loff, tab, slots);
 }
 
 // Fixed-order sum over the chunks (c = 0 .. nch-1) of each (row, entry), written to the entry's
 // output row.
-__device__ __forceinline__ void reduce_write(const GemvArgs& a, const float* part, const int* ment, const Tile& t,
-                                             int ne, int lane) {
+__device__ __forceinline__ void reduce_write(const GemvArgs& a, const float* part, const int2* ent, int b0,
+                                             const Tile& t, int ne, int lane) {
     if (lane >= t.nrows) return;
     for (int e = 0; e < ne; ++e) {
-        if (!ment[4 + e]) continue;
+        const int2 en = ent[b0 + e];
+        if (en.x < 0) continue;
         float s = part[e * a.RT + lane];
         for (int c = 1; c < a.nch; ++c) s = __fadd_rn(s, part[(c * kMaxEntriesPerPass + e) * a.RT + lane]);
-        a.out[static_cast<int64_t>(ment[12 + e]) * a.out_stride + t.row0 + lane] = s;
+        a.out[static_cast<int64_t>(en.y) * a.out_stride + t.row0 + lane] = s;
     }
 }
 
@@ -644,13 +625,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, NT = blockDim.x;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.off_bar);
     uint64_t* empty = full + a.stages;
-    // misc: [0] tiles issued, [1] abort flag, [32..47] / [48..63] entry blocks of act buffers 0 / 1,
-    // [64 + s] arrivals at ring slot s (the last warp of a tile sums its chunk partials)
+    // misc: [0] tiles issued, [1] abort flag, [2] n_groups, [64 + s] arrivals at ring slot s (the
+    // last warp of a tile sums its chunk partials)
     int* misc = reinterpret_cast<int*>(smem + a.off_misc);
     GroupInfo* gi = reinterpret_cast<GroupInfo*>(smem + a.off_grp);
     long long* cum = reinterpret_cast<long long*>(gi + a.cap_groups);
+    int2* ent = reinterpret_cast<int2*>(smem + a.off_ent);  // per entry: (act row or -1, out row)
     const int S = a.stages;
     const int rbpg = a.rows >> 3, rt8 = a.RT >> 3;
+    // the whole activation matrix fits in the act region: staged once, indexed by act row
+    const bool all_rows = a.n_act_rows <= a.act_cap;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -667,16 +651,51 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
     uint32_t tab[4];
     load_table<TYPE>(a, tab);
     if (!a.prefetch_before_wait) pdl_wait();
-    int G = *a.n_groups;
+
+    // One round of independent loads: the group count, every group slot and every entry slot (the
+    // arrays hold cap_groups / cap_entries items whatever *n_groups is), and, for gate/up, the
+    // activation rows (inputs after the wait).
+    if (tid == 0) misc[2] = *a.n_groups;
+    for (int g = tid; g < a.cap_groups; g += NT)
+        gi[g] = GroupInfo{nullptr, a.grp_expert[g], a.grp_start[g], a.grp_start[g + 1], 0};
+    for (int e = tid; e < a.cap_entries; e += NT) {
+        const int in = a.ent_in ? a.ent_in[e] : e;
+        const int o = a.ent_out ? a.ent_out[e] : e;
+        const bool ok = in >= 0 && in < a.n_act_rows && o >= 0 && o < a.out_rows;
+        ent[e] = make_int2(ok ? in : -1, o);
+    }
+    if (all_rows && !a.prefetch_before_wait) stage_all<TYPE>(a, smem, a.n_act_rows, tid, NT);
+    __syncthreads();
+    int G = misc[2];
     if (G < 0 || G > a.cap_groups) {
         if (blockIdx.x == 0 && tid == 0) set_err(a.err, MOE_ERR_NGROUPS);
         G = G < 0 ? 0 : a.cap_groups;
     }
-    // the group table, one group per thread, then the prefix of the costs (warp 0)
+    // validate the groups (one per thread), fetch their weight pointers, cost them
     for (int g = tid; g < G; g += NT) {
-        int x, e0, e1;
-        const bool ok = group_ok(a, g, x, e0, e1, blockIdx.x == 0);
-        gi[g] = GroupInfo{ok ? static_cast<const uint8_t*>(a.w[x]) : nullptr, x, e0, e1, ok ? a.alpha + (e1 - e0) : 0};
+        GroupInfo v = gi[g];
+        bool ok = true;
+        const bool rep = blockIdx.x == 0;
+        if (v.x < 0 || v.x >= a.n_experts) {
+            ok = false;
+            if (rep) set_err(a.err, MOE_ERR_EXPERT);
+        } else if (v.e0 < 0 || v.e1 < v.e0 || v.e1 > a.cap_entries) {
+            ok = false;
+            if (rep) set_err(a.err, MOE_ERR_START);
+        } else if (v.e1 == v.e0) {
+            ok = false;
+        } else {
+            v.ptr = static_cast<const uint8_t*>(a.w[v.x]);
+            if (reinterpret_cast<uintptr_t>(v.ptr) & 15u) {
+                ok = false;
+                if (rep) set_err(a.err, MOE_ERR_ALIGN);
+            } else if (rep) {
+                for (int e = v.e0; e < v.e1; ++e)
+                    if (ent[e].x < 0) set_err(a.err, MOE_ERR_ENTRY);
+            }
+        }
+        v.cost = ok ? a.alpha + (v.e1 - v.e0) : 0;
+        gi[g] = v;
     }
     __syncthreads();
     if (warp == 0) {
@@ -751,23 +770,23 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
     const int ct = tid - 32, cnt = a.CW * 32;
     const uint32_t loff = TYPE == MOE_CB3 ? lane * 4u : (lane & 15u) * 8u;
 
-    // A range spanning at most two groups of at most 4 entries each (the common case) has both
-    // groups' activations staged once, here, and every warp-set runs freely; otherwise warp-set 0
-    // alone walks the range and restages at every group (or 4-entry batch) change.
+    // Activations: staged already (gate/up) or now, after the wait (down), when they all fit;
+    // otherwise a range spanning at most two groups of at most 4 entries each has both groups'
+    // rows staged here, and any other range is walked by warp-set 0 alone, restaging at every
+    // group (or 4-entry batch) change.
     const int gA = static_cast<int>(rb0 / rbpg), gB = static_cast<int>((rb1 - 1) / rbpg);
     const int neA = gi[gA].e1 - gi[gA].e0, neB = gi[gB].e1 - gi[gB].e0;
-    const bool fast = gB - gA <= 1 && (gi[gA].cost == 0 || neA <= kMaxEntriesPerPass) &&
-                      (gi[gB].cost == 0 || neB <= kMaxEntriesPerPass);
-    if (fast) {
-        if (ct == 0) {
-            if (gi[gA].cost) setup_entries(a, misc + 32, gi[gA].e0, neA);
-            if (gB != gA && gi[gB].cost) setup_entries(a, misc + 48, gi[gB].e0, neB);
-        }
+    const bool two = !all_rows && gB - gA <= 1 && (gi[gA].cost == 0 || neA <= kMaxEntriesPerPass) &&
+                     (gi[gB].cost == 0 || neB <= kMaxEntriesPerPass);
+    const bool fast = all_rows || two;
+    if (all_rows && a.prefetch_before_wait) {
+        stage_all<TYPE>(a, smem, a.n_act_rows, ct, cnt);
         named_sync(1, cnt);
-        if (gi[gA].cost) stage_act<TYPE>(a, smem, misc + 32, neA, ct, cnt, 0);
-        if (gB != gA && gi[gB].cost) stage_act<TYPE>(a, smem, misc + 48, neB, ct, cnt, 1);
+    } else if (two) {
+        if (gi[gA].cost) stage_entries<TYPE>(a, smem, ent, gi[gA].e0, neA, 0, ct, cnt);
+        if (gB != gA && gi[gB].cost) stage_entries<TYPE>(a, smem, ent, gi[gB].e0, neB, kMaxEntriesPerPass, ct, cnt);
         named_sync(1, cnt);
-    } else if (set != 0) {
+    } else if (!fast && set != 0) {
         return;
     }
     const int TPe = fast ? a.TP : 1;
@@ -792,21 +811,29 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
             *reinterpret_cast<volatile int*>(misc + 1) = 1;
         }
         if (*reinterpret_cast<volatile int*>(misc + 1)) aborted = true;
-        // entry batches: one for a group of up to 4 entries (always in fast mode)
+        // entry batches: one for a group of up to 4 entries
         for (int b0 = g.e0; b0 < g.e1; b0 += kMaxEntriesPerPass) {
             const int ne = g.e1 - b0 < kMaxEntriesPerPass ? g.e1 - b0 : kMaxEntriesPerPass;
-            const int buf = fast && t.g != gA ? 1 : 0;
-            const int* ment = misc + 32 + 16 * buf;
+            int slots[4];
+            if (all_rows) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = ent[b0 + (e < ne ? e : ne - 1)].x;
+                    slots[e] = r < 0 ? 0 : r;
+                }
+            } else {
+                const int s0 = two && t.g != gA ? kMaxEntriesPerPass : 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) slots[e] = s0 + (e < ne ? e : ne - 1);
+            }
             if (!fast && (t.g != cur_g || b0 != cur_b0)) {
                 named_sync(1, scnt);
-                if (st == 0) setup_entries(a, misc + 32, b0, ne);
-                named_sync(1, scnt);
-                stage_act<TYPE>(a, smem, misc + 32, ne, st, scnt, 0);
+                stage_entries<TYPE>(a, smem, ent, b0, ne, 0, st, scnt);
                 named_sync(1, scnt);
                 cur_g = t.g;
                 cur_b0 = b0;
             }
-            if (!aborted) compute_batch<TYPE>(a, smem, tile, part, ne, wi, lane, t.nrows, loff, tab, buf);
+            if (!aborted) compute_batch<TYPE>(a, smem, tile, part, ne, wi, lane, t.nrows, loff, tab, slots);
             if (fast) {
                 // release the weights, then the set's last warp sums the chunk partials
                 __syncwarp();
@@ -819,7 +846,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (last) {
                     __threadfence_block();
-                    if (!aborted) reduce_write(a, part, ment, t, ne, lane);
+                    if (!aborted) reduce_write(a, part, ent, b0, t, ne, lane);
                     __syncwarp();
                     if (lane == 0) {
                         misc[64 + slot] = 0;
@@ -828,7 +855,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
                 }
             } else {
                 named_sync(1, scnt);
-                if (wi == 0 && !aborted) reduce_write(a, part, ment, t, ne, lane);
+                if (wi == 0 && !aborted) reduce_write(a, part, ent, b0, t, ne, lane);
                 named_sync(1, scnt);
             }
         }
@@ -854,14 +881,8 @@ template <int TYPE>
 __global__ void __launch_bounds__(256) isum_kernel(const GemvArgs a, const uint8_t* blob, int rows, int32_t* isum) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, NT = blockDim.x, lane = tid & 31;
-    int* misc = reinterpret_cast<int*>(smem + a.off_misc);
-    if (tid == 0) {
-        misc[4] = 1; misc[5] = misc[6] = misc[7] = 0;
-        misc[8] = 0;
-    }
-    __syncthreads();
     stage_codebook<TYPE>(a, smem, tid, NT);
-    stage_act<TYPE>(a, smem, misc, 1, tid, NT);
+    stage_all<TYPE>(a, smem, 1, tid, NT);
     __syncthreads();
     uint32_t tab[4];
     load_table<TYPE>(a, tab);
@@ -881,7 +902,8 @@ __global__ void __launch_bounds__(256) isum_kernel(const GemvArgs a, const uint8
             for (int k = 0; k < qb / 4; ++k) q[k] = ld32(codes + j * qb + 4 * k);
             uint32_t A[1][8];
             float dx[1], aux[1];
-            load_act<1>(a, smem, c * 8 + j, A, dx, aux);
+            const int slot0[1] = {0};
+            load_act<1>(a, smem, c * 8 + j, slot0, A, dx, aux);
             uint32_t W[8];
             slot_decode<TYPE>(q, W);
             out[j] = 2 * dot8(W, A[0]) + __float_as_int(aux[0]);
@@ -893,7 +915,8 @@ __global__ void __launch_bounds__(256) isum_kernel(const GemvArgs a, const uint8
             constexpr int j = decltype(jc)::value;
             uint32_t A[1][8];
             float dx[1], aux[1];
-            load_act<1>(a, smem, c * 8 + j, A, dx, aux);
+            const int slot0[1] = {0};
+            load_act<1>(a, smem, c * 8 + j, slot0, A, dx, aux);
             uint32_t W[8];
             cb_decode<TYPE, j>(row, smem, loff, W);
             int d = 0;
@@ -915,7 +938,8 @@ __global__ void __launch_bounds__(256) isum_kernel(const GemvArgs a, const uint8
             constexpr int j = decltype(jc)::value;
             uint32_t A[1][8];
             float dx[1], aux[1];
-            load_act<1>(a, smem, c * 8 + j, A, dx, aux);
+            const int slot0[1] = {0};
+            load_act<1>(a, smem, c * 8 + j, slot0, A, dx, aux);
             uint32_t W[8];
             float dw, mw;
             if constexpr (TYPE == MOE_NL4) nl4_decode<j>(raw, tab, W, dw);

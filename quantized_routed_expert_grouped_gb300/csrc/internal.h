@@ -60,7 +60,8 @@ struct GemvArgs {
     int prefetch_before_wait;  // weight tiles may be requested before griddepcontrol.wait
     // dynamic shared-memory layout (byte offsets; a CB codebook, when present, is at offset 0;
     // two activation buffers of kMaxEntriesPerPass entries; the group table holds cap_groups)
-    int off_ring, off_part, off_actq, off_act2, off_bar, off_misc, off_grp;
+    int off_ring, off_part, off_actq, off_act2, off_bar, off_misc, off_grp, off_ent;
+    int act_cap;     // activation rows the act region holds (>= 8)
     int part_bytes;  // per-slot partial sums: nch x 4 entries x RT floats
     int nb;   // activation blocks per row (K/32)
     int nbp;  // padded block slots per activation half-row
