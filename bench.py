@@ -110,10 +110,14 @@ class Clocks:
 # ------------------------------------------------------------------ our arm
 
 class Window:
-    """Device state of one T: inputs, routing outputs, scratch and the captured 48-layer graph."""
+    """Device state of one T: inputs, routing outputs, scratch and the captured 48-layer graph.
 
-    def __init__(self, m, T, tab_gu, tab_dn, cb_gu, cb_dn, dev, gu_type=GU_T):
+    fused: each layer is one moe_expert_layer launch (routing, q8_1, gate/up, SwiGLU + q8_1, down);
+    otherwise each layer is moe_route_group + moe_quantize_q8_1 + moe_expert_grouped (5 launches)."""
+
+    def __init__(self, m, T, tab_gu, tab_dn, cb_gu, cb_dn, dev, gu_type=GU_T, fused=True):
         self.T = T
+        self.fused = fused
         L, n = WL.layers, T * WL.k
         i32 = dict(dtype=torch.int32, device=dev)
         self.ids_h = torch.from_numpy(np.stack([routing_for(l, T) for l in range(L)])).pin_memory()
@@ -135,11 +139,19 @@ class Window:
         self.calls = [m.ExpertCall(gu_type, cb_gu, DN_T, cb_dn, WL.N, WL.F, tab_gu[l], tab_dn[l], WL.E, self.ge[l],
                                    self.gs[l], self.ng[l], n, 0, n, self.xq[l], self.es[l], self.ed[l], self.gu,
                                    self.hq, self.out[l], self.err, m.F_PDL) for l in range(L)]
+        self.sync = torch.zeros(m.layer_sync_ints(T, WL.k, WL.F), **i32)
+        self.lcalls = [m.LayerCall(gu_type, cb_gu, DN_T, cb_dn, WL.N, WL.F, tab_gu[l], tab_dn[l], WL.E, self.ids[l],
+                                   self.x[l], self.out[l], self.gu, self.hq, self.sync, self.err, m.F_PDL)
+                       for l in range(L)]
         self.m = m
         self.graph = None
 
     def run_layers(self, stream=None):
         m = self.m
+        if self.fused:
+            for l in range(WL.layers):
+                self.lcalls[l](stream)
+            return
         for l in range(WL.layers):
             m.route_group(self.ids[l], WL.E, 0, self.ge[l], self.gs[l], self.ng[l], self.es[l], self.ed[l],
                           self.err, stream=stream)
@@ -156,8 +168,8 @@ class Window:
         return g
 
 
-def launches_per_window():
-    return WL.layers * 5  # route, quantize, gate/up, SwiGLU+q8_1, down
+def launches_per_window(fused=True):
+    return WL.layers * (1 if fused else 5)  # one fused launch, or route, quantize, gate/up, SwiGLU+q8_1, down
 
 
 def run_ours(args, rank, world):
@@ -194,14 +206,21 @@ def run_ours(args, rank, world):
         raise RuntimeError(f"transcoding error bits {int(terr.item())}")
     setup_s = time.time() - t0
 
+    # headline: fused layer launches on the slot layout; compared: the separate-kernel window on the
+    # same layout, and the fused window reading CB3 directly
     wins = {T: Window(m, T, tab_gx, tab_dn, None, cb_dn, dev, gu_type=XT) for T in TS}
+    sepv = {T: Window(m, T, tab_gx, tab_dn, None, cb_dn, dev, gu_type=XT, fused=False) for T in TS}
     natv = {T: Window(m, T, tab_gu, tab_dn, cb_gu, cb_dn, dev) for T in TS}
-    for w in list(wins.values()) + list(natv.values()):
+    every = list(wins.values()) + list(sepv.values()) + list(natv.values())
+    for w in every:
         w.capture()
     torch.cuda.synchronize()
-    for w in list(wins.values()) + list(natv.values()):
+    for w in every:
         if int(w.err.item()):
             raise RuntimeError(f"device error bits {int(w.err.item())}")
+    for T in TS:  # the fused window reproduces the separate kernels bit for bit
+        if not torch.equal(wins[T].out.view(torch.int32), sepv[T].out.view(torch.int32)):
+            raise RuntimeError(f"fused and separate windows differ at T={T}")
 
     s = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -243,34 +262,38 @@ def run_ours(args, rank, world):
                       "frac_of_measured_hbm": round(bytes_t[T][0] / (us_t[T] * 1e-6) / 1e9 / hbm_peak, 4),
                       "groups_per_layer": round(float(np.mean(bytes_t[T][2])), 2)} for T in TS}
 
-    # ---- the native layout (CB3 read directly), timed the same way after the headline run
-    nat_t = {T: [] for T in TS}
-    for _ in range(args.warmup):
+    # ---- the comparison windows, timed the same way after the headline run
+    def time_windows(ws):
+        ts = {T: [] for T in TS}
+        for _ in range(args.warmup):
+            for T in TS:
+                ws[T].graph.replay()
+        for _ in range(args.steps):
+            for T in TS:
+                a, b = ev(), ev()
+                a.record(s)
+                ws[T].graph.replay()
+                b.record(s)
+                ts[T].append((a, b))
+        torch.cuda.synchronize()
+        res = {}
         for T in TS:
-            natv[T].graph.replay()
-    for _ in range(args.steps):
-        for T in TS:
-            a, b = ev(), ev()
-            a.record(s)
-            natv[T].graph.replay()
-            b.record(s)
-            nat_t[T].append((a, b))
-    torch.cuda.synchronize()
-    native = {str(T): {"us": round(float(np.median([a.elapsed_time(b) * 1e3 for a, b in nat_t[T]])), 2)}
-              for T in TS}
-    for T in TS:
-        us = native[str(T)]["us"]
-        native[str(T)]["GBps"] = round(bytes_t[T][0] / (us * 1e-6) / 1e9, 1)
-        native[str(T)]["frac_of_measured_hbm"] = round(bytes_t[T][0] / (us * 1e-6) / 1e9 / hbm_peak, 4)
+            us = float(np.median([a.elapsed_time(b) * 1e3 for a, b in ts[T]]))
+            res[str(T)] = {"us": round(us, 2), "GBps": round(bytes_t[T][0] / (us * 1e-6) / 1e9, 1),
+                           "frac_of_measured_hbm": round(bytes_t[T][0] / (us * 1e-6) / 1e9 / hbm_peak, 4)}
+        return res
 
-    # ---- dominant kernel (grouped gate/up) timed on its own, T = 4, all 48 layers per launch set
-    roof = gate_up_roofline(m, wins[4], bytes_t[4], hbm_peak, peak_kind, s)
-    breakdown = {f"T{T}": step_breakdown(m, wins[T], s) for T in (1, 4)}
+    separate = time_windows(sepv)
+    native = time_windows(natv)
+
+    # ---- dominant kernel: the fused layer kernel (T = 4 window: 48 launches per graph)
+    roof = layer_roofline(wins[4], bytes_t[4], hbm_peak, peak_kind, s)
+    breakdown = {f"T{T}": step_breakdown(m, sepv[T], s) for T in (1, 4)}
 
     # ---- end to end: pinned host inputs -> device, the window graphs, outputs -> host
     e2e = end_to_end(wins, args, s, world, dev)
 
-    launches = args.steps * len(TS) * launches_per_window()
+    launches = args.steps * len(TS) * launches_per_window(True)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "us/window", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": False,
@@ -278,9 +301,12 @@ def run_ours(args, rank, world):
         "config": {"workload": "window48: 48 layers x 128 experts, top-8, n_embd 2560, n_ff 768, CB3 gate/up + "
                                "NL4 down (16.4 GB pool), T=1..4, one CUDA graph per T",
                    "layout": "gate/up held as CB3X slots (CB3 transcoded at load, same integers); down NL4",
+                   "launch": "one fused launch per layer (routing, q8_1, gate/up, SwiGLU + q8_1, down), PDL-chained",
                    "l2": "inputs larger than L2 (>= 1 GB of weights per window), no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "per_T": per_T, "native_layout": {"gate_up": "CB3 (read directly)", "per_T": native},
+        "per_T": per_T,
+        "separate_kernels": {"launch": "route + quantize + gate/up + SwiGLU/q8_1 + down per layer", "per_T": separate},
+        "native_layout": {"gate_up": "CB3 (read directly), fused launches", "per_T": native},
         "roofline": roof, "step_us_per_layer_alone": breakdown, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
         "setup_s": round(setup_s, 1),
     }
@@ -289,31 +315,29 @@ def run_ours(args, rank, world):
     return line
 
 
-def gate_up_roofline(m, w, bytes_t, hbm_peak, peak_kind, s):
-    """The grouped gate/up kernel launched alone for the 48 layers of the T = 4 window (inputs
-    already routed and quantized), CUDA events on the launching stream."""
-    for l in range(WL.layers):
-        m.grouped_gu(w.gu_type, w.calls[l]._keep[0], WL.N, WL.F, w.calls[l]._keep[2], WL.E, w.ge[l], w.gs[l],
-                     w.ng[l], w.T * WL.k, 0, w.xq[l], w.es[l], w.T * WL.k, w.gu, w.err, stream=s)
+def layer_roofline(w, bytes_t, hbm_peak, peak_kind, s, reps=10):
+    """The fused layer kernel: the T = 4 window graph (48 launches, one per layer) replayed with
+    CUDA events on the launching stream; duration per launch = graph time / 48 (consecutive
+    launches overlap slightly under PDL). Algorithmic bytes per launch = the CB3 + NL4 blob bytes
+    of the layer's groups, averaged over the 48 layers."""
+    w.graph.replay()
     torch.cuda.synchronize()
-    reps = 5
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(s)
     for _ in range(reps):
-        for l in range(WL.layers):
-            m.grouped_gu(w.gu_type, w.calls[l]._keep[0], WL.N, WL.F, w.calls[l]._keep[2], WL.E, w.ge[l], w.gs[l],
-                         w.ng[l], w.T * WL.k, 0, w.xq[l], w.es[l], w.T * WL.k, w.gu, w.err, stream=s)
+        w.graph.replay()
     b.record(s)
     torch.cuda.synchronize()
     dur_s = a.elapsed_time(b) * 1e-3 / (reps * WL.layers)
-    per_launch = bytes_t[1] / WL.layers
+    per_launch = bytes_t[0] / WL.layers
     ach = per_launch / dur_s / 1e9
-    streamed = per_launch * synth.blob_bytes(w.gu_type, 2 * WL.F, WL.N) / synth.blob_bytes(GU_T, 2 * WL.F, WL.N)
-    return {"kernel": f"grouped gate/up ({synth.NAMES[w.gu_type]} slots of CB3, T=4)", "bound": "hbm",
-            "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
-            "traffic": None, "peak_kind": peak_kind, "bytes_per_launch": int(per_launch),
-            "streamed_bytes_per_launch": int(streamed), "streamed_GBps": round(streamed / dur_s / 1e9, 1),
-            "us_per_launch": round(dur_s * 1e6, 2)}
+    streamed = per_launch + bytes_t[1] / WL.layers * (
+        synth.blob_bytes(w.gu_type, 2 * WL.F, WL.N) / synth.blob_bytes(GU_T, 2 * WL.F, WL.N) - 1)
+    return {"kernel": f"fused layer kernel ({synth.NAMES[w.gu_type]} gate/up slots of CB3, NL4 down, T=4)",
+            "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(ach / hbm_peak, 4), "traffic": None, "peak_kind": peak_kind,
+            "bytes_per_launch": int(per_launch), "streamed_bytes_per_launch": int(streamed),
+            "streamed_GBps": round(streamed / dur_s / 1e9, 1), "us_per_launch": round(dur_s * 1e6, 2)}
 
 
 def step_breakdown(m, w, s, reps=5):
@@ -491,12 +515,19 @@ def run_case(args):
         gu_type, cbg, tg = XT, None, tx
     call = m.ExpertCall(gu_type, cbg, DN_T, cb_dn, WL.N, WL.F, tg, tab(pool_dn), WL.E, ge, gs, ng, n, 0, n,
                         xq, es, ed, gu, hq, out, err, m.F_PDL)
+    sync = torch.zeros(m.layer_sync_ints(T, WL.k, WL.F), **i32)
+    lcall = m.LayerCall(gu_type, cbg, DN_T, cb_dn, WL.N, WL.F, tg, tab(pool_dn), WL.E, ids, x, out, gu, hq, sync,
+                        err, m.F_PDL)
     for _ in range(args.steps):
+        if args.case_fused:
+            lcall()
+            continue
         m.route_group(ids, WL.E, 0, ge, gs, ng, es, ed, err)
         m.quantize_q8_1(x, xq)
         call()
     torch.cuda.synchronize()
-    print(json.dumps({"case": f"one layer of window48 at T={T}", "err": int(err.item()),
+    print(json.dumps({"case": f"one layer of window48 at T={T}" + (" (fused)" if args.case_fused else ""),
+                      "err": int(err.item()),
                       "groups": int(ng.item())}))
 
 
@@ -505,6 +536,7 @@ def main():
     ap.add_argument("--case", action="store_true", help="run the single-layer profiling case instead")
     ap.add_argument("--case-t", type=int, default=4)
     ap.add_argument("--case-slot", action="store_true", help="profiling case with the gate/up pool in slot layout")
+    ap.add_argument("--case-fused", action="store_true", help="profiling case with the fused layer launch")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)

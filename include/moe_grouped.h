@@ -95,7 +95,7 @@ extern "C" {
 #define MOE_ERR_ENTRY 8     /* an entry's source or destination row out of range (entry skipped) */
 #define MOE_ERR_ALIGN 16    /* an expert's weight pointer not 16-byte aligned (group skipped) */
 #define MOE_ERR_CODEBOOK 32 /* a CB grid value is even (results of that call are unspecified) */
-#define MOE_ERR_TIMEOUT 64  /* a bounded wait on a staged weight tile gave up */
+#define MOE_ERR_TIMEOUT 64  /* a bounded wait (a staged weight tile, another CTA's rows) gave up */
 #define MOE_ERR_ROUTE 128   /* a routed expert id outside [0, n_experts) (entry dropped) */
 
 /* One q8_1 block (36 bytes). d and s are IEEE binary16 bit patterns. */
@@ -226,6 +226,63 @@ int moe_expert_grouped(const moe_expert_call* call, cudaStream_t stream);
  */
 #define MOE_STATIC_SCRATCH_BYTES (4u << 20)
 int moe_expert_grouped_static(const moe_expert_call* call, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- fused layer call
+ * The whole hot path of one layer in one kernel launch (the pages split it into a routing step
+ * and three kernels, #363 "experts: smaller and fewer launches for the verify window's PCIe
+ * call", "What changes"; this call fuses them): routing/grouping of topk_ids (as
+ * moe_route_group with entry_base 0), q8_1 of x (as moe_quantize_q8_1), grouped gate/up, SwiGLU +
+ * q8_1 and grouped down (as moe_expert_grouped with cap_groups = cap_entries = T*k, n_xq_rows = T,
+ * out_rows = T*k). Every output equals that sequence's bit for bit.
+ *  - out row t*k + slot receives entry (t, slot)'s n_embd values; rows of dropped ids (outside
+ *    [0, n_experts), reported as MOE_ERR_ROUTE) are not written.
+ *  - gu, hq: scratch [T*k][2*n_ff] and [T*k][n_ff/32] as in moe_expert_call, rows indexed by
+ *    entry (groups by ascending expert id, entries of a group by ascending (t, slot)); after the
+ *    call they hold the gate/up rows and the q8_1 h rows.
+ *  - sync: moe_layer_sync_ints(T, k, n_ff) int32 counters the launch's CTAs synchronise through.
+ *    The caller zeroes them once before the first call (e.g. cudaMemsetAsync); every call leaves
+ *    them zero. A call that reported MOE_ERR_TIMEOUT may leave them non-zero: zero them again.
+ *    Calls that may overlap on the GPU need separate sync arrays (and scratch).
+ *  - grp_expert [T*k], grp_start [T*k+1], n_groups [1], ent_src / ent_dst [T*k], xq
+ *    [T][n_embd/32]: optional (NULL = not written) copies of the grouping and of the activation
+ *    q8_1, for inspection.
+ *  - x and gu must be 16-byte aligned (else MOE_E_ALIGN).
+ *  - Formats: any gate/up format; down MOE_NL4 or MOE_Q8_0 (else MOE_E_TYPE).
+ *  - Limits: T*k <= 512 and the T activation rows staged in shared memory (44 bytes per 32
+ *    values, padded) must fit 64 KB (e.g. T <= 18 at n_embd 2560), else MOE_E_CAP; 32 rows of
+ *    either blob must fit 96 KB, else MOE_E_SHAPE.
+ *  - The launch's CTAs wait on one another (bounded, ~1 s, then MOE_ERR_TIMEOUT); the grid never
+ *    exceeds one CTA per SM, so it needs the GPU's SMs to itself for the duration of the call.
+ * MOE_F_PDL in flags chains the launch to the previous work on the stream with programmatic
+ * dependent launch (it reads topk_ids and x only after that work has completed). */
+typedef struct moe_layer_call {
+    moe_wfmt gu_fmt, down_fmt;
+    int32_t n_embd, n_ff, n_experts;
+    const void* const* w_gu;   /* [n_experts] device pointers to gate/up blobs */
+    const void* const* w_down; /* [n_experts] device pointers to down blobs */
+    const int32_t* topk_ids;   /* [T][k] */
+    int32_t T, k;
+    const float* x;            /* [T][n_embd] */
+    float* out;                /* [T*k][out_row_stride] */
+    int64_t out_row_stride;
+    float* gu;                 /* scratch [T*k][2*n_ff] */
+    moe_q8_1* hq;              /* scratch [T*k][n_ff/32] */
+    int32_t* sync;             /* [moe_layer_sync_ints(T, k, n_ff)], zero before the first call */
+    int32_t* grp_expert;       /* optional */
+    int32_t* grp_start;        /* optional */
+    int32_t* n_groups;         /* optional */
+    int32_t* ent_src;          /* optional */
+    int32_t* ent_dst;          /* optional */
+    moe_q8_1* xq;              /* optional */
+    int32_t* err;              /* optional */
+    int32_t flags;             /* MOE_F_* */
+} moe_layer_call;
+
+/* Number of int32 counters moe_expert_layer needs for windows of T tokens, top-k, n_ff
+ * (T*k + 1; 0 for invalid arguments). */
+int64_t moe_layer_sync_ints(int T, int k, int n_ff);
+
+int moe_expert_layer(const moe_layer_call* call, cudaStream_t stream);
 
 /* Test hook: the per-32-block integer sums of `rows` consecutive rows of one blob (row bytes
  * apart) against one q8_1 row xq[K/32], computed by the same device decode and dot-product

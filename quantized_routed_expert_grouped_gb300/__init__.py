@@ -18,6 +18,7 @@ __all__ = [
     "Q8_0", "Q4B", "NL4", "CB2", "CB3", "CB3X", "CB2X", "MoeError", "transcode_cb", "lib", "row_bytes", "strerror",
     "quantize_q8_1", "route_group", "grouped_gu", "swiglu_q8_1", "grouped_down",
     "expert_grouped", "ExpertCall", "STATIC_SCRATCH_BYTES", "test_block_isum", "ERR_BITS", "F_PDL",
+    "LayerCall", "layer_sync_ints",
 ]
 
 Q8_0, Q4B, NL4, CB2, CB3, CB3X, CB2X = 1, 2, 3, 4, 5, 6, 7
@@ -55,6 +56,17 @@ class ExpertCallC(ctypes.Structure):
     ]
 
 
+class LayerCallC(ctypes.Structure):
+    _fields_ = [
+        ("gu_fmt", WFmt), ("down_fmt", WFmt),
+        ("n_embd", ctypes.c_int32), ("n_ff", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+        ("w_gu", _P), ("w_down", _P), ("topk_ids", _P), ("T", ctypes.c_int32), ("k", ctypes.c_int32),
+        ("x", _P), ("out", _P), ("out_row_stride", ctypes.c_int64), ("gu", _P), ("hq", _P), ("sync", _P),
+        ("grp_expert", _P), ("grp_start", _P), ("n_groups", _P), ("ent_src", _P), ("ent_dst", _P), ("xq", _P),
+        ("err", _P), ("flags", ctypes.c_int32),
+    ]
+
+
 def lib():
     """Load the CUDA library (raises if it has not been built)."""
     global _LIB
@@ -76,9 +88,12 @@ def lib():
         L.moe_expert_grouped_static.argtypes = [ctypes.POINTER(ExpertCallC), _P]
         L.moe_test_block_isum.argtypes = [WFmt, _I, _P, _I, _P, _P, _P]
         L.moe_transcode_cb.argtypes = [WFmt, _I, _I, _I, _I, _P, _P, _P, _P]
+        L.moe_expert_layer.argtypes = [ctypes.POINTER(LayerCallC), _P]
+        L.moe_layer_sync_ints.argtypes = [_I, _I, _I]
+        L.moe_layer_sync_ints.restype = _I64
         for f in ("moe_quantize_q8_1", "moe_route_group", "moe_grouped_gu", "moe_swiglu_q8_1",
                   "moe_grouped_down", "moe_expert_grouped", "moe_expert_grouped_static", "moe_test_block_isum",
-                  "moe_transcode_cb"):
+                  "moe_transcode_cb", "moe_expert_layer"):
             getattr(L, f).restype = _I
         _LIB = L
     return _LIB
@@ -172,6 +187,35 @@ class ExpertCall:
         """The same call through moe_expert_grouped_static: gu/hq are ignored and the library's
         static device scratch buffer is used instead (nothing is allocated)."""
         _check(lib().moe_expert_grouped_static(ctypes.byref(self.c), _stream(stream)))
+
+
+def layer_sync_ints(T: int, k: int, n_ff: int) -> int:
+    """int32 counters a moe_expert_layer call needs (zero them once before the first call)."""
+    return int(lib().moe_layer_sync_ints(T, k, n_ff))
+
+
+class LayerCall:
+    """Arguments of one moe_expert_layer call (the whole layer in one launch), kept alive with their
+    tensors. topk_ids int32 [T, k], x fp32 [T, n_embd], out fp32 [T*k, >= n_embd]; gu / hq scratch
+    as for ExpertCall; sync int32 [layer_sync_ints(T, k, n_ff)] zeroed before the first call.
+    grp_expert .. xq: optional tensors that receive the grouping and the activation q8_1."""
+
+    def __init__(self, gu_type, gu_codebook, down_type, down_codebook, n_embd, n_ff, w_gu_table, w_down_table,
+                 n_experts, topk_ids, x, out, gu, hq, sync, err=None, flags=F_PDL, grp_expert=None, grp_start=None,
+                 n_groups=None, ent_src=None, ent_dst=None, xq=None):
+        T, k = topk_ids.shape
+        opt = (grp_expert, grp_start, n_groups, ent_src, ent_dst, xq)
+        self._keep = (gu_codebook, down_codebook, w_gu_table, w_down_table, topk_ids, x, out, gu, hq, sync,
+                      err) + opt
+        ptr = lambda t: None if t is None else t.data_ptr()
+        self.c = LayerCallC(
+            _fmt(gu_type, gu_codebook), _fmt(down_type, down_codebook), n_embd, n_ff, n_experts,
+            w_gu_table.data_ptr(), w_down_table.data_ptr(), topk_ids.data_ptr(), T, k, x.data_ptr(),
+            out.data_ptr(), out.stride(0), gu.data_ptr(), hq.data_ptr(), sync.data_ptr(),
+            *[ptr(t) for t in opt], ptr(err), flags)
+
+    def __call__(self, stream=None):
+        _check(lib().moe_expert_layer(ctypes.byref(self.c), _stream(stream)))
 
 
 def expert_grouped(*args, stream=None, **kw):

@@ -228,6 +228,140 @@ int down_impl(moe_wfmt fmt, int n_embd, int n_ff, const void* const* w_down, int
     return run_gemv(fmt.type, a, grid_groups, stream, pdl);
 }
 
+// ---------------------------------------------------------------- fused layer call
+
+constexpr int kLayerMaxEntries = 512;  // routing: one thread per id
+
+// Warp organisation of one phase: chunks per warp and warps per set as plan_gemv chooses them.
+void phase_warps(int nch, GemvArgs& a) {
+    int CPW = 1, best = 0;
+    for (int cpw = 1; cpw <= nch; ++cpw) {
+        const int wps = (nch + cpw - 1) / cpw;
+        if (wps > 15) continue;
+        const int cw = wps * (15 / wps);
+        if (cw > best) { best = cw; CPW = cpw; }
+    }
+    a.CPW = CPW;
+    a.WPS = (nch + CPW - 1) / CPW;
+    a.TP = 15 / a.WPS;
+    a.CW = a.WPS * a.TP;
+}
+
+// Geometry and shared-memory layout of one fused layer launch. The ring slot holds a gate/up
+// tile (32 rows, or 16 when 32 rows exceed 96 KB) or a down tile of nsub x 32 rows.
+constexpr int kLayerPtrCache = 256;  // experts whose pointers are cached in shared memory
+constexpr int kLayerThreads = 512;   // producer warp + 15 consumer warps
+constexpr int kBatch = 4;            // entries staged per down batch
+
+int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, int& NT, int& smem) {
+    const int n = T * k;
+    if (n <= 0 || n > kLayerMaxEntries) return MOE_E_CAP;
+    GemvArgs& A = L.gu;
+    GemvArgs& D = L.dn;
+    const int64_t rbA = moe_row_bytes(gt, N), rbD = moe_row_bytes(dt, F);
+    A.K = N; A.rows = 2 * F; A.nch = N / 256; A.nb = N / 32; A.nbp = A.nb + A.nb / 8;
+    D.K = F; D.rows = N; D.nch = F / 256; D.nb = F / 32; D.nbp = D.nb + D.nb / 8;
+    if (rbA <= 0 || rbD <= 0 || A.nch > 32 || D.nch > 32) return MOE_E_SHAPE;
+    if (32 * rbD > 96 * 1024 || 16 * rbA > 96 * 1024) return MOE_E_SHAPE;
+    A.row_bytes = static_cast<int>(rbA);
+    D.row_bytes = static_cast<int>(rbD);
+    phase_warps(A.nch, A);
+    phase_warps(D.nch, D);
+    A.RT = 32 * rbA <= 96 * 1024 ? 32 : 16;
+    // activations: T token rows (gate/up role) or 4 entry rows (down role), the same region
+    const int actqA = round_up(T * 2 * A.nbp * 16, 128), act2A = round_up(T * A.nb * 8, 128);
+    const int actqD = round_up(2 * kBatch * 2 * D.nbp * 16, 128);
+    const int act2D = round_up(2 * kBatch * D.nb * 8, 128);
+    if (actqA + act2A > 64 * 1024) return MOE_E_CAP;
+    const int act = actqA + act2A > actqD + act2D ? actqA + act2A : actqD + act2D;
+    const int grp = round_up(24 * n + 4 * (n + 1), 128), entb = round_up(8 * n, 128);
+    const int route = round_up(4 * (6 * n + 4), 128);
+    const int cbb = cb_type(gt) ? 32768 : 0;
+    const int ptrs = E <= kLayerPtrCache ? round_up(16 * E, 128) : 0;
+    const int fixed = cbb + act + 2 * grp + 2 * entb + route + ptrs + 512 + 512;
+    // one ring for both phases: a slot holds a gate/up tile (RT rows) or a down tile of nsub 32-row
+    // sub-tiles; per stage a slot, partial sums and one unit buffer
+    const int64_t tileA = A.RT * rbA;
+    int nsub = static_cast<int>(tileA / (32 * rbD));
+    nsub = nsub < 1 ? 1 : nsub > 4 ? 4 : nsub;
+    D.RT = 32 * nsub;
+    const int64_t tile = tileA > D.RT * rbD ? tileA : D.RT * rbD;
+    const int stage = round_up(static_cast<int>(tile) + 16, 128);
+    const int pA = A.nch * 4 * A.RT, pD = D.nch * 4 * D.RT;
+    const int part = 4 * (pA > pD ? pA : pD);
+    int S = (kSmemPerSm - 1024 - fixed) / (stage + part + 512);
+    S = S > 8 ? 8 : S;
+    if (S < 2) return MOE_E_SHAPE;
+    int off = cbb;  // the gate/up codebook sits at offset 0
+    A.off_ring = D.off_ring = off;
+    off += S * stage;
+    A.off_part = D.off_part = off;
+    off += S * part;
+    L.off_unit = off;
+    off += S * 512;
+    A.off_actq = D.off_actq = off;
+    A.off_act2 = off + actqA;
+    D.off_act2 = off + actqD;
+    off += act;
+    A.off_grp = off;
+    off += grp;
+    D.off_grp = off;
+    off += grp;
+    A.off_ent = off;
+    off += entb;
+    D.off_ent = off;
+    off += entb;
+    L.off_route = off;
+    off += route;
+    L.off_ptr = ptrs ? off : 0;
+    off += ptrs;
+    A.off_bar = D.off_bar = off;
+    off += 512;  // 5 x 8 mbarriers
+    A.off_misc = D.off_misc = off;
+    off += 512;
+    A.stages = D.stages = S;
+    A.stage_bytes = D.stage_bytes = stage;
+    A.part_bytes = D.part_bytes = part;
+    A.act_cap = T;
+    D.act_cap = 2 * kBatch;
+    A.cap_groups = A.cap_entries = D.cap_groups = D.cap_entries = n;
+    L.T = T;
+    L.k = k;
+    L.n = n;
+    L.F = F;
+    L.nbj = F / 32;
+    L.nsub = nsub;
+    L.upg = F / 32;
+    L.tpu = 64 / A.RT;
+    NT = kLayerThreads;
+    smem = off;
+    return MOE_OK;
+}
+
+cudaError_t layer_occupancy(int gt, int dt, int NT, int smem, int* ctas) {
+    switch (gt) {
+    case MOE_Q8_0: return layer_occupancy_q8_0(dt, NT, smem, ctas);
+    case MOE_Q4B: return layer_occupancy_q4b(dt, NT, smem, ctas);
+    case MOE_NL4: return layer_occupancy_nl4(dt, NT, smem, ctas);
+    case MOE_CB2: return layer_occupancy_cb2(dt, NT, smem, ctas);
+    case MOE_CB3X: return layer_occupancy_cb3x(dt, NT, smem, ctas);
+    case MOE_CB2X: return layer_occupancy_cb2x(dt, NT, smem, ctas);
+    default: return layer_occupancy_cb3(dt, NT, smem, ctas);
+    }
+}
+
+cudaError_t launch_layer(int gt, int dt, const LayerArgs& a, int grid, int NT, int smem, cudaStream_t s, bool pdl) {
+    switch (gt) {
+    case MOE_Q8_0: return launch_layer_q8_0(a, dt, grid, NT, smem, s, pdl);
+    case MOE_Q4B: return launch_layer_q4b(a, dt, grid, NT, smem, s, pdl);
+    case MOE_NL4: return launch_layer_nl4(a, dt, grid, NT, smem, s, pdl);
+    case MOE_CB2: return launch_layer_cb2(a, dt, grid, NT, smem, s, pdl);
+    case MOE_CB3X: return launch_layer_cb3x(a, dt, grid, NT, smem, s, pdl);
+    case MOE_CB2X: return launch_layer_cb2x(a, dt, grid, NT, smem, s, pdl);
+    default: return launch_layer_cb3(a, dt, grid, NT, smem, s, pdl);
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -329,6 +463,68 @@ int moe_expert_grouped(const moe_expert_call* c, cudaStream_t stream) {
     return down_impl(c->down_fmt, c->n_embd, c->n_ff, c->w_down, c->n_experts, c->grp_expert, c->grp_start,
                      c->n_groups, c->cap_groups, c->grid_groups, c->hq, c->cap_entries, c->ent_dst, c->out,
                      c->out_rows, c->out_row_stride, c->err, stream, pdl, pdl);
+}
+
+int64_t moe_layer_sync_ints(int T, int k, int n_ff) {
+    if (T <= 0 || k <= 0 || n_ff <= 0 || n_ff % 32) return 0;
+    return static_cast<int64_t>(T) * k + 1;
+}
+
+int moe_expert_layer(const moe_layer_call* c, cudaStream_t stream) {
+    if (!c) return MOE_E_NULL;
+    int rc;
+    if ((rc = check_fmt(c->gu_fmt)) || (rc = check_fmt(c->down_fmt))) return rc;
+    if (c->down_fmt.type != MOE_NL4 && c->down_fmt.type != MOE_Q8_0) return MOE_E_TYPE;
+    if ((rc = check_dims(c->n_embd, c->n_ff))) return rc;
+    if (!c->w_gu || !c->w_down || !c->topk_ids || !c->x || !c->out || !c->gu || !c->hq || !c->sync)
+        return MOE_E_NULL;
+    if (c->T <= 0 || c->k <= 0) return MOE_E_SHAPE;
+    if (c->n_experts <= 0) return MOE_E_CAP;
+    if (c->out_row_stride < c->n_embd) return MOE_E_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(c->x) | reinterpret_cast<uintptr_t>(c->gu)) & 15u) return MOE_E_ALIGN;
+    LayerArgs L = {};
+    int NT = 0, smem = 0;
+    if ((rc = plan_layer(c->gu_fmt.type, c->down_fmt.type, c->n_embd, c->n_ff, c->T, c->k, c->n_experts, L, NT, smem)))
+        return rc;
+    int ctas = 0;
+    if (layer_occupancy(c->gu_fmt.type, c->down_fmt.type, NT, smem, &ctas) != cudaSuccess || ctas < 1)
+        return MOE_E_CUDA;
+    const int sms = sm_count();
+    if (sms <= 0) return MOE_E_CUDA;
+    GemvArgs& A = L.gu;
+    GemvArgs& D = L.dn;
+    A.w = c->w_gu;
+    D.w = c->w_down;
+    A.n_experts = D.n_experts = c->n_experts;
+    A.codebook = c->gu_fmt.codebook;
+    D.codebook = c->down_fmt.codebook;
+    A.err = D.err = c->err;
+    A.n_act_rows = c->T;
+    A.out = c->gu;
+    A.out_rows = L.n;
+    A.out_stride = 2 * static_cast<int64_t>(c->n_ff);
+    D.act = c->hq;
+    D.n_act_rows = L.n;
+    D.out = c->out;
+    D.out_rows = L.n;
+    D.out_stride = c->out_row_stride;
+    L.ids = c->topk_ids;
+    L.x = c->x;
+    L.hq = c->hq;
+    L.sync = c->sync;
+    L.o_ge = c->grp_expert;
+    L.o_gs = c->grp_start;
+    L.o_ng = c->n_groups;
+    L.o_es = c->ent_src;
+    L.o_ed = c->ent_dst;
+    L.o_xq = c->xq;
+    // one CTA per SM (co-resident), split on the device between the gate/up and the down roles
+    const int64_t grid = sms;
+    const bool pdl = (c->flags & MOE_F_PDL) != 0;
+    if (launch_layer(c->gu_fmt.type, c->down_fmt.type, L, static_cast<int>(grid), NT, smem, stream, pdl) !=
+        cudaSuccess)
+        return MOE_E_CUDA;
+    return MOE_OK;
 }
 
 int moe_transcode_cb(moe_wfmt src, int dst_type, int K, int rows, int n_blobs, const void* const* src_blobs,

@@ -49,42 +49,44 @@ namespace moe {
 // CHUNK: bytes of one 256-weight chunk (for the slot layouts: its codes; the 8-byte scale
 // records follow all of a row's codes). CB: native codebook format (grid staged in shared
 // memory). SLOT: transcoded slot layout (BIAS: code bias). ALPHA: decode cost of a row relative to
-// one entry's dot products (work balancing).
+// one entry's dot products (work balancing). DEC, DOT: warp-instructions per 32-row x 256-weight
+// chunk for the decode and per entry for the dot products (measured on the chunk loop alone; a
+// cost model for splitting work between phases).
 template <int TYPE>
 struct Fmt;
 template <>
 struct Fmt<MOE_Q8_0> {
-    static constexpr int CHUNK = 272, ALPHA = 1;
+    static constexpr int CHUNK = 272, ALPHA = 1, DEC = 120, DOT = 148;
     static constexpr bool CB = false, SLOT = false;
 };
 template <>
 struct Fmt<MOE_Q4B> {
-    static constexpr int CHUNK = 160, ALPHA = 2;
+    static constexpr int CHUNK = 160, ALPHA = 2, DEC = 200, DOT = 160;
     static constexpr bool CB = false, SLOT = false;
 };
 template <>
 struct Fmt<MOE_NL4> {
-    static constexpr int CHUNK = 144, ALPHA = 5;
+    static constexpr int CHUNK = 144, ALPHA = 5, DEC = 574, DOT = 127;
     static constexpr bool CB = false, SLOT = false;
 };
 template <>
 struct Fmt<MOE_CB2> {
-    static constexpr int CHUNK = 70, ALPHA = 4, NW = 18, SGN = 8, SUB = 16;
+    static constexpr int CHUNK = 70, ALPHA = 4, NW = 18, SGN = 8, SUB = 16, DEC = 480, DOT = 150;
     static constexpr bool CB = true, SLOT = false;
 };
 template <>
 struct Fmt<MOE_CB3> {
-    static constexpr int CHUNK = 102, ALPHA = 5, NW = 26, SGN = 16, SUB = 24;
+    static constexpr int CHUNK = 102, ALPHA = 5, NW = 26, SGN = 16, SUB = 24, DEC = 550, DOT = 150;
     static constexpr bool CB = true, SLOT = false;
 };
 template <>
 struct Fmt<MOE_CB3X> {
-    static constexpr int CHUNK = 128, ALPHA = 1, BIAS = 8;
+    static constexpr int CHUNK = 128, ALPHA = 1, BIAS = 8, DEC = 197, DOT = 148;
     static constexpr bool CB = false, SLOT = true;
 };
 template <>
 struct Fmt<MOE_CB2X> {
-    static constexpr int CHUNK = 64, ALPHA = 1, BIAS = 2;
+    static constexpr int CHUNK = 64, ALPHA = 1, BIAS = 2, DEC = 180, DOT = 148;
     static constexpr bool CB = false, SLOT = true;
 };
 
@@ -98,6 +100,30 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Ring protocol, consumer side: before waiting on the "full" barrier of the slot of ring tile q,
+// wait until the producer has issued tile q (issued[0] > q, written after the copy is requested).
+// Several warp-sets share the slots, so a set may reach tile q before the slot's previous tile
+// (q - stages, another set's) has landed; the barrier would then still be in that tile's phase,
+// whose parity is that of the phase before, and a parity wait would return at once. The producer
+// issues tile q only after tile q - stages was released, so once it is issued the slot's barrier
+// is in tile q's phase. Gives up (false) after kWaitLimitNs or when the abort flag issued[1] is set.
+__device__ __forceinline__ bool wait_issued(const volatile int* issued, int q) {
+    if (issued[0] > q) {
+        __threadfence_block();
+        return true;
+    }
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(32);
+        if (issued[0] > q) {
+            __threadfence_block();
+            return true;
+        }
+        if (issued[1]) return false;
+        if ((it & 15u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+    }
 }
 
 // ---------------------------------------------------------------- per-format decode
@@ -359,8 +385,9 @@ __device__ __forceinline__ void load_table(const GemvArgs& a, uint32_t tab[4]) {
 // Staged activations: slot i of the shared-memory act region holds one q8_1 row as 16-byte code
 // halves (q[(i*2 + h)*nbp + bp], bp = b + b/8: conflict-free 128-bit loads) and (d, aux) pairs
 // (q2[i*nb + b]); aux = exact code sum S times the format's factor (CB: S, slots: -(2 bias - 1) S),
-// s (Q4B) or 0. Row `src` < 0 stages zeros.
-template <int TYPE>
+// s (Q4B) or 0. Row `src` < 0 stages zeros. CG: read through L2 only (rows written earlier by
+// the same launch); otherwise through the read-only path.
+template <int TYPE, bool CG = false>
 __device__ __forceinline__ void stage_block(const GemvArgs& a, uint8_t* smem, int slot, int src, int b) {
     int4* q = reinterpret_cast<int4*>(smem + a.off_actq);
     float2* q2 = reinterpret_cast<float2*>(smem + a.off_act2);
@@ -369,7 +396,7 @@ __device__ __forceinline__ void stage_block(const GemvArgs& a, uint8_t* smem, in
     if (src >= 0) {
         const uint32_t* p = reinterpret_cast<const uint32_t*>(a.act + static_cast<int64_t>(src) * a.nb + b);
 #pragma unroll
-        for (int k = 0; k < 9; ++k) w[k] = __ldg(p + k);
+        for (int k = 0; k < 9; ++k) w[k] = CG ? __ldcg(p + k) : __ldg(p + k);
     } else {
 #pragma unroll
         for (int k = 0; k < 9; ++k) w[k] = 0;
@@ -394,6 +421,29 @@ __device__ __forceinline__ void stage_block(const GemvArgs& a, uint8_t* smem, in
     q2[slot * a.nb + b] = make_float2(h2f_bits(w[0]), aux);
 }
 
+// One q8_1 block held by one thread (code words w[0..7], header hdr = d16 | s16 << 16, exact code
+// sum S) into slot `slot`, block b, in the layout stage_block writes.
+template <int TYPE>
+__device__ __forceinline__ void stage_words(const GemvArgs& a, uint8_t* smem, int slot, int b, const uint32_t w[8],
+                                            uint32_t hdr, int S) {
+    uint32_t c[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) c[k] = TYPE == MOE_NL4 ? prmt(w[k], 0u, 0x3120u) : w[k];
+    int4* q = reinterpret_cast<int4*>(smem + a.off_actq);
+    const int bp = b + (b >> 3);
+    q[(slot * 2 + 0) * a.nbp + bp] = make_int4(c[0], c[1], c[2], c[3]);
+    q[(slot * 2 + 1) * a.nbp + bp] = make_int4(c[4], c[5], c[6], c[7]);
+    float aux = 0.0f;
+    if constexpr (Fmt<TYPE>::SLOT) {
+        aux = __int_as_float(S * -(2 * Fmt<TYPE>::BIAS - 1));
+    } else if constexpr (Fmt<TYPE>::CB) {
+        aux = __int_as_float(S);
+    } else if constexpr (TYPE == MOE_Q4B) {
+        aux = h2f_bits(hdr >> 16);
+    }
+    reinterpret_cast<float2*>(smem + a.off_act2)[slot * a.nb + b] = make_float2(h2f_bits(hdr), aux);
+}
+
 // All n rows of the activation matrix into slots 0..n-1.
 template <int TYPE>
 __device__ __forceinline__ void stage_all(const GemvArgs& a, uint8_t* smem, int n, int t, int nt) {
@@ -404,12 +454,12 @@ __device__ __forceinline__ void stage_all(const GemvArgs& a, uint8_t* smem, int 
 }
 
 // The activation rows of entries e0 .. e0+ne-1 (ent[e].x, -1 when invalid) into slots slot0 ...
-template <int TYPE>
+template <int TYPE, bool CG = false>
 __device__ __forceinline__ void stage_entries(const GemvArgs& a, uint8_t* smem, const int2* ent, int e0, int ne,
                                               int slot0, int t, int nt) {
     for (int i = t; i < ne * a.nb; i += nt) {
         const int s = i / a.nb;
-        stage_block<TYPE>(a, smem, slot0 + s, ent[e0 + s].x, i - s * a.nb);
+        stage_block<TYPE, CG>(a, smem, slot0 + s, ent[e0 + s].x, i - s * a.nb);
     }
 }
 
@@ -429,8 +479,6 @@ __device__ __forceinline__ void load_act(const GemvArgs& a, const uint8_t* smem,
         aux[e] = v.y;
     }
 }
-
-// ---------------------------------------------------------------- compute
 
 // ---------------------------------------------------------------- compute
 
@@ -735,6 +783,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
             bulk_g2s(smem + a.off_ring + static_cast<size_t>(s) * a.stage_bytes,
                      g.ptr + static_cast<size_t>(t.row0) * a.row_bytes, bytes, &full[s]);
             ++issued;
+            __threadfence_block();
             *reinterpret_cast<volatile int*>(misc) = issued;
             return 1;
         }
@@ -772,13 +821,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
 
     // Activations: staged already (gate/up) or now, after the wait (down), when they all fit;
     // otherwise a range spanning at most two groups of at most 4 entries each has both groups'
-    // rows staged here, and any other range is walked by warp-set 0 alone, restaging at every
-    // group (or 4-entry batch) change.
+    // rows staged here. Any other range, and any range holding a group of more than 4 entries,
+    // is walked by warp-set 0 alone with barriers between entry batches, restaging (unless all
+    // rows are staged) at every group or batch change.
     const int gA = static_cast<int>(rb0 / rbpg), gB = static_cast<int>((rb1 - 1) / rbpg);
     const int neA = gi[gA].e1 - gi[gA].e0, neB = gi[gB].e1 - gi[gB].e0;
-    const bool two = !all_rows && gB - gA <= 1 && (gi[gA].cost == 0 || neA <= kMaxEntriesPerPass) &&
-                     (gi[gB].cost == 0 || neB <= kMaxEntriesPerPass);
-    const bool fast = all_rows || two;
+    // A group of more than kMaxEntriesPerPass entries takes several entry batches per tile; those
+    // run on the barrier path (the last-warp path keeps one batch's partials per slot).
+    bool multi = false;
+    for (int g = gA; g <= gB; ++g) multi |= gi[g].cost != 0 && gi[g].e1 - gi[g].e0 > kMaxEntriesPerPass;
+    const bool two = !all_rows && !multi && gB - gA <= 1;
+    const bool fast = !multi && (all_rows || two);
     if (all_rows && a.prefetch_before_wait) {
         stage_all<TYPE>(a, smem, a.n_act_rows, ct, cnt);
         named_sync(1, cnt);
@@ -805,7 +858,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
         const uint32_t parity = static_cast<uint32_t>(kk / S) & 1u;
         const uint8_t* tile = smem + a.off_ring + static_cast<size_t>(slot) * a.stage_bytes;
         float* part = reinterpret_cast<float*>(smem + a.off_part + static_cast<size_t>(slot) * a.part_bytes);
-        if (!aborted && !mbar_wait_bounded(&full[slot], parity)) {
+        if (!aborted && !(wait_issued(misc, kk) && mbar_wait_bounded(&full[slot], parity))) {
             aborted = true;
             set_err(a.err, MOE_ERR_TIMEOUT);
             *reinterpret_cast<volatile int*>(misc + 1) = 1;
@@ -826,7 +879,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
 #pragma unroll
                 for (int e = 0; e < 4; ++e) slots[e] = s0 + (e < ne ? e : ne - 1);
             }
-            if (!fast && (t.g != cur_g || b0 != cur_b0)) {
+            if (!fast && !all_rows && (t.g != cur_g || b0 != cur_b0)) {
                 named_sync(1, scnt);
                 stage_entries<TYPE>(a, smem, ent, b0, ne, 0, st, scnt);
                 named_sync(1, scnt);

@@ -71,6 +71,24 @@ struct GemvPlan {
     int NT, smem;
 };
 
+// Arguments of one fused layer launch (layer.cuh).
+struct LayerArgs {
+    GemvArgs gu, dn;     // per-phase geometry and pointers (shared ring, partials, barriers, misc)
+    const int32_t* ids;  // [T][k] top-k expert ids
+    const float* x;      // [T][n_embd]
+    moe_q8_1* hq;        // [n][F/32]: the q8_1 h rows (exchanged between the CTAs)
+    int32_t* sync;       // [n] per-group h-block counters, [1] exit counter
+    int32_t *o_ge, *o_gs, *o_ng, *o_es, *o_ed;  // optional copies of the grouping (CTA 0)
+    moe_q8_1* o_xq;                             // optional copy of the activation q8_1 (CTA 0)
+    int T, k, n;         // n = T * k entries (and the capacity of every per-group table)
+    int F, nbj;          // n_ff, n_ff / 32
+    int nsub;            // 32-row sub-tiles per down tile
+    int upg, tpu;        // gate/up units (32 h values) per group, ring tiles per unit
+    int off_unit;        // shared-memory unit buffers: [stages][4 entries][32] h values
+    int off_route;       // shared-memory routing scratch
+    int off_ptr;         // shared-memory cache of both expert pointer tables (0: not cached)
+};
+
 cudaError_t launch_quantize_q8_1(const float* x, int64_t rows, int64_t cols, moe_q8_1* xq, cudaStream_t s,
                                  bool pdl);
 cudaError_t launch_swiglu_q8_1(const float* gu, int n_ff, const int32_t* grp_start, const int32_t* n_groups,
@@ -97,5 +115,19 @@ MOE_DECLARE_FORMAT(cb3)
 MOE_DECLARE_FORMAT(cb3x)
 MOE_DECLARE_FORMAT(cb2x)
 #undef MOE_DECLARE_FORMAT
+
+// Fused layer launchers, one translation unit per gate/up format (down: NL4 or Q8_0).
+#define MOE_DECLARE_LAYER(NAME)                                                                         \
+    cudaError_t launch_layer_##NAME(const LayerArgs& a, int dt, int grid, int NT, int smem, cudaStream_t s, \
+                                    bool pdl);                                                          \
+    cudaError_t layer_occupancy_##NAME(int dt, int NT, int smem, int* ctas);
+MOE_DECLARE_LAYER(q8_0)
+MOE_DECLARE_LAYER(q4b)
+MOE_DECLARE_LAYER(nl4)
+MOE_DECLARE_LAYER(cb2)
+MOE_DECLARE_LAYER(cb3)
+MOE_DECLARE_LAYER(cb3x)
+MOE_DECLARE_LAYER(cb2x)
+#undef MOE_DECLARE_LAYER
 
 }  // namespace moe

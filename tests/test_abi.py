@@ -66,3 +66,30 @@ def test_host_argument_errors(m):
     assert L.moe_route_group(dummy, 40, 32, 8, 0, dummy, dummy, dummy, dummy, dummy, None, None) == -3
     assert L.moe_expert_grouped(None, None) == -1
     assert L.moe_test_block_isum(W(1, None), 300, dummy, 1, dummy, dummy, None) == -3
+
+
+def test_layer_call_host_errors(m):
+    L = m.lib()
+    W = m.WFmt
+    d = 16
+    assert m.layer_sync_ints(4, 8, 768) == 32 + 1
+    assert m.layer_sync_ints(0, 8, 768) == 0
+
+    def call(**kw):
+        f = dict(gu_fmt=W(1, None), down_fmt=W(1, None), n_embd=2560, n_ff=768, n_experts=4, w_gu=d, w_down=d,
+                 topk_ids=d, T=4, k=8, x=d, out=d, out_row_stride=2560, gu=d, hq=d, sync=d, flags=0)
+        f.update(kw)
+        c = m.LayerCallC(**f)
+        return L.moe_expert_layer(ctypes.byref(c), None)
+
+    assert L.moe_expert_layer(None, None) == -1
+    assert call(down_fmt=W(4, ctypes.c_void_p(d))) == -2        # CB2 down: not supported by the fused call
+    assert call(gu_fmt=W(5, None)) == -2                         # CB3 without codebook
+    assert call(n_ff=700) == -3
+    assert call(sync=None) == -1 and call(x=None) == -1 and call(topk_ids=None) == -1
+    assert call(T=0) == -3
+    assert call(T=65) == -4                                      # T*k > 512
+    assert call(T=40, k=2) == -4                                 # 40 activation rows exceed the staging budget
+    assert call(out_row_stride=100) == -3
+    assert call(n_experts=0) == -4
+

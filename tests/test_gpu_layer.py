@@ -1,0 +1,202 @@
+"""The fused layer call (moe_expert_layer: routing, q8_1, gate/up, SwiGLU + q8_1 and down in one
+launch) against the separate steps and against the CPU oracle.
+
+The fused call performs the same arithmetic in the same order as the separate kernels, so every
+output (grouping, activation q8_1, gate/up rows, q8_1 h rows, output rows) must match them bit for
+bit; the output is also checked against the oracle directly (max|err| / max|ref| <= 1e-5 unless
+an h code flipped, as in the end-to-end parity test).
+"""
+import numpy as np
+import pytest
+import torch
+
+import harness as H
+import synth
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-5
+
+CASES = [("tiny", (synth.Q8_0, synth.Q8_0), 1, None), ("verify", (synth.CB2, synth.NL4), 4, None),
+         ("window48", (synth.CB3, synth.NL4), 1, None), ("window48", (synth.CB3, synth.NL4), 2, synth.CB3X),
+         ("window48", (synth.CB3, synth.NL4), 4, synth.CB3X), ("verify", (synth.CB2, synth.NL4), 4, synth.CB2X),
+         ("verify", (synth.CB2, synth.NL4), 8, None), ("window48", (synth.CB3, synth.NL4), 6, synth.CB3X),
+         ("sweep", (synth.Q4B, synth.NL4), 4, None), ("sweep", (synth.CB3, synth.Q8_0), 4, None)]
+CASE_IDS = [f"{c[0]}-{synth.NAMES[c[1][0]]}-{synth.NAMES[c[1][1]]}-T{c[2]}" + (f"-{synth.NAMES[c[3]]}" if c[3] else "")
+            for c in CASES]
+
+
+@pytest.fixture(scope="module")
+def m():
+    import quantized_routed_expert_grouped_gb300 as mod
+    mod.lib()
+    return mod
+
+
+class Fused:
+    """Device buffers of one fused call (NaN / 0xA5 prefilled so unwritten rows show)."""
+
+    def __init__(self, m, L, ids=None, flags=1):
+        wl, T = L.wl, L.T
+        n = T * wl.k
+        dev = "cuda"
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.ids = torch.from_numpy(L.ids if ids is None else ids).to(dev)
+        self.x = torch.from_numpy(L.x).to(dev)
+        self.out = torch.full((n, wl.N), float("nan"), dtype=torch.float32, device=dev)
+        self.gu = torch.full((n, 2 * wl.F), float("nan"), dtype=torch.float32, device=dev)
+        self.hq = torch.full((n, wl.F // 32, 36), 0xA5, dtype=torch.uint8, device=dev)
+        self.sync = torch.zeros(m.layer_sync_ints(T, wl.k, wl.F), **i32)
+        self.ge = torch.full((n,), -7, **i32)
+        self.gs = torch.full((n + 1,), -7, **i32)
+        self.ng = torch.full((1,), -7, **i32)
+        self.es = torch.full((n,), -7, **i32)
+        self.ed = torch.full((n,), -7, **i32)
+        self.xq = torch.full((T, wl.N // 32, 36), 0xA5, dtype=torch.uint8, device=dev)
+        self.err = torch.zeros(1, **i32)
+        self.call = m.LayerCall(L.gu_t, L.cb_gu_d, L.dn_t, L.cb_dn_d, wl.N, wl.F, L.tab_gu, L.tab_dn, wl.E, self.ids,
+                                self.x, self.out, self.gu, self.hq, self.sync, self.err, flags, self.ge, self.gs,
+                                self.ng, self.es, self.ed, self.xq)
+
+
+def _separate(m, L):
+    B = H.make_bufs(L)
+    H.gpu_route_and_quantize(m, L, B)
+    H.expert_call(m, L, B)()
+    torch.cuda.synchronize()
+    return B
+
+
+def _bits(t):
+    return t.view(torch.int32).cpu().numpy()
+
+
+def _same_as_separate(F, B, ntot):
+    G = int(B.n_groups.item())
+    assert int(F.ng.item()) == G
+    assert torch.equal(F.ge[:G], B.grp_expert[:G]) and torch.equal(F.gs[:G + 1], B.grp_start[:G + 1])
+    assert torch.equal(F.es[:ntot], B.ent_src[:ntot]) and torch.equal(F.ed[:ntot], B.ent_dst[:ntot])
+    assert torch.equal(F.xq, B.xq)
+    assert np.array_equal(_bits(F.gu[:ntot]), _bits(B.gu[:ntot]))
+    assert torch.equal(F.hq[:ntot], B.hq[:ntot])
+    assert np.array_equal(_bits(F.out), _bits(B.out))
+
+
+@pytest.mark.parametrize("wname,pair,T,xt", CASES, ids=CASE_IDS)
+def test_layer_equals_separate_steps_and_oracle(m, orc, wname, pair, T, xt):
+    wl = synth.WORKLOADS[wname]
+    L0 = H.make_layer(wl, pair, T)
+    L = H.transcoded(m, L0, xt) if xt else L0
+    n = T * wl.k
+    B = _separate(m, L)
+    F = Fused(m, L)
+    F.call()
+    torch.cuda.synchronize()
+    assert int(F.err.item()) == 0 and int(B.err.item()) == 0
+    _same_as_separate(F, B, n)
+    assert not F.sync.any(), "counters must be left zero"
+    ref = H.oracle_call(orc, L0)
+    flips, scale_diffs = H.q8_1_code_flips(F.hq.cpu().numpy(), ref["hq"])
+    assert flips <= max(2, n * wl.F // 4096) and scale_diffs <= 2, (flips, scale_diffs)
+    err = H.rel_err(F.out.cpu().numpy(), ref["out"])
+    assert err <= (TOL if flips == 0 and scale_diffs == 0 else 2e-3), (err, flips)
+    assert H.rel_err(F.gu.cpu().numpy(), ref["gu"]) <= TOL
+
+
+def test_layer_repeated_calls_pdl_and_graph(m, orc):
+    """Several layers sharing one counter array, eager (with and without PDL) and captured in a
+    CUDA graph replayed twice: identical outputs every time, counters left zero."""
+    wl = synth.WORKLOADS["window48"]
+    layers = [H.transcoded(m, H.make_layer(wl, (synth.CB3, synth.NL4), 3, layer=l), synth.CB3X) for l in range(3)]
+    fs = [Fused(m, L) for L in layers]
+    sync = fs[0].sync
+    for f in fs:  # one shared counter array
+        f.call.c.sync = sync.data_ptr()
+    for f in fs:
+        f.call()
+    torch.cuda.synchronize()
+    base = [f.out.clone() for f in fs]
+    for L, f in zip(layers, fs):
+        _same_as_separate(f, _separate(m, L), L.T * wl.k)
+    for flags in (0, 1):
+        for f in fs:
+            f.call.c.flags = flags
+            f.out.fill_(float("nan"))
+            f.call()
+        torch.cuda.synchronize()
+        for f, b in zip(fs, base):
+            assert torch.equal(f.out.view(torch.int32), b.view(torch.int32))
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for f in fs:
+            f.call(s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        for f in fs:
+            f.call()
+    for _ in range(2):
+        for f in fs:
+            f.out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for f, b in zip(fs, base):
+            assert torch.equal(f.out.view(torch.int32), b.view(torch.int32))
+    assert all(int(f.err.item()) == 0 for f in fs)
+    assert not sync.any()
+
+
+def test_layer_dropped_ids_and_empty(m, orc):
+    wl = synth.WORKLOADS["verify"]
+    L = H.make_layer(wl, (synth.CB2, synth.NL4), 4)
+    ids = L.ids.copy()
+    ids[0, 3] = -1
+    ids[2, 0] = wl.E
+    ids[3, 7] = 10 ** 6
+    F = Fused(m, L, ids=ids)
+    F.call()
+    torch.cuda.synchronize()
+    assert int(F.err.item()) == 128  # MOE_ERR_ROUTE only
+    assert not F.sync.any()
+    # the separate path on the same ids
+    Ld = H.Layer(**{**L.__dict__, "ids": ids})
+    B = _separate(m, Ld)
+    ntot = int(B.grp_start[int(B.n_groups.item())].item())
+    assert ntot == wl.k * L.T - 3
+    _same_as_separate(F, B, ntot)
+    out = F.out.cpu().numpy()
+    for r in (0 * wl.k + 3, 2 * wl.k + 0, 3 * wl.k + 7):
+        assert np.isnan(out[r]).all()
+    # every id dropped: nothing computed, nothing written
+    F2 = Fused(m, L, ids=np.full_like(L.ids, -1))
+    F2.call()
+    torch.cuda.synchronize()
+    assert int(F2.err.item()) == 128 and int(F2.ng.item()) == 0
+    assert torch.isnan(F2.out).all() and torch.isnan(F2.gu).all() and (F2.hq == 0xA5).all()
+    assert not F2.sync.any()
+
+
+def test_layer_misaligned_expert_is_skipped(m, orc):
+    """A weight pointer that is not 16-byte aligned: that group is skipped with MOE_ERR_ALIGN, no
+    wait times out, and every other entry's output equals the separate path's."""
+    wl = synth.WORKLOADS["verify"]
+    L = H.make_layer(wl, (synth.CB2, synth.NL4), 4)
+    bad = int(L.ids[1, 2])
+    B = _separate(m, L)
+    tab = L.tab_gu.clone()
+    tab[bad] += 2
+    Lb = H.Layer(**{**L.__dict__, "tab_gu": tab})
+    F = Fused(m, Lb)
+    F.call()
+    torch.cuda.synchronize()
+    assert int(F.err.item()) == 16
+    assert not F.sync.any()
+    out, ref = F.out.cpu().numpy(), B.out.cpu().numpy()
+    for t in range(L.T):
+        for s in range(wl.k):
+            r = t * wl.k + s
+            if int(L.ids[t, s]) == bad:
+                assert np.isnan(out[r]).all()
+            else:
+                assert np.array_equal(out[r].view(np.int32), ref[r].view(np.int32))

@@ -165,7 +165,9 @@ def _stage_inputs(orc, L, r):
 # (workload, (gate/up, down), T, slot layout the gate/up pool is transcoded to or None)
 CASES = [("tiny", (synth.Q8_0, synth.Q8_0), 1, None), ("verify", (synth.CB2, synth.NL4), 4, None),
          ("window48", (synth.CB3, synth.NL4), 1, None), ("window48", (synth.CB3, synth.NL4), 3, None),
-         ("window48", (synth.CB3, synth.NL4), 4, synth.CB3X), ("verify", (synth.CB2, synth.NL4), 4, synth.CB2X)]
+         ("window48", (synth.CB3, synth.NL4), 4, synth.CB3X), ("verify", (synth.CB2, synth.NL4), 4, synth.CB2X),
+         # T > 4: groups of up to T entries, several 4-entry batches per weight tile
+         ("verify", (synth.CB2, synth.NL4), 8, None), ("window48", (synth.CB3, synth.NL4), 6, synth.CB3X)]
 CASE_IDS = [f"{c[0]}-T{c[2]}" + (f"-{synth.NAMES[c[3]]}" if c[3] else "") for c in CASES]
 
 
