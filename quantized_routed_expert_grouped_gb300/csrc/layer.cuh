@@ -336,7 +336,41 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         __threadfence_block();
         bar_arrive(3, NT);  // tables ready
     } else {
-        named_sync(3, NT);
+        // meanwhile the consumer warps quantize the activations (independent of the grouping)
+        const int ct = tid - 32, cnt = NT - 32;
+        // ---- activations: x -> q8_1 of all T tokens, staged in slot t; one lane quad per block
+        {
+            const int nb = A.nb, j = ct & 3, nq = cnt >> 2, tot = L.T * nb;
+            const unsigned qmask = 0xFu << (lane & 28);
+            for (int i0 = ct >> 2; i0 < tot; i0 += 4 * nq) {
+                float4 f[4][2];  // four blocks' loads in flight before any arithmetic
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * nq;
+                    if (i < tot) {
+                        const int t = i / nb, b = i - t * nb;
+                        const float4* xp =
+                            reinterpret_cast<const float4*>(L.x + static_cast<int64_t>(t) * A.K + b * 32 + 8 * j);
+                        f[u][0] = __ldg(xp);
+                        f[u][1] = __ldg(xp + 1);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * nq;
+                    if (i >= tot) break;
+                    const int t = i / nb, b = i - t * nb;
+                    const float v[8] = {f[u][0].x, f[u][0].y, f[u][0].z, f[u][0].w,
+                                        f[u][1].x, f[u][1].y, f[u][1].z, f[u][1].w};
+                    uint32_t w[2], hdr;
+                    int Ssum;
+                    quad_q8_1(v, qmask, w, hdr, Ssum);
+                    stage_quad<GT>(A, smem, t, b, j, w, hdr, Ssum);
+                    if (blockIdx.x == 0 && L.o_xq) put_quad(L.o_xq + i, j, w, hdr);
+                }
+            }
+        }
+        named_sync(3, NT);  // with warp 0's arrival: tables ready, activations staged
     }
     const int G = *rng, ngu = gridDim.x;
     const int32_t* ready = L.sync;  // per group: h blocks written (complete at F/32)
@@ -378,39 +412,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         } else {
             const int cw = warp - 1, ncw = (NT >> 5) - 1, ct = tid - 32, cnt = ncw * 32;
             const uint32_t loff = GT == MOE_CB3 ? lane * 4u : (lane & 15u) * 8u;
-            // ---- activations: x -> q8_1 of all T tokens, staged in slot t; one lane quad per block
-            {
-                const int nb = A.nb, j = ct & 3, nq = cnt >> 2, tot = L.T * nb;
-                const unsigned qmask = 0xFu << (lane & 28);
-                for (int i0 = ct >> 2; i0 < tot; i0 += 4 * nq) {
-                    float4 f[4][2];  // four blocks' loads in flight before any arithmetic
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int i = i0 + u * nq;
-                        if (i < tot) {
-                            const int t = i / nb, b = i - t * nb;
-                            const float4* xp =
-                                reinterpret_cast<const float4*>(L.x + static_cast<int64_t>(t) * A.K + b * 32 + 8 * j);
-                            f[u][0] = __ldg(xp);
-                            f[u][1] = __ldg(xp + 1);
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int i = i0 + u * nq;
-                        if (i >= tot) break;
-                        const int t = i / nb, b = i - t * nb;
-                        const float v[8] = {f[u][0].x, f[u][0].y, f[u][0].z, f[u][0].w,
-                                            f[u][1].x, f[u][1].y, f[u][1].z, f[u][1].w};
-                        uint32_t w[2], hdr;
-                        int Ssum;
-                        quad_q8_1(v, qmask, w, hdr, Ssum);
-                        stage_quad<GT>(A, smem, t, b, j, w, hdr, Ssum);
-                        if (blockIdx.x == 0 && L.o_xq) put_quad(L.o_xq + i, j, w, hdr);
-                    }
-                }
-                named_sync(1, cnt);
-            }
             // ---- gate/up tiles, one at a time with all consumer warps (a warp per 256-weight chunk,
             // lane = row; the last warp to finish sums the chunks): SwiGLU in the tile epilogue, q8_1 of
             // h by the tile that completes the unit, then the group's counter
