@@ -20,7 +20,9 @@ CASES = [("tiny", (synth.Q8_0, synth.Q8_0), 1, None), ("verify", (synth.CB2, syn
          ("window48", (synth.CB3, synth.NL4), 1, None), ("window48", (synth.CB3, synth.NL4), 2, synth.CB3X),
          ("window48", (synth.CB3, synth.NL4), 4, synth.CB3X), ("verify", (synth.CB2, synth.NL4), 4, synth.CB2X),
          ("verify", (synth.CB2, synth.NL4), 8, None), ("window48", (synth.CB3, synth.NL4), 6, synth.CB3X),
-         ("sweep", (synth.Q4B, synth.NL4), 4, None), ("sweep", (synth.CB3, synth.Q8_0), 4, None)]
+         ("sweep", (synth.Q4B, synth.NL4), 4, None), ("sweep", (synth.CB3, synth.Q8_0), 4, None),
+         ("sweep", (synth.Q8_0, synth.Q8_0), 4, None), ("sweep", (synth.CB2, synth.NL4), 4, None),
+         ("sweep", (synth.Q4B, synth.Q8_0), 4, None), ("sweep", (synth.CB3, synth.NL4), 4, None)]
 CASE_IDS = [f"{c[0]}-{synth.NAMES[c[1][0]]}-{synth.NAMES[c[1][1]]}-T{c[2]}" + (f"-{synth.NAMES[c[3]]}" if c[3] else "")
             for c in CASES]
 
@@ -200,3 +202,23 @@ def test_layer_misaligned_expert_is_skipped(m, orc):
                 assert np.isnan(out[r]).all()
             else:
                 assert np.array_equal(out[r].view(np.int32), ref[r].view(np.int32))
+
+
+@pytest.mark.parametrize("layer", [17, 47])
+def test_layer_sampled_window_layers(m, orc, layer):
+    """Other layers of the 48-layer window (their own experts, routing and activations) at T = 4 on
+    the slot layout: fused equals separate bit for bit and matches the oracle."""
+    wl = synth.WORKLOADS["window48"]
+    L0 = H.make_layer(wl, (synth.CB3, synth.NL4), 4, layer=layer)
+    L = H.transcoded(m, L0, synth.CB3X)
+    B = _separate(m, L)
+    F = Fused(m, L)
+    F.call()
+    torch.cuda.synchronize()
+    assert int(F.err.item()) == 0
+    _same_as_separate(F, B, 4 * wl.k)
+    ref = H.oracle_call(orc, L0)
+    flips, scale_diffs = H.q8_1_code_flips(F.hq.cpu().numpy(), ref["hq"])
+    err = H.rel_err(F.out.cpu().numpy(), ref["out"])
+    assert err <= (TOL if flips == 0 and scale_diffs == 0 else 2e-3), (err, flips)
+
