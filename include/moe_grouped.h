@@ -279,7 +279,7 @@ typedef struct moe_layer_call {
 } moe_layer_call;
 
 /* Number of int32 counters moe_expert_layer needs for windows of T tokens, top-k, n_ff
- * (T*k + 1; 0 for invalid arguments). */
+ * (T*k + 2; 0 for invalid arguments). */
 int64_t moe_layer_sync_ints(int T, int k, int n_ff);
 
 int moe_expert_layer(const moe_layer_call* call, cudaStream_t stream);

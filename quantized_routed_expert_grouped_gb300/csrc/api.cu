@@ -268,19 +268,20 @@ int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, 
     phase_warps(A.nch, A);
     phase_warps(D.nch, D);
     A.RT = 32 * rbA <= 96 * 1024 ? 32 : 16;
-    // activations: T token rows (gate/up role) or 4 entry rows (down role), the same region
+    // activations: T token rows (gate/up role) and two buffers of 4 entry rows (down role, staged
+    // by the producer warp while the consumers work on the other buffer), separate regions
     const int actqA = round_up(T * 2 * A.nbp * 16, 128), act2A = round_up(T * A.nb * 8, 128);
     const int actqD = round_up(2 * kBatch * 2 * D.nbp * 16, 128);
     const int act2D = round_up(2 * kBatch * D.nb * 8, 128);
     if (actqA + act2A > 64 * 1024) return MOE_E_CAP;
-    const int act = actqA + act2A > actqD + act2D ? actqA + act2A : actqD + act2D;
+    const int act = actqA + act2A + actqD + act2D;
     const int grp = round_up(24 * n + 4 * (n + 1), 128), entb = round_up(8 * n, 128);
     const int route = round_up(4 * (6 * n + 4), 128);
     const int cbb = cb_type(gt) ? 32768 : 0;
     const int ptrs = E <= kLayerPtrCache ? round_up(16 * E, 128) : 0;
-    const int fixed = cbb + act + 2 * grp + 2 * entb + route + ptrs + 512 + 512;
+    const int fixed = cbb + act + 2 * grp + 2 * entb + route + ptrs + 512 + 1024;
     // one ring for both phases: a slot holds a gate/up tile (RT rows) or a down tile of nsub 32-row
-    // sub-tiles; per stage a slot, partial sums and one unit buffer
+    // sub-tiles; per stage a slot and its partial sums
     const int64_t tileA = A.RT * rbA;
     int nsub = static_cast<int>(tileA / (32 * rbD));
     nsub = nsub < 1 ? 1 : nsub > 4 ? 4 : nsub;
@@ -289,7 +290,7 @@ int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, 
     const int stage = round_up(static_cast<int>(tile) + 16, 128);
     const int pA = A.nch * 4 * A.RT, pD = D.nch * 4 * D.RT;
     const int part = 4 * (pA > pD ? pA : pD);
-    int S = (kSmemPerSm - 1024 - fixed) / (stage + part + 512);
+    int S = (kSmemPerSm - 1024 - fixed) / (stage + part);
     S = S > 8 ? 8 : S;
     if (S < 2) return MOE_E_SHAPE;
     int off = cbb;  // the gate/up codebook sits at offset 0
@@ -297,11 +298,10 @@ int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, 
     off += S * stage;
     A.off_part = D.off_part = off;
     off += S * part;
-    L.off_unit = off;
-    off += S * 512;
-    A.off_actq = D.off_actq = off;
+    A.off_actq = off;
     A.off_act2 = off + actqA;
-    D.off_act2 = off + actqD;
+    D.off_actq = off + actqA + act2A;
+    D.off_act2 = D.off_actq + actqD;
     off += act;
     A.off_grp = off;
     off += grp;
@@ -316,9 +316,9 @@ int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, 
     L.off_ptr = ptrs ? off : 0;
     off += ptrs;
     A.off_bar = D.off_bar = off;
-    off += 512;  // 5 x 8 mbarriers
+    off += 512;  // 3 x 8 ring mbarriers + 16 descriptor mbarriers
     A.off_misc = D.off_misc = off;
-    off += 512;
+    off += 1024;
     A.stages = D.stages = S;
     A.stage_bytes = D.stage_bytes = stage;
     A.part_bytes = D.part_bytes = part;
@@ -467,7 +467,7 @@ int moe_expert_grouped(const moe_expert_call* c, cudaStream_t stream) {
 
 int64_t moe_layer_sync_ints(int T, int k, int n_ff) {
     if (T <= 0 || k <= 0 || n_ff <= 0 || n_ff % 32) return 0;
-    return static_cast<int64_t>(T) * k + 1;
+    return static_cast<int64_t>(T) * k + 2;
 }
 
 int moe_expert_layer(const moe_layer_call* c, cudaStream_t stream) {

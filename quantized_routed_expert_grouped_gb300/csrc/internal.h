@@ -84,7 +84,6 @@ struct LayerArgs {
     int F, nbj;          // n_ff, n_ff / 32
     int nsub;            // 32-row sub-tiles per down tile
     int upg, tpu;        // gate/up units (32 h values) per group, ring tiles per unit
-    int off_unit;        // shared-memory unit buffers: [stages][4 entries][32] h values
     int off_route;       // shared-memory routing scratch
     int off_ptr;         // shared-memory cache of both expert pointer tables (0: not cached)
 };

@@ -10,10 +10,14 @@
 //  * Every CTA groups the window's top-k ids itself (one warp: ballots and shuffles when T*k <= 32);
 //    CTA 0 also writes the grouping and the activation q8_1 rows to global memory for inspection.
 //    The expert pointer tables, like the codebooks, are read before the dependency wait.
-//  * Two phases on every CTA, one after the other: gate/up, then down. Gate/up work comes in units
-//    of one 32-value h block of one group, dealt round-robin in group order (tile-sized work,
-//    evenly spread); down work is a contiguous, cost-balanced run of (group, 8-row block) pairs
-//    per CTA, which waits only for its own (at most two) groups.
+//  * One stream of work items for the whole grid, pulled in order from a global counter: first
+//    the gate/up units (one 32-value h block of one group, group-major), then the down chunks (a
+//    few row tiles of one group, group-major). A CTA's first item is its own index; it fetches the
+//    next index while the current item streams. So gate/up and down overlap across the grid,
+//    faster CTAs take more items, and no CTA waits for a phase boundary.
+//  * Each CTA has one producer warp and 15 consumer warps around a ring of shared-memory slots
+//    (1-D bulk copies and full/empty mbarriers). The producer writes a descriptor per ring index
+//    (kind, group, rows, entries); the consumer warps all walk the same ring indices.
 //  * A gate/up unit is gate rows 32jb .. 32jb+31 and up rows F+32jb .. F+32jb+31 of one expert:
 //    two ring tiles (four when rows are long) of 16 gate rows and the matching 16 up rows (two
 //    bulk copies into one slot). Chunk warps (a warp per 256-weight chunk, lane = row) only compute
@@ -23,18 +27,18 @@
 //    writes their q8_1 block to hq and adds one to the group's counter (after a fence). Every h
 //    block is computed once, and no compute warp waits on an epilogue.
 //  * The activations are staged as q8_1 by every CTA (one lane quad per block).
-//  * A down tile holds up to nsub 32-row sub-tiles (the ring slot is sized for a gate/up tile); its
-//    (sub-tile, 256-weight chunk) work items are dealt to the consumer warps in turn across tiles;
-//    the CTA waits (bounded) for its groups' counters to reach F/32 and stages their q8_1 h rows
-//    from hq once (two groups of up to 4 entries; larger runs restage per group or 4-entry batch).
-//  * Both phases stream their tiles through one ring of shared-memory slots (1-D bulk copies and
-//    mbarriers, issued by a producer warp); the down tiles follow the gate/up tiles in the ring,
-//    so they are prefetched while the last gate/up tiles are computed.
+//  * Down chunks: the producer copies the chunk's weight tiles into free slots first, then waits
+//    (bounded) for the group's counter to reach F/32 and stages its q8_1 h rows from hq into one
+//    of two buffers (4-entry batches; a buffer is refilled once every tile that read it has been
+//    released), then publishes the tiles. A down tile holds up to nsub 32-row sub-tiles; its
+//    (sub-tile, 256-weight chunk) work items are dealt to the consumer warps in turn across
+//    tiles, and the last warp of a sub-tile sums its chunks and writes the output rows.
 //  * The counters live in a caller-owned int array that must be zero before the first call; the
 //    last CTA to finish (a global exit counter) zeroes them again, so every call starts clean.
-//  * Every wait (mbarriers, group counters) has a time limit; on expiry the kernel sets
-//    MOE_ERR_TIMEOUT, skips the remaining work, waits (bounded) for its own copies in flight
-//    and still takes part in the exit count.
+//  * Every wait (mbarriers, group counters, the ring) has a time limit; on expiry the kernel sets
+//    MOE_ERR_TIMEOUT, the producer stops, the consumers walk the published ring indices without
+//    computing, the CTA waits (bounded) for its own copies in flight and still takes part in the
+//    exit count.
 #pragma once
 
 #include "gemv.cuh"
@@ -42,6 +46,8 @@
 #include "route.cuh"
 
 namespace moe {
+
+constexpr int kDescRing = 16;  // tile descriptors in flight per CTA (ring indices)
 
 __device__ __forceinline__ int ld_acquire(const int32_t* p) {
     int v;
@@ -165,56 +171,26 @@ __device__ __forceinline__ void route_warp(const int32_t* ids, int n, int k, int
     }
 }
 
-// Flattened (group, 8-row block) index at which the cumulative cost reaches `target` (cum: int32
-// inclusive prefix of cost * rbpg, cum[0] = 0).
-__device__ __forceinline__ int locate32(const GroupInfo* gi, const int* cum, int G, int rbpg, int target) {
-    if (target >= cum[G]) return G * rbpg;
-    int lo = 0, hi = G - 1;  // first g with cum[g+1] > target (its cost is > 0)
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (cum[mid + 1] > target) hi = mid;
-        else lo = mid + 1;
-    }
-    return lo * rbpg + (target - cum[lo]) / gi[lo].cost;
-}
-
 // One warp: group tables for both phases (weight pointers from the shared-memory cache when it
-// holds them; cost 0 marks a skipped group; a down 8-row block of a group of n entries costs
-// alpha + n), the entry tables, the inspection copies (CTA 0) and this CTA's down range
-// misc[10..11] (a contiguous, cost-balanced run of (group, 8-row block) pairs).
+// holds them; cost 0 marks a skipped group), the entry tables and the inspection copies (CTA 0).
 template <int GT, int DT>
 __device__ __forceinline__ void build_tables(const LayerArgs& L, const uint8_t* const* pcA, const uint8_t* const* pcD,
                                              const int* rgx, const int* rgs, const int* rng, const int* rsrc,
-                                             const int* rdst, GroupInfo* giA, GroupInfo* giD, int* cumD, int2* entA,
-                                             int2* entD, int* misc, int lane) {
+                                             const int* rdst, GroupInfo* giA, GroupInfo* giD, int2* entA, int2* entD,
+                                             int* misc, int lane) {
     const GemvArgs& A = L.gu;
     const GemvArgs& D = L.dn;
-    const int G = *rng, ntot = rgs[G], rbpgD = D.rows >> 3;
+    const int G = *rng, ntot = rgs[G];
     const bool report = blockIdx.x == 0;
-    int run = 0;
-    for (int base = 0; base < G; base += 32) {
-        const int g = base + lane;
-        int cD = 0;
-        if (g < G) {
-            const int x = rgx[g], e0 = rgs[g], e1 = rgs[g + 1];
-            const uint8_t* pa = pcA ? pcA[x] : static_cast<const uint8_t*>(A.w[x]);
-            const uint8_t* pd = pcD ? pcD[x] : static_cast<const uint8_t*>(D.w[x]);
-            const bool ok = ((reinterpret_cast<uintptr_t>(pa) | reinterpret_cast<uintptr_t>(pd)) & 15u) == 0;
-            if (!ok && report) set_err(A.err, MOE_ERR_ALIGN);
-            cD = ok ? D.alpha + (e1 - e0) : 0;
-            giA[g] = GroupInfo{pa, x, e0, e1, ok ? 1 : 0};
-            giD[g] = GroupInfo{pd, x, e0, e1, cD};
-        }
-        int sD = cD * rbpgD;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, sD, o);
-            if (lane >= o) sD += y;
-        }
-        if (g < G) cumD[g + 1] = run + sD;
-        run += __shfl_sync(0xffffffffu, sD, 31);
+    for (int g = lane; g < G; g += 32) {
+        const int x = rgx[g], e0 = rgs[g], e1 = rgs[g + 1];
+        const uint8_t* pa = pcA ? pcA[x] : static_cast<const uint8_t*>(A.w[x]);
+        const uint8_t* pd = pcD ? pcD[x] : static_cast<const uint8_t*>(D.w[x]);
+        const bool ok = ((reinterpret_cast<uintptr_t>(pa) | reinterpret_cast<uintptr_t>(pd)) & 15u) == 0;
+        if (!ok && report) set_err(A.err, MOE_ERR_ALIGN);
+        giA[g] = GroupInfo{pa, x, e0, e1, ok ? 1 : 0};
+        giD[g] = GroupInfo{pd, x, e0, e1, ok ? 1 : 0};
     }
-    if (lane == 0) cumD[0] = 0;
     for (int e = lane; e < ntot; e += 32) {
         entA[e] = make_int2(rsrc[e], e);
         entD[e] = make_int2(e, rdst[e]);
@@ -231,12 +207,11 @@ __device__ __forceinline__ void build_tables(const LayerArgs& L, const uint8_t* 
         }
     }
     __syncwarp();
-    if (lane < 2) {  // boundary c * tot / grid without 64-bit division (tot < 2^31)
-        const int c = blockIdx.x + lane, grid = gridDim.x;
-        const int target = (run / grid) * c + ((run % grid) * c) / grid;
-        misc[10 + lane] = locate32(giD, cumD, G, rbpgD, target);
-    }
-    __syncwarp();
+}
+
+// `count` arrivals at once on a shared-memory mbarrier.
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ void bar_arrive(int id, int threads) {
@@ -276,14 +251,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + A.off_bar);
     uint64_t* empty = full + SB;
     uint64_t* cdone = empty + SB;  // gate/up: a tile's chunk partials are written (one arrival per chunk)
-    // misc: [0] tiles issued, [1] abort flag, [2] last-CTA flag, [12] gate/up CTAs,
-    // [16 + u] tiles done of unit buffer u, [32 + s] sub-tiles done of slot s,
-    // [64 + 8s + b] warps done with sub-tile b of slot s
+    uint64_t* dread = cdone + SB;  // descriptor d read by every consumer warp
+    // misc: [0] tiles published, [1] abort flag, [2] last-CTA flag, [5] no more tiles, [6] copies issued,
+    // [16 + u % 8] tiles done of gate/up unit u (barrier path), [32 + s] sub-tiles done of slot s,
+    // [64 + 8s + b] warps done with sub-tile b of slot s, [128 + 8d ..] descriptor d of ring index q
+    // (d = q % kDescRing)
     int* misc = reinterpret_cast<int*>(smem + A.off_misc);
     volatile int* vmisc = misc;
     GroupInfo* giA = reinterpret_cast<GroupInfo*>(smem + A.off_grp);
     GroupInfo* giD = reinterpret_cast<GroupInfo*>(smem + D.off_grp);
-    int* cumD = reinterpret_cast<int*>(giD + n);  // down cost prefix [G + 1]
     int2* entA = reinterpret_cast<int2*>(smem + A.off_ent);  // entry -> (token row, gate/up row)
     int2* entD = reinterpret_cast<int2*>(smem + D.off_ent);  // entry -> (h row, output row)
     int* rs = reinterpret_cast<int*>(smem + L.off_route);
@@ -295,18 +271,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     int* rng = rgs + n + 1;
     int* rsrc = rng + 1;
     int* rdst = rsrc + n;
-    float* ubuf = reinterpret_cast<float*>(smem + L.off_unit);  // [stages][4 entries][32] h values
     // expert pointer tables cached in shared memory (static data: read before the dependency wait)
     const uint8_t** pcA = L.off_ptr ? reinterpret_cast<const uint8_t**>(smem + L.off_ptr) : nullptr;
     const uint8_t** pcD = pcA ? pcA + A.n_experts : nullptr;
 
-    if (tid < 128) misc[tid] = 0;
-    if (tid == 0)
+    if (tid < 256) misc[tid] = 0;
+    if (tid == 0) {
         for (int s = 0; s < SB; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
             mbar_init(&cdone[s], A.nch);
         }
+        for (int d = 0; d < kDescRing; ++d) mbar_init(&dread[d], (NT >> 5) - 1);
+    }
     fence_barrier_init();
     // static data before the dependency wait: codebook replicas, NL4 tables, pointer tables
     if (warp > 0) stage_codebook<GT>(A, smem, tid - 32, NT - 32);
@@ -332,7 +309,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     if (warp == 0) {
         if (n <= 32) route_warp(L.ids, n, L.k, A.n_experts, rgx, rgs, rng, rsrc, rdst, A.err, blockIdx.x == 0, lane);
         __syncwarp();
-        build_tables<GT, DT>(L, pcA, pcD, rgx, rgs, rng, rsrc, rdst, giA, giD, cumD, entA, entD, misc, lane);
+        build_tables<GT, DT>(L, pcA, pcD, rgx, rgs, rng, rsrc, rdst, giA, giD, entA, entD, misc, lane);
         __threadfence_block();
         bar_arrive(3, NT);  // tables ready
     } else {
@@ -372,163 +349,302 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         }
         named_sync(3, NT);  // with warp 0's arrival: tables ready, activations staged
     }
-    const int G = *rng, ngu = gridDim.x;
+    const int G = *rng;
     const int32_t* ready = L.sync;  // per group: h blocks written (complete at F/32)
-    int qA = 0;  // gate/up tiles of this CTA (the down ring's tiles are numbered after them)
+    // ---- one stream of work items for the whole grid, taken in order from a global counter:
+    // gate/up units (group-major), then down chunks of dchunk tiles of one group (group-major).
+    // Each CTA's producer warp pulls items and streams their tiles through the ring, writing a
+    // descriptor per ring index; the consumers follow the ring. A descriptor is reused kDescRing
+    // indices later, once every consumer warp has read it (warps that take no part in a tile may
+    // lag behind the warps that release its slot). The producer warp also stages each down
+    // group's q8_1 h rows (4-entry batches) into one of two buffers, so the consumer warps never
+    // stop for a restage: a buffer is refilled once every tile that read it has been released.
+    const int S = A.stages, RT = A.RT, half = RT >> 1, RTD = D.RT;
+    const int tpg = (D.rows + RTD - 1) / RTD;
+    int dchunk = (G * tpg) / (2 * static_cast<int>(gridDim.x));  // about two down items per CTA
+    dchunk = dchunk < 1 ? 1 : dchunk > 3 ? 3 : dchunk;
+    const int nunits = G * upg, cpg = (tpg + dchunk - 1) / dchunk;
+    const int nitems = nunits + G * cpg;
+    int* work = L.sync + n + 1;  // global item counter
+    // per ring index q (d = q % kDescRing): [8d] kind (0 gate/up, 1 down), [8d+1] group,
+    // [8d+2] jb or first row, [8d+3] h or rows, down only: [8d+4] first entry, [8d+5] entries,
+    // [8d+6] first staging slot
+    int* desc = misc + 128;
 
-    {
-        const int S = A.stages, RT = A.RT, half = RT >> 1, nunits = G * upg;
-        if (warp == 0) {
-            // ---- gate/up producer: this CTA's units (round-robin in group order), tpu tiles each,
-            // each tile two bulk copies (gate rows, up rows) into one slot
-            if (lane == 0) {
-                int issued = 0;
-                const uint32_t hb = static_cast<uint32_t>(half) * static_cast<uint32_t>(A.row_bytes);
-                for (int i = blockIdx.x; i < nunits; i += ngu) {
-                    const int g = i / upg, jb = i - g * upg;
-                    const GroupInfo gr = giA[g];
-                    if (gr.cost == 0) continue;
-                    bool stop = false;
-                    for (int h = 0; h < tpu; ++h) {
-                        const int s = issued % S;
-                        if (vmisc[1] || (issued >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>(issued / S - 1) & 1u))) {
-                            if (!vmisc[1]) set_err(A.err, MOE_ERR_TIMEOUT);
-                            vmisc[1] = 1;
-                            stop = true;
-                            break;
-                        }
-                        uint8_t* dst = smem + A.off_ring + static_cast<size_t>(s) * A.stage_bytes;
-                        const size_t rg = static_cast<size_t>(32 * jb + h * half);
-                        mbar_arrive_expect_tx(&full[s], 2 * hb);
-                        bulk_g2s(dst, gr.ptr + rg * A.row_bytes, hb, &full[s]);
-                        bulk_g2s(dst + hb, gr.ptr + (rg + F) * A.row_bytes, hb, &full[s]);
-                        ++issued;
-                        __threadfence_block();
-                        vmisc[0] = issued;
-                    }
-                    if (stop) break;
-                }
+    if (warp == 0) {
+        // lane 0 claims slots, issues the copies and publishes the ring indices; the whole warp
+        // stages h rows
+        int issued = 0;                          // ring indices published (lane 0)
+        int st_g = -1, st_b0 = -1, st_n = 0;     // staged group and batch, stagings so far
+        int st_last = 0;                         // first ring index of the last staging (lane 0)
+        bool stop = false;
+        // ring slot j % S free for index j: the tile S indices earlier released (lane 0)
+        auto slot_free = [&](int j) -> bool {
+            if (vmisc[1]) return false;
+            if (j >= S && !mbar_wait_bounded(&empty[j % S], static_cast<uint32_t>(j / S - 1) & 1u)) {
+                set_err(A.err, MOE_ERR_TIMEOUT);
+                vmisc[1] = 1;
+                return false;
             }
-        } else {
-            const int cw = warp - 1, ncw = (NT >> 5) - 1, ct = tid - 32, cnt = ncw * 32;
-            const uint32_t loff = GT == MOE_CB3 ? lane * 4u : (lane & 15u) * 8u;
-            // ---- gate/up tiles, one at a time with all consumer warps (a warp per 256-weight chunk,
-            // lane = row; the last warp to finish sums the chunks): SwiGLU in the tile epilogue, q8_1 of
-            // h by the tile that completes the unit, then the group's counter
-            const int64_t gst = A.out_stride;
-            bool multi = false;
-            for (int g = 0; g < G; ++g) multi |= giA[g].cost != 0 && giA[g].e1 - giA[g].e0 > kMaxEntriesPerPass;
-            const int cwc = A.nch < ncw ? A.nch : ncw;  // chunk warps
-            const int ew = ncw - cwc > 4 ? 4 : ncw - cwc;  // epilogue warps
-            if (!multi && ew > 0) {
-                // Chunk warps only compute (a warp per chunk, lane = row) and arrive on the slot's
-                // chunk-done barrier; epilogue warp u % ew takes unit u: per tile it sums the chunk
-                // partials, releases the slot, writes the gate/up rows and keeps SwiGLU(gate, up) of its
-                // rows; with the unit's 32 h values per entry gathered in its lanes it writes their q8_1
-                // block to hq and adds one to the group's counter.
-                const int ewi = cw - cwc;  // epilogue warp index (>= 0)
-                int q = 0, k = 0;          // tile and unit counters of this CTA
-                for (int i = blockIdx.x; i < nunits; i += ngu) {
-                    const int g = i / upg, jb = i - g * upg;
-                    const GroupInfo gr = giA[g];
-                    if (gr.cost == 0) continue;
-                    const int ku = k++;
-                    const int ne = gr.e1 - gr.e0;
-                    int slots[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) slots[e] = entA[gr.e0 + (e < ne ? e : ne - 1)].x;
-                    const bool mine_unit = ewi >= 0 && ewi < ew && ku % ew == ewi;
-                    float hv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    for (int h = 0; h < tpu; ++h) {
-                        const int qq = q++, slot = qq % S;
-                        const uint8_t* tile = smem + A.off_ring + static_cast<size_t>(slot) * A.stage_bytes;
-                        float* part = reinterpret_cast<float*>(smem + A.off_part + static_cast<size_t>(slot) * A.part_bytes);
-                        if (cw < cwc) {
-                            if (!vmisc[1] &&
-                                !(wait_issued(vmisc, qq) && mbar_wait_bounded(&full[slot], static_cast<uint32_t>(qq / S) & 1u))) {
-                                set_err(A.err, MOE_ERR_TIMEOUT);
-                                vmisc[1] = 1;
-                            }
-                            const bool skip = vmisc[1] != 0;
-                            for (int c = cw; c < A.nch; c += cwc) {
-                                if (!skip && lane < RT) chunk_part<GT>(A, smem, tile, part, ne, c, lane, loff, tabA, slots);
-                                __syncwarp();
-                                if (lane == 0) mbar_arrive(&cdone[slot]);
-                            }
-                        } else if (mine_unit) {
-                            if (!vmisc[1] &&
-                                !(wait_issued(vmisc, qq) && mbar_wait_bounded(&cdone[slot], static_cast<uint32_t>(qq / S) & 1u))) {
-                                set_err(A.err, MOE_ERR_TIMEOUT);
-                                vmisc[1] = 1;
-                            }
-                            const bool skip = vmisc[1] != 0;
-                            float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                            if (!skip && lane < RT)
-#pragma unroll
-                                for (int e = 0; e < 4; ++e)
-                                    if (e < ne) {
-                                        float sv = part[e * RT + lane];
-                                        for (int cc = 1; cc < A.nch; ++cc)
-                                            sv = __fadd_rn(sv, part[(cc * kMaxEntriesPerPass + e) * RT + lane]);
-                                        v[e] = sv;
-                                    }
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&empty[slot]);  // partials read: the slot is free
-                            // gate/up row of tile row `lane`
-                            const int rowg = 32 * jb + h * half + (lane < half ? lane : lane - half + F);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                if (e >= ne) break;
-                                if (!skip && lane < RT) A.out[static_cast<int64_t>(gr.e0 + e) * gst + rowg] = v[e];
-                                const float uv = __shfl_down_sync(0xffffffffu, v[e], half);
-                                // this tile's h for j = h*half + lane (lane < half), moved to lane h*half + lane
-                                const float ht = __shfl_up_sync(0xffffffffu, swiglu_rn(v[e], uv), h * half);
-                                if (lane >= h * half && lane < (h + 1) * half) hv[e] = ht;
-                            }
-                        }
-                    }
-                    if (mine_unit && !vmisc[1]) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (e < ne) warp_q8_1(hv[e], L.hq + static_cast<int64_t>(gr.e0 + e) * L.nbj + jb, lane);
-                        __syncwarp();
-                        if (lane == 0) {
-                            __threadfence();
-                            atomicAdd(L.sync + g, 1);
-                        }
-                    }
-                }
-                qA = q;
-            } else {
-            int q = 0, k = 0;  // tile and unit counters of this CTA
-            for (int i = blockIdx.x; i < nunits; i += ngu) {
+            return true;
+        };
+        // descriptor of ring index `issued` (once every consumer warp has read the one kDescRing
+        // indices earlier), then the index is published (lane 0)
+        auto publish = [&](int kind, int g, int a0, int a1, int e0, int ne, int s0) -> bool {
+            const int d = issued % kDescRing;
+            if (issued >= kDescRing && !mbar_wait_bounded(&dread[d], static_cast<uint32_t>(issued / kDescRing - 1) & 1u)) {
+                if (!vmisc[1]) set_err(A.err, MOE_ERR_TIMEOUT);
+                vmisc[1] = 1;
+                return false;
+            }
+            int* dd = desc + 8 * d;
+            dd[0] = kind;
+            dd[1] = g;
+            dd[2] = a0;
+            dd[3] = a1;
+            dd[4] = e0;
+            dd[5] = ne;
+            dd[6] = s0;
+            ++issued;
+            __threadfence_block();
+            vmisc[0] = issued;
+            return true;
+        };
+        // copy of ring index j's tile into its slot; vmisc[6]: copies issued (lane 0)
+        auto copy_tile = [&](int j, const uint8_t* src0, uint32_t b0, const uint8_t* src1, uint32_t b1) {
+            uint8_t* dst = smem + A.off_ring + static_cast<size_t>(j % S) * A.stage_bytes;
+            mbar_arrive_expect_tx(&full[j % S], b0 + b1);
+            bulk_g2s(dst, src0, b0, &full[j % S]);
+            if (b1) bulk_g2s(dst + b0, src1, b1, &full[j % S]);
+            vmisc[6] = j + 1;
+        };
+        const uint32_t hb = static_cast<uint32_t>(half) * static_cast<uint32_t>(A.row_bytes);
+        // the first item of CTA b is item b; later ones come from the counter, whose next value is
+        // fetched while the current item streams
+        int nx = 0;
+        for (int i = blockIdx.x; !stop && i < nitems; i = __shfl_sync(0xffffffffu, nx, 0)) {
+            if (lane == 0) nx = static_cast<int>(gridDim.x) + atomicAdd(work, 1);
+            if (i < nunits) {
                 const int g = i / upg, jb = i - g * upg;
                 const GroupInfo gr = giA[g];
                 if (gr.cost == 0) continue;
-                const int ub = k++ % S;  // unit buffer
-                float* ux = ubuf + ub * 128;
-                const bool single = gr.e1 - gr.e0 <= kMaxEntriesPerPass;
-                for (int h = 0; h < tpu; ++h) {
-                    const int qq = q++, slot = qq % S;
-                    const uint8_t* tile = smem + A.off_ring + static_cast<size_t>(slot) * A.stage_bytes;
-                    float* part = reinterpret_cast<float*>(smem + A.off_part + static_cast<size_t>(slot) * A.part_bytes);
-                    // gate/up row of tile row `lane`
-                    const int rowg = 32 * jb + h * half + (lane < half ? lane : lane - half + F);
+                if (lane == 0)
+                    for (int h = 0; h < tpu; ++h) {
+                        if (!slot_free(issued)) {
+                            stop = true;
+                            break;
+                        }
+                        const size_t rg = static_cast<size_t>(32 * jb + h * half);
+                        copy_tile(issued, gr.ptr + rg * A.row_bytes, hb, gr.ptr + (rg + F) * A.row_bytes, hb);
+                        if (!publish(0, g, jb, h, 0, 0, 0)) {
+                            stop = true;
+                            break;
+                        }
+                    }
+                stop = __shfl_sync(0xffffffffu, stop, 0);
+            } else {
+                const int d = i - nunits, g = d / cpg, c = d - g * cpg;
+                const GroupInfo gr = giD[g];
+                if (gr.cost == 0) continue;
+                const int t0 = c * dchunk, t1 = t0 + dchunk < tpg ? t0 + dchunk : tpg;
+                auto tile_src = [&](int t, uint32_t& bytes) {
+                    const int row0 = t * RTD, nrows = D.rows - row0 < RTD ? D.rows - row0 : RTD;
+                    bytes = static_cast<uint32_t>(nrows) * static_cast<uint32_t>(D.row_bytes);
+                    return gr.ptr + static_cast<size_t>(row0) * D.row_bytes;
+                };
+                for (int b0 = gr.e0; b0 < gr.e1 && !stop; b0 += kMaxEntriesPerPass) {
+                    const int ne = gr.e1 - b0 < kMaxEntriesPerPass ? gr.e1 - b0 : kMaxEntriesPerPass;
+                    int pre = 0;  // tiles of this batch copied ahead of the h wait (lane 0)
+                    if (g != st_g || b0 != st_b0) {
+                        int ok = 1;
+                        if (lane == 0) {
+                            // the weights do not depend on h: copy up to S tiles into free slots first
+                            for (int t = t0; t < t1 && pre < S && ok; ++t, ++pre) {
+                                ok = slot_free(issued + pre);
+                                uint32_t bytes;
+                                const uint8_t* src = tile_src(t, bytes);
+                                if (ok) copy_tile(issued + pre, src, bytes, nullptr, 0);
+                            }
+                            // h rows of group g complete; buffer st_n & 1 free (from the third
+                            // staging on): every ring index before the last staging's first one
+                            // released (indices before issued - S are, as their slots were claimed
+                            // again)
+                            ok = ok && !vmisc[1] && wait_count(ready + g, upg);
+                            if (st_n >= 2)
+                                for (int j = issued - S > 0 ? issued - S : 0; ok && j < st_last; ++j)
+                                    ok = mbar_wait_bounded(&empty[j % S], static_cast<uint32_t>(j / S) & 1u);
+                            if (!ok && !vmisc[1]) set_err(A.err, MOE_ERR_TIMEOUT);
+                            if (!ok) vmisc[1] = 1;
+                            st_last = issued;
+                        }
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok) {
+                            stop = true;
+                            break;
+                        }
+                        __syncwarp();
+                        __threadfence();  // lane 0's acquire of the counter covers every lane's loads
+                        stage_entries<DT, true>(D, smem, entD, b0, ne, kMaxEntriesPerPass * (st_n & 1), lane, 32);
+                        __syncwarp();
+                        st_g = g;
+                        st_b0 = b0;
+                        ++st_n;
+                    }
+                    const int s0 = kMaxEntriesPerPass * ((st_n - 1) & 1);
+                    if (lane == 0)
+                        for (int t = t0; t < t1; ++t) {
+                            if (t - t0 >= pre) {
+                                if (!slot_free(issued)) {
+                                    stop = true;
+                                    break;
+                                }
+                                uint32_t bytes;
+                                const uint8_t* src = tile_src(t, bytes);
+                                copy_tile(issued, src, bytes, nullptr, 0);
+                            }
+                            const int row0 = t * RTD, nrows = D.rows - row0 < RTD ? D.rows - row0 : RTD;
+                            if (!publish(1, g, row0, nrows, b0, ne, s0)) {
+                                stop = true;
+                                break;
+                            }
+                        }
+                    stop = __shfl_sync(0xffffffffu, stop, 0);
+                }
+            }
+        }
+        if (lane == 0) vmisc[5] = 1;  // no more tiles: the consumers stop at ring index vmisc[0]
+    } else {
+        const int cw = warp - 1, ncw = (NT >> 5) - 1, ct = tid - 32, cnt = ncw * 32;
+        const uint32_t loff = GT == MOE_CB3 ? lane * 4u : (lane & 15u) * 8u;
+        const int64_t gst = A.out_stride;
+        const int cwc = A.nch < ncw ? A.nch : ncw;           // gate/up chunk warps
+        const int ew = ncw - cwc > 4 ? 4 : ncw - cwc;        // gate/up epilogue warps
+        const int ewi = cw - cwc;                            // epilogue warp index (>= 0)
+        int k = -1;                                          // gate/up units seen (the current one)
+        float hv[4] = {0.0f, 0.0f, 0.0f, 0.0f};             // epilogue: the unit's h values, one per lane
+        int wbase = 0;                                       // down: work items dealt so far
+        for (int q = 0;; ++q) {
+            // the next ring index: issued, or the end of the stream. Every warp walks the same ring
+            // indices to the producer's final count (after an abort too, skipping the work), so the
+            // named barriers inside the tiles always see every consumer warp.
+            {
+                const unsigned long long t0 = global_ns();
+                bool more = false;
+                for (uint32_t it = 0;; ++it) {
+                    if (vmisc[0] > q) {
+                        more = true;
+                        break;
+                    }
+                    if (vmisc[5]) {  // the producer is done: its final count was published before
+                        __threadfence_block();
+                        more = vmisc[0] > q;
+                        break;
+                    }
+                    __nanosleep(32);
+                    if ((it & 15u) == 15u) {
+                        // the producer stops at once after an abort, or within one bounded wait
+                        const unsigned long long dt = global_ns() - t0;
+                        if (dt > kWaitLimitNs && !vmisc[1]) {
+                            set_err(A.err, MOE_ERR_TIMEOUT);
+                            vmisc[1] = 1;
+                        }
+                        if (dt > 8 * kWaitLimitNs) break;  // last resort; not reached while the producer runs
+                    }
+                }
+                if (!more) break;
+                __threadfence_block();
+            }
+            const int slot = q % S, dq = q % kDescRing;
+            const int* dd = desc + 8 * dq;
+            const int kind = dd[0], g = dd[1], a0 = dd[2], a1 = dd[3], d4 = dd[4], d5 = dd[5], d6 = dd[6];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&dread[dq]);
+            const uint8_t* tile = smem + A.off_ring + static_cast<size_t>(slot) * A.stage_bytes;
+            float* part = reinterpret_cast<float*>(smem + A.off_part + static_cast<size_t>(slot) * A.part_bytes);
+            if (kind == 0) {
+                // ---- gate/up tile h = a1 of unit (g, jb = a0)
+                const int jb = a0, h = a1;
+                const GroupInfo gr = giA[g];
+                const int ne = gr.e1 - gr.e0;
+                if (h == 0) {
+                    ++k;
+                    hv[0] = hv[1] = hv[2] = hv[3] = 0.0f;
+                }
+                // gate/up row of tile row `lane`
+                const int rowg = 32 * jb + h * half + (lane < half ? lane : lane - half + F);
+                if (ne <= kMaxEntriesPerPass && ew > 0) {
+                    // chunk warps compute and arrive on the slot's chunk-done barrier; epilogue warp k % ew
+                    // sums, releases the slot, writes the rows and keeps SwiGLU(gate, up) in its lanes
+                    int slots[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) slots[e] = entA[gr.e0 + (e < ne ? e : ne - 1)].x;
+                    if (cw < cwc) {
+                        if (!vmisc[1] && !mbar_wait_bounded(&full[slot], static_cast<uint32_t>(q / S) & 1u)) {
+                            set_err(A.err, MOE_ERR_TIMEOUT);
+                            vmisc[1] = 1;
+                        }
+                        const bool skip = vmisc[1] != 0;
+                        for (int c = cw; c < A.nch; c += cwc) {
+                            if (!skip && lane < RT) chunk_part<GT>(A, smem, tile, part, ne, c, lane, loff, tabA, slots);
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&cdone[slot]);
+                        }
+                    } else if (ewi < ew && k % ew == ewi) {
+                        if (!vmisc[1] && !mbar_wait_bounded(&cdone[slot], static_cast<uint32_t>(q / S) & 1u)) {
+                            set_err(A.err, MOE_ERR_TIMEOUT);
+                            vmisc[1] = 1;
+                        }
+                        const bool skip = vmisc[1] != 0;
+                        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        if (!skip && lane < RT)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (e < ne) {
+                                    float sv = part[e * RT + lane];
+                                    for (int cc = 1; cc < A.nch; ++cc)
+                                        sv = __fadd_rn(sv, part[(cc * kMaxEntriesPerPass + e) * RT + lane]);
+                                    v[e] = sv;
+                                }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[slot]);  // partials read: the slot is free
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (e >= ne) break;
+                            if (!skip && lane < RT) A.out[static_cast<int64_t>(gr.e0 + e) * gst + rowg] = v[e];
+                            const float uv = __shfl_down_sync(0xffffffffu, v[e], half);
+                            // this tile's h for j = h*half + lane (lane < half), moved to lane h*half + lane
+                            const float ht = __shfl_up_sync(0xffffffffu, swiglu_rn(v[e], uv), h * half);
+                            if (lane >= h * half && lane < (h + 1) * half) hv[e] = ht;
+                        }
+                        if (h == tpu - 1 && !skip) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (e < ne) warp_q8_1(hv[e], L.hq + static_cast<int64_t>(gr.e0 + e) * L.nbj + jb, lane);
+                            __syncwarp();
+                            if (lane == 0) {
+                                __threadfence();
+                                atomicAdd(L.sync + g, 1);
+                            }
+                        }
+                    }
+                } else {
+                    // more than 4 entries (or no spare warps): every consumer warp, 4-entry batches with
+                    // barriers; the last warp of a batch sums; h of the unit from the gate/up rows once
+                    // its last tile is done
                     for (int b0 = gr.e0; b0 < gr.e1; b0 += kMaxEntriesPerPass) {
-                        const int ne = gr.e1 - b0 < kMaxEntriesPerPass ? gr.e1 - b0 : kMaxEntriesPerPass;
+                        const int nb4 = gr.e1 - b0 < kMaxEntriesPerPass ? gr.e1 - b0 : kMaxEntriesPerPass;
                         const bool lastb = b0 + kMaxEntriesPerPass >= gr.e1;
                         if (b0 != gr.e0) named_sync(1, cnt);  // the previous batch's partials are summed
-                        if (!vmisc[1] &&
-                            !(wait_issued(vmisc, qq) && mbar_wait_bounded(&full[slot], static_cast<uint32_t>(qq / S) & 1u))) {
+                        if (!vmisc[1] && !mbar_wait_bounded(&full[slot], static_cast<uint32_t>(q / S) & 1u)) {
                             set_err(A.err, MOE_ERR_TIMEOUT);
                             vmisc[1] = 1;
                         }
                         const bool skip = vmisc[1] != 0;
                         int slots[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) slots[e] = entA[b0 + (e < ne ? e : ne - 1)].x;
+                        for (int e = 0; e < 4; ++e) slots[e] = entA[b0 + (e < nb4 ? e : nb4 - 1)].x;
                         for (int c = cw; c < A.nch; c += ncw) {
-                            if (!skip && lane < RT) chunk_part<GT>(A, smem, tile, part, ne, c, lane, loff, tabA, slots);
+                            if (!skip && lane < RT) chunk_part<GT>(A, smem, tile, part, nb4, c, lane, loff, tabA, slots);
                             __syncwarp();
                             __threadfence_block();
                             int last = 0;
@@ -536,163 +652,67 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                             last = __shfl_sync(0xffffffffu, last, 0);
                             if (!last) continue;
                             __threadfence_block();
-                            if (!skip)
-                                for (int e = 0; e < ne; ++e) {
-                                    float v = 0.0f;
-                                    if (lane < RT) {
-                                        v = part[e * RT + lane];
-                                        for (int cc = 1; cc < A.nch; ++cc)
-                                            v = __fadd_rn(v, part[(cc * kMaxEntriesPerPass + e) * RT + lane]);
-                                        A.out[static_cast<int64_t>(b0 + e) * gst + rowg] = v;
-                                    }
-                                    const float uv = __shfl_down_sync(0xffffffffu, v, half);
-                                    if (single && lane < half) ux[e * 32 + h * half + lane] = swiglu_rn(v, uv);
+                            if (!skip && lane < RT)
+                                for (int e = 0; e < nb4; ++e) {
+                                    float sv = part[e * RT + lane];
+                                    for (int cc = 1; cc < A.nch; ++cc)
+                                        sv = __fadd_rn(sv, part[(cc * kMaxEntriesPerPass + e) * RT + lane]);
+                                    A.out[static_cast<int64_t>(b0 + e) * gst + rowg] = sv;
                                 }
                             __syncwarp();
                             if (lane == 0) misc[64 + 8 * slot] = 0;
                             if (!lastb) continue;
+                            // the unit's last tile to finish computes h from its gate/up rows
                             int done = 0;
                             if (lane == 0) {
-                                __threadfence_block();
-                                done = atomicAdd(&misc[16 + ub], 1) == tpu - 1;
+                                __threadfence();
+                                done = atomicAdd(&misc[16 + (k & 7)], 1) == tpu - 1;
                             }
                             done = __shfl_sync(0xffffffffu, done, 0);
                             if (done) {
-                                // the unit's 32 h values per entry: from the unit buffer, or (groups of more
-                                // than 4 entries) from the gate/up rows written in this CTA
-                                if (single) __threadfence_block();
-                                else __threadfence();
-                                if (!skip)
-                                    for (int e = gr.e0; e < gr.e1; ++e) {
-                                        float hv;
-                                        if (single) {
-                                            hv = ux[(e - gr.e0) * 32 + lane];
-                                        } else {
-                                            const float* r = A.out + static_cast<int64_t>(e) * gst + 32 * jb + lane;
-                                            hv = swiglu_rn(__ldcg(r), __ldcg(r + F));
-                                        }
-                                        warp_q8_1(hv, L.hq + static_cast<int64_t>(e) * L.nbj + jb, lane);
-                                    }
+                                __threadfence();
+                                if (lane == 0) misc[16 + (k & 7)] = 0;
+                            }
+                            if (done && !skip) {
+                                for (int e = gr.e0; e < gr.e1; ++e) {
+                                    const float* r = A.out + static_cast<int64_t>(e) * gst + 32 * jb + lane;
+                                    warp_q8_1(swiglu_rn(__ldcg(r), __ldcg(r + F)), L.hq + static_cast<int64_t>(e) * L.nbj + jb,
+                                              lane);
+                                }
                                 __syncwarp();
                                 if (lane == 0) {
-                                    misc[16 + ub] = 0;
-                                    if (!skip) {
-                                        __threadfence();
-                                        atomicAdd(L.sync + g, 1);
-                                    }
+                                    __threadfence();
+                                    atomicAdd(L.sync + g, 1);
                                 }
                             }
-                            if (lane == 0) mbar_arrive(&empty[slot]);
+                            if (lane == 0) {
+                                // the slot's chunk-done barrier advances once per tile of any kind
+                                mbar_arrive_cnt(&cdone[slot], A.nch);
+                                mbar_arrive(&empty[slot]);
+                            }
                         }
                     }
                 }
-            }
-            qA = q;
-            }
-        }
-    }
-    {
-        // ---- down phase: this CTA's contiguous, cost-balanced run of (group, 8-row block) pairs in
-        // tiles of up to RT rows, through the same ring as the gate/up tiles (numbered after them),
-        // so they are prefetched into the slots the last gate/up tiles free
-        const int S = A.stages, RT = D.RT, rbpgD = D.rows >> 3, rt8 = RT >> 3;
-        const long long d0 = misc[10], d1 = misc[11];
-        if (warp == 0) {
-            if (lane == 0) {
-                int issued = vmisc[0];
-                long long cur = d0;
-                while (cur < d1) {
-                    const Tile t = next_tile(cur, d1, rbpgD, rt8);
-                    const GroupInfo gr = giD[t.g];
-                    if (gr.cost == 0) continue;
-                    const int s = issued % S;
-                    if (vmisc[1] || (issued >= S && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>(issued / S - 1) & 1u))) {
-                        if (!vmisc[1]) set_err(A.err, MOE_ERR_TIMEOUT);
-                        vmisc[1] = 1;
-                        break;
-                    }
-                    const uint32_t bytes = static_cast<uint32_t>(t.nrows) * static_cast<uint32_t>(D.row_bytes);
-                    mbar_arrive_expect_tx(&full[s], bytes);
-                    bulk_g2s(smem + A.off_ring + static_cast<size_t>(s) * A.stage_bytes,
-                             gr.ptr + static_cast<size_t>(t.row0) * D.row_bytes, bytes, &full[s]);
-                    ++issued;
-                    __threadfence_block();
-                    vmisc[0] = issued;
-                }
-            }
-        } else {
-            const int cw = warp - 1, ncw = (NT >> 5) - 1, ct = tid - 32, cnt = ncw * 32;
-            int gB0 = 0, gB1 = -1;
-            bool multi = false;
-            if (d0 < d1) {
-                gB0 = static_cast<int>(d0 / rbpgD);
-                gB1 = static_cast<int>((d1 - 1) / rbpgD);
-                for (int g = gB0; g <= gB1; ++g)
-                    multi |= giD[g].cost != 0 && giD[g].e1 - giD[g].e0 > kMaxEntriesPerPass;
-            }
-            // two: the range spans at most two groups of at most 4 entries, staged once (slots 0-3
-            // and 4-7); otherwise a group or batch change waits and restages slots 0-3
-            const bool two = d0 < d1 && !multi && gB1 - gB0 <= 1;
-            if (two) {
-                if (ct == 0)
-                    for (int g = gB0; g <= gB1; ++g)
-                        if (giD[g].cost && !vmisc[1] && !wait_count(ready + g, upg)) {
-                            set_err(A.err, MOE_ERR_TIMEOUT);
-                            vmisc[1] = 1;
-                        }
-                named_sync(1, cnt);
-                if (!vmisc[1]) {
-                    if (giD[gB0].cost)
-                        stage_entries<DT, true>(D, smem, entD, giD[gB0].e0, giD[gB0].e1 - giD[gB0].e0, 0, ct, cnt);
-                    if (gB1 != gB0 && giD[gB1].cost)
-                        stage_entries<DT, true>(D, smem, entD, giD[gB1].e0, giD[gB1].e1 - giD[gB1].e0,
-                                                kMaxEntriesPerPass, ct, cnt);
-                }
-                named_sync(1, cnt);
-            }
-            // work items (sub-tile, chunk) are numbered across this CTA's tiles and dealt to the
-            // consumer warps in turn; the last warp of a sub-tile sums its chunks
-            int q = qA, wbase = 0, cur_g = -1, cur_b0 = -1;
-            long long cur = d0;
-            while (cur < d1) {
-                const Tile t = next_tile(cur, d1, rbpgD, rt8);
-                const int g = t.g;
-                const GroupInfo gr = giD[g];
-                if (gr.cost == 0) continue;
-                const int nsb = (t.nrows + 31) >> 5, nbat = (gr.e1 - gr.e0 + kMaxEntriesPerPass - 1) / kMaxEntriesPerPass;
-                const int qq = q++, slot = qq % S;
-                const uint8_t* tile = smem + A.off_ring + static_cast<size_t>(slot) * A.stage_bytes;
-                float* part = reinterpret_cast<float*>(smem + A.off_part + static_cast<size_t>(slot) * A.part_bytes);
-                for (int b0 = gr.e0; b0 < gr.e1; b0 += kMaxEntriesPerPass) {
-                    const int ne = gr.e1 - b0 < kMaxEntriesPerPass ? gr.e1 - b0 : kMaxEntriesPerPass;
-                    if (!two && (g != cur_g || b0 != cur_b0)) {
-                        // a new group or batch: wait for its h rows, restage once every warp is done
-                        // with the previous ones
-                        if (ct == 0 && g != cur_g && !vmisc[1] && !wait_count(ready + g, upg)) {
-                            set_err(A.err, MOE_ERR_TIMEOUT);
-                            vmisc[1] = 1;
-                        }
-                        named_sync(1, cnt);
-                        if (!vmisc[1]) stage_entries<DT, true>(D, smem, entD, b0, ne, 0, ct, cnt);
-                        named_sync(1, cnt);
-                        cur_g = g;
-                        cur_b0 = b0;
-                    }
-                    const int s0 = two && g != gB0 ? kMaxEntriesPerPass : 0;
-                    const int nitems = nsb * D.nch;
-                    const int w0 = wbase + ((cw - wbase) % ncw + ncw) % ncw;
-                    wbase += nitems;
-                    if (w0 >= wbase) continue;  // no item of this tile for this warp
-                    if (!vmisc[1] &&
-                        !(wait_issued(vmisc, qq) && mbar_wait_bounded(&full[slot], static_cast<uint32_t>(qq / S) & 1u))) {
+            } else {
+                // ---- down tile: rows a0 .. a0+a1-1 of group g for entries e0 .. e0+ne-1, whose h
+                // rows the producer staged in slots s0 .. s0+ne-1
+                const int row0 = a0, nrows = a1, e0 = d4, ne = d5, s0 = d6;
+                const int nsb = (nrows + 31) >> 5;
+                // work items (sub-tile, chunk) numbered across the CTA's down tiles, dealt to the
+                // consumer warps in turn; the last warp of a sub-tile sums its chunks
+                const int nit = nsb * D.nch;
+                const int w0 = wbase + ((cw - wbase) % ncw + ncw) % ncw;
+                wbase += nit;
+                if (w0 < wbase) {
+                    if (!vmisc[1] && !mbar_wait_bounded(&full[slot], static_cast<uint32_t>(q / S) & 1u)) {
                         set_err(A.err, MOE_ERR_TIMEOUT);
                         vmisc[1] = 1;
                     }
                     const bool skip = vmisc[1] != 0;
                     const int slots[4] = {s0, s0 + (ne > 1 ? 1 : 0), s0 + (ne > 2 ? 2 : ne - 1), s0 + (ne > 3 ? 3 : ne - 1)};
                     for (int w = w0; w < wbase; w += ncw) {
-                        const int j = w - (wbase - nitems), sb = j / D.nch, c = j - sb * D.nch;
-                        const int nr = t.nrows - sb * 32 < 32 ? t.nrows - sb * 32 : 32;
+                        const int j = w - (wbase - nit), sb = j / D.nch, c = j - sb * D.nch;
+                        const int nr = nrows - sb * 32 < 32 ? nrows - sb * 32 : 32;
                         if (!skip && lane < nr)
                             chunk_part<DT>(D, smem, tile + static_cast<size_t>(sb) * 32 * D.row_bytes, part + sb * 32, ne, c,
                                            lane, 0, tabD, slots);
@@ -703,13 +723,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                         last = __shfl_sync(0xffffffffu, last, 0);
                         if (!last) continue;
                         __threadfence_block();
-                        if (!skip) reduce_write(D, part + sb * 32, entD, b0, Tile{g, t.row0 + sb * 32, nr}, ne, lane);
+                        if (!skip) reduce_write(D, part + sb * 32, entD, e0, Tile{g, row0 + sb * 32, nr}, ne, lane);
                         __syncwarp();
                         if (lane == 0) {
                             misc[64 + 8 * slot + sb] = 0;
                             __threadfence_block();
-                            if (atomicAdd(&misc[32 + slot], 1) == nsb * nbat - 1) {
+                            if (atomicAdd(&misc[32 + slot], 1) == nsb - 1) {
                                 misc[32 + slot] = 0;
+                                mbar_arrive_cnt(&cdone[slot], A.nch);  // once per tile of any kind
                                 mbar_arrive(&empty[slot]);
                             }
                         }
@@ -722,7 +743,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     // ---- after an abort: wait (bounded) for this CTA's copies still in flight
     __syncthreads();
     if (tid == 0 && vmisc[1]) {
-        const int nq = vmisc[0], S = A.stages;
+        const int nq = vmisc[6], S = A.stages;  // copies issued (published or not)
         for (int qq = nq - S > 0 ? nq - S : 0; qq < nq; ++qq)
             mbar_wait_bounded(&full[qq % S], static_cast<uint32_t>(qq / S) & 1u);
     }
@@ -734,7 +755,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     __syncthreads();
     if (misc[2]) {
         __threadfence();
-        for (int i = tid; i <= n; i += NT) L.sync[i] = 0;
+        for (int i = tid; i <= n + 1; i += NT) L.sync[i] = 0;
     }
 }
 

@@ -72,7 +72,7 @@ def test_layer_call_host_errors(m):
     L = m.lib()
     W = m.WFmt
     d = 16
-    assert m.layer_sync_ints(4, 8, 768) == 32 + 1
+    assert m.layer_sync_ints(4, 8, 768) == 32 + 2
     assert m.layer_sync_ints(0, 8, 768) == 0
 
     def call(**kw):
