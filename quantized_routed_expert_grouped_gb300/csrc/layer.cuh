@@ -359,8 +359,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     // lag behind the warps that release its slot). The producer warp also stages each down
     // group's q8_1 h rows (4-entry batches) into one of two buffers, so the consumer warps never
     // stop for a restage: a buffer is refilled once every tile that read it has been released.
-    const int S = A.stages, RT = A.RT, half = RT >> 1, RTD = D.RT;
-    const int tpg = (D.rows + RTD - 1) / RTD;
+    const int S = A.stages, RT = A.RT, half = RT >> 1;
+    const int RTD = D.RT, tpg = (D.rows + RTD - 1) / RTD;
     int dchunk = (G * tpg) / (2 * static_cast<int>(gridDim.x));  // about two down items per CTA
     dchunk = dchunk < 1 ? 1 : dchunk > 3 ? 3 : dchunk;
     const int nunits = G * upg, cpg = (tpg + dchunk - 1) / dchunk;
@@ -482,8 +482,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                             stop = true;
                             break;
                         }
-                        __syncwarp();
-                        __threadfence();  // lane 0's acquire of the counter covers every lane's loads
+                        (void)ld_acquire(ready + g);  // every lane acquires the counter lane 0 saw complete
                         stage_entries<DT, true>(D, smem, entD, b0, ne, kMaxEntriesPerPass * (st_n & 1), lane, 32);
                         __syncwarp();
                         st_g = g;
