@@ -250,6 +250,7 @@ void phase_warps(int nch, GemvArgs& a) {
 // Geometry and shared-memory layout of one fused layer launch. The ring slot holds a gate/up
 // tile (32 rows, or 16 when 32 rows exceed 96 KB) or a down tile of nsub x 32 rows.
 constexpr int kLayerPtrCache = 256;  // experts whose pointers are cached in shared memory
+constexpr int kUnitBytes = 4 * 4 * 32 * 4;  // gate/up unit buffers (4 units x 4 entries x 32 floats)
 constexpr int kLayerThreads = 512;   // producer warp + 15 consumer warps
 constexpr int kBatch = 4;            // entries staged per down batch
 
@@ -279,7 +280,7 @@ int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, 
     const int route = round_up(4 * (6 * n + 4), 128);
     const int cbb = cb_type(gt) ? 32768 : 0;
     const int ptrs = E <= kLayerPtrCache ? round_up(16 * E, 128) : 0;
-    const int fixed = cbb + act + 2 * grp + 2 * entb + route + ptrs + 512 + 1024;
+    const int fixed = cbb + act + 2 * grp + 2 * entb + route + ptrs + kUnitBytes + 512 + 1024;
     // one ring for both phases: a slot holds a gate/up tile (RT rows) or a down tile of nsub 32-row
     // sub-tiles; per stage a slot and its partial sums
     const int64_t tileA = A.RT * rbA;
@@ -298,6 +299,8 @@ int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, 
     off += S * stage;
     A.off_part = D.off_part = off;
     off += S * part;
+    L.off_unit = off;
+    off += kUnitBytes;
     A.off_actq = off;
     A.off_act2 = off + actqA;
     D.off_actq = off + actqA + act2A;
@@ -316,7 +319,7 @@ int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, 
     L.off_ptr = ptrs ? off : 0;
     off += ptrs;
     A.off_bar = D.off_bar = off;
-    off += 512;  // 3 x 8 ring mbarriers + 16 descriptor mbarriers
+    off += 512;  // 2 x 8 ring mbarriers, 2 x 16 descriptor mbarriers, 4 unit mbarriers
     A.off_misc = D.off_misc = off;
     off += 1024;
     A.stages = D.stages = S;

@@ -85,6 +85,7 @@ struct LayerArgs {
     int nsub;            // 32-row sub-tiles per down tile
     int upg, tpu;        // gate/up units (32 h values) per group, ring tiles per unit
     int off_route;       // shared-memory routing scratch
+    int off_unit;        // shared-memory gate/up unit buffers: [4 units][4 entries][32] h values
     int off_ptr;         // shared-memory cache of both expert pointer tables (0: not cached)
 };
 

@@ -48,6 +48,7 @@
 namespace moe {
 
 constexpr int kDescRing = 16;  // tile descriptors in flight per CTA (ring indices)
+constexpr int kUnitBufs = 4;   // gate/up units in flight per CTA (h buffers in shared memory)
 
 __device__ __forceinline__ int ld_acquire(const int32_t* p) {
     int v;
@@ -250,13 +251,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     const int SB = A.stages;  // ring slots
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + A.off_bar);
     uint64_t* empty = full + SB;
-    uint64_t* cdone = empty + SB;  // gate/up: a tile's chunk partials are written (one arrival per chunk)
-    uint64_t* dread = cdone + SB;  // descriptor d read by every consumer warp
-    // misc: [0] tiles published, [1] abort flag, [2] last-CTA flag, [5] no more tiles, [6] copies issued,
-    // [16 + u % 8] tiles done of gate/up unit u (barrier path), [32 + s] sub-tiles done of slot s,
-    // [64 + 8s + b] warps done with sub-tile b of slot s, [128 + 8d ..] descriptor d of ring index q
-    // (d = q % kDescRing)
+    uint64_t* dread = empty + SB;         // descriptor d passed by every consumer warp
+    uint64_t* ufree = dread + kDescRing;  // unit buffer u free again (its unit's h blocks written)
+    uint64_t* pub = ufree + kUnitBufs;    // descriptor d published (or the stream ended there)
+    // misc: [0] ring indices published, [1] abort flag, [2] last-CTA flag, [5] no more tiles,
+    // [6] copies issued, [7] work items published, [8] work items taken, [16 + u] tiles done of the
+    // gate/up unit in buffer u, [32 + s] sub-tiles done of slot s, [64 + 8s + b] chunks done of
+    // (sub-)tile b of slot s, [128 + 8d ..] descriptor d of ring index q (d = q % kDescRing)
     int* misc = reinterpret_cast<int*>(smem + A.off_misc);
+    // gate/up unit buffers: [kUnitBufs][4 entries][32] h values (the CTA's unit k uses k % kUnitBufs)
+    float* ubuf = reinterpret_cast<float*>(smem + L.off_unit);
     volatile int* vmisc = misc;
     GroupInfo* giA = reinterpret_cast<GroupInfo*>(smem + A.off_grp);
     GroupInfo* giD = reinterpret_cast<GroupInfo*>(smem + D.off_grp);
@@ -280,9 +284,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         for (int s = 0; s < SB; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&cdone[s], A.nch);
         }
         for (int d = 0; d < kDescRing; ++d) mbar_init(&dread[d], (NT >> 5) - 1);
+        for (int u = 0; u < kUnitBufs; ++u) mbar_init(&ufree[u], 1);
+        for (int d = 0; d < kDescRing; ++d) mbar_init(&pub[d], 1);
     }
     fence_barrier_init();
     // static data before the dependency wait: codebook replicas, NL4 tables, pointer tables
@@ -353,28 +358,31 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     const int32_t* ready = L.sync;  // per group: h blocks written (complete at F/32)
     // ---- one stream of work items for the whole grid, taken in order from a global counter:
     // gate/up units (group-major), then down chunks of dchunk tiles of one group (group-major).
-    // Each CTA's producer warp pulls items and streams their tiles through the ring, writing a
-    // descriptor per ring index; the consumers follow the ring. A descriptor is reused kDescRing
-    // indices later, once every consumer warp has read it (warps that take no part in a tile may
-    // lag behind the warps that release its slot). The producer warp also stages each down
-    // group's q8_1 h rows (4-entry batches) into one of two buffers, so the consumer warps never
-    // stop for a restage: a buffer is refilled once every tile that read it has been released.
-    const int S = A.stages, RT = A.RT, half = RT >> 1;
-    const int RTD = D.RT, tpg = (D.rows + RTD - 1) / RTD;
+    // Each CTA's producer warp pulls items and streams their tiles through the ring, publishing a
+    // descriptor per ring index (reused kDescRing indices later, once every consumer warp has
+    // passed it). The ring indices' work items (a gate/up tile's 256-weight chunks, a down tile's
+    // (sub-tile, chunk) pairs) are numbered in ring order and taken one at a time by whichever
+    // consumer warp is free (a shared counter), so a warp busy with an epilogue holds up nobody.
+    // The producer warp also stages each down group's q8_1 h rows (4-entry batches) into one of
+    // two buffers: a buffer is refilled once every tile that read it has been released.
+    const int S = A.stages, RT = A.RT, half = RT >> 1, RTD = D.RT;
+    const int tpg = (D.rows + RTD - 1) / RTD;
     int dchunk = (G * tpg) / (2 * static_cast<int>(gridDim.x));  // about two down items per CTA
     dchunk = dchunk < 1 ? 1 : dchunk > 3 ? 3 : dchunk;
     const int nunits = G * upg, cpg = (tpg + dchunk - 1) / dchunk;
     const int nitems = nunits + G * cpg;
     int* work = L.sync + n + 1;  // global item counter
     // per ring index q (d = q % kDescRing): [8d] kind (0 gate/up, 1 down), [8d+1] group,
-    // [8d+2] jb or first row, [8d+3] h or rows, down only: [8d+4] first entry, [8d+5] entries,
-    // [8d+6] first staging slot
+    // [8d+2] jb or first row, [8d+3] h or rows, [8d+4] first entry, [8d+5] entries (<= 4),
+    // [8d+6] gate/up: the CTA's unit number, down: first staging slot, [8d+7] first work item
     int* desc = misc + 128;
 
     if (warp == 0) {
         // lane 0 claims slots, issues the copies and publishes the ring indices; the whole warp
         // stages h rows
         int issued = 0;                          // ring indices published (lane 0)
+        int nwork = 0;                           // work items published (lane 0)
+        int ku = 0;                              // gate/up units (4-entry batches) issued (lane 0)
         int st_g = -1, st_b0 = -1, st_n = 0;     // staged group and batch, stagings so far
         int st_last = 0;                         // first ring index of the last staging (lane 0)
         bool stop = false;
@@ -388,9 +396,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
             }
             return true;
         };
-        // descriptor of ring index `issued` (once every consumer warp has read the one kDescRing
-        // indices earlier), then the index is published (lane 0)
-        auto publish = [&](int kind, int g, int a0, int a1, int e0, int ne, int s0) -> bool {
+        // descriptor of ring index `issued` (once every consumer warp has passed the one kDescRing
+        // indices earlier), then the index and its work items are published (lane 0)
+        auto publish = [&](int kind, int g, int a0, int a1, int e0, int ne, int a6, int items) -> bool {
             const int d = issued % kDescRing;
             if (issued >= kDescRing && !mbar_wait_bounded(&dread[d], static_cast<uint32_t>(issued / kDescRing - 1) & 1u)) {
                 if (!vmisc[1]) set_err(A.err, MOE_ERR_TIMEOUT);
@@ -404,10 +412,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
             dd[3] = a1;
             dd[4] = e0;
             dd[5] = ne;
-            dd[6] = s0;
+            dd[6] = a6;
+            dd[7] = nwork;
             ++issued;
+            nwork += items;
             __threadfence_block();
             vmisc[0] = issued;
+            vmisc[7] = nwork;
+            mbar_arrive(&pub[d]);
             return true;
         };
         // copy of ring index j's tile into its slot; vmisc[6]: copies issued (lane 0)
@@ -429,17 +441,31 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 const GroupInfo gr = giA[g];
                 if (gr.cost == 0) continue;
                 if (lane == 0)
-                    for (int h = 0; h < tpu; ++h) {
-                        if (!slot_free(issued)) {
+                    for (int b0 = gr.e0; b0 < gr.e1 && !stop; b0 += kMaxEntriesPerPass) {
+                        const int ne = gr.e1 - b0 < kMaxEntriesPerPass ? gr.e1 - b0 : kMaxEntriesPerPass;
+                        // unit buffer ku % kUnitBufs free: the unit kUnitBufs earlier has written its h
+                        // blocks
+                        if (vmisc[1] || (ku >= kUnitBufs &&
+                                         !mbar_wait_bounded(&ufree[ku % kUnitBufs],
+                                                            static_cast<uint32_t>(ku / kUnitBufs - 1) & 1u))) {
+                            if (!vmisc[1]) set_err(A.err, MOE_ERR_TIMEOUT);
+                            vmisc[1] = 1;
                             stop = true;
                             break;
                         }
-                        const size_t rg = static_cast<size_t>(32 * jb + h * half);
-                        copy_tile(issued, gr.ptr + rg * A.row_bytes, hb, gr.ptr + (rg + F) * A.row_bytes, hb);
-                        if (!publish(0, g, jb, h, 0, 0, 0)) {
-                            stop = true;
-                            break;
+                        for (int h = 0; h < tpu; ++h) {
+                            if (!slot_free(issued)) {
+                                stop = true;
+                                break;
+                            }
+                            const size_t rg = static_cast<size_t>(32 * jb + h * half);
+                            copy_tile(issued, gr.ptr + rg * A.row_bytes, hb, gr.ptr + (rg + F) * A.row_bytes, hb);
+                            if (!publish(0, g, jb, h, b0, ne, ku, A.nch)) {
+                                stop = true;
+                                break;
+                            }
                         }
+                        ++ku;
                     }
                 stop = __shfl_sync(0xffffffffu, stop, 0);
             } else {
@@ -447,6 +473,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 const GroupInfo gr = giD[g];
                 if (gr.cost == 0) continue;
                 const int t0 = c * dchunk, t1 = t0 + dchunk < tpg ? t0 + dchunk : tpg;
+                const int nbat = (gr.e1 - gr.e0 + kMaxEntriesPerPass - 1) / kMaxEntriesPerPass;
                 auto tile_src = [&](int t, uint32_t& bytes) {
                     const int row0 = t * RTD, nrows = D.rows - row0 < RTD ? D.rows - row0 : RTD;
                     bytes = static_cast<uint32_t>(nrows) * static_cast<uint32_t>(D.row_bytes);
@@ -465,11 +492,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                                 const uint8_t* src = tile_src(t, bytes);
                                 if (ok) copy_tile(issued + pre, src, bytes, nullptr, 0);
                             }
-                            // h rows of group g complete; buffer st_n & 1 free (from the third
-                            // staging on): every ring index before the last staging's first one
-                            // released (indices before issued - S are, as their slots were claimed
-                            // again)
-                            ok = ok && !vmisc[1] && wait_count(ready + g, upg);
+                            // h rows of group g complete (every 4-entry batch of every unit);
+                            // buffer st_n & 1 free (from the third staging on): every ring index
+                            // before the last staging's first one released (indices before
+                            // issued - S are, as their slots were claimed again)
+                            ok = ok && !vmisc[1] && wait_count(ready + g, upg * nbat);
                             if (st_n >= 2)
                                 for (int j = issued - S > 0 ? issued - S : 0; ok && j < st_last; ++j)
                                     ok = mbar_wait_bounded(&empty[j % S], static_cast<uint32_t>(j / S) & 1u);
@@ -502,7 +529,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                                 copy_tile(issued, src, bytes, nullptr, 0);
                             }
                             const int row0 = t * RTD, nrows = D.rows - row0 < RTD ? D.rows - row0 : RTD;
-                            if (!publish(1, g, row0, nrows, b0, ne, s0)) {
+                            if (!publish(1, g, row0, nrows, b0, ne, s0, ((nrows + 31) >> 5) * D.nch)) {
                                 stop = true;
                                 break;
                             }
@@ -511,228 +538,155 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 }
             }
         }
-        if (lane == 0) vmisc[5] = 1;  // no more tiles: the consumers stop at ring index vmisc[0]
+        if (lane == 0) {
+            // no more tiles: the stream ends at ring index vmisc[0]; the consumers waiting for that
+            // index are woken by an arrival without a descriptor, made (like a publish) once every
+            // consumer warp has passed the index kDescRing earlier
+            vmisc[5] = 1;
+            const int d = issued % kDescRing;
+            if (!vmisc[1] && issued >= kDescRing &&
+                !mbar_wait_bounded(&dread[d], static_cast<uint32_t>(issued / kDescRing - 1) & 1u)) {
+                set_err(A.err, MOE_ERR_TIMEOUT);
+                vmisc[1] = 1;
+            }
+            __threadfence_block();
+            mbar_arrive(&pub[d]);
+        }
     } else {
-        const int cw = warp - 1, ncw = (NT >> 5) - 1, ct = tid - 32, cnt = ncw * 32;
         const uint32_t loff = GT == MOE_CB3 ? lane * 4u : (lane & 15u) * 8u;
         const int64_t gst = A.out_stride;
-        const int cwc = A.nch < ncw ? A.nch : ncw;           // gate/up chunk warps
-        const int ew = ncw - cwc > 4 ? 4 : ncw - cwc;        // gate/up epilogue warps
-        const int ewi = cw - cwc;                            // epilogue warp index (>= 0)
-        int k = -1;                                          // gate/up units seen (the current one)
-        float hv[4] = {0.0f, 0.0f, 0.0f, 0.0f};             // epilogue: the unit's h values, one per lane
-        int wbase = 0;                                       // down: work items dealt so far
-        for (int q = 0;; ++q) {
-            // the next ring index: issued, or the end of the stream. Every warp walks the same ring
-            // indices to the producer's final count (after an abort too, skipping the work), so the
-            // named barriers inside the tiles always see every consumer warp.
-            {
-                const unsigned long long t0 = global_ns();
-                bool more = false;
-                for (uint32_t it = 0;; ++it) {
-                    if (vmisc[0] > q) {
-                        more = true;
+        // the ring index whose work items are [qb, qb + qn), its descriptor (qn < 0: not read yet)
+        int q = 0, qb = 0, qn = -1;
+        int kind = 0, g = 0, a0 = 0, a1 = 0, e0 = 0, ne = 0, a6 = 0;
+        for (;;) {
+            int it = 0;
+            if (lane == 0) it = atomicAdd(&misc[8], 1);
+            it = __shfl_sync(0xffffffffu, it, 0);
+            // wait until item `it` is published or the stream ends, passing (and releasing the
+            // descriptors of) the ring indices that end at or before it; a wait for a ring index is
+            // a blocking mbarrier wait
+            bool have = false;
+            for (;;) {
+                if (qn < 0) {
+                    if (!mbar_wait_bounded(&pub[q % kDescRing], static_cast<uint32_t>(q / kDescRing) & 1u)) {
+                        if (!vmisc[1]) set_err(A.err, MOE_ERR_TIMEOUT);
+                        vmisc[1] = 1;
                         break;
                     }
-                    if (vmisc[5]) {  // the producer is done: its final count was published before
-                        __threadfence_block();
-                        more = vmisc[0] > q;
-                        break;
-                    }
-                    __nanosleep(32);
-                    if ((it & 15u) == 15u) {
-                        // the producer stops at once after an abort, or within one bounded wait
-                        const unsigned long long dt = global_ns() - t0;
-                        if (dt > kWaitLimitNs && !vmisc[1]) {
-                            set_err(A.err, MOE_ERR_TIMEOUT);
-                            vmisc[1] = 1;
-                        }
-                        if (dt > 8 * kWaitLimitNs) break;  // last resort; not reached while the producer runs
-                    }
+                    if (vmisc[0] <= q) break;  // the end-of-stream arrival
+                    const int* dd = desc + 8 * (q % kDescRing);
+                    kind = dd[0];
+                    g = dd[1];
+                    a0 = dd[2];
+                    a1 = dd[3];
+                    e0 = dd[4];
+                    ne = dd[5];
+                    a6 = dd[6];
+                    qb = dd[7];
+                    qn = kind == 0 ? A.nch : ((a1 + 31) >> 5) * D.nch;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&dread[q % kDescRing]);
                 }
-                if (!more) break;
-                __threadfence_block();
+                if (it < qb + qn) {
+                    have = true;
+                    break;
+                }
+                ++q;
+                qn = -1;
             }
-            const int slot = q % S, dq = q % kDescRing;
-            const int* dd = desc + 8 * dq;
-            const int kind = dd[0], g = dd[1], a0 = dd[2], a1 = dd[3], d4 = dd[4], d5 = dd[5], d6 = dd[6];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&dread[dq]);
+            if (!have) break;
+            const int slot = q % S, j = it - qb;
             const uint8_t* tile = smem + A.off_ring + static_cast<size_t>(slot) * A.stage_bytes;
             float* part = reinterpret_cast<float*>(smem + A.off_part + static_cast<size_t>(slot) * A.part_bytes);
+            if (!vmisc[1] && !mbar_wait_bounded(&full[slot], static_cast<uint32_t>(q / S) & 1u)) {
+                set_err(A.err, MOE_ERR_TIMEOUT);
+                vmisc[1] = 1;
+            }
+            if (vmisc[1]) break;  // after an abort nothing more is computed (no barrier waits on this warp)
             if (kind == 0) {
-                // ---- gate/up tile h = a1 of unit (g, jb = a0)
-                const int jb = a0, h = a1;
-                const GroupInfo gr = giA[g];
-                const int ne = gr.e1 - gr.e0;
-                if (h == 0) {
-                    ++k;
-                    hv[0] = hv[1] = hv[2] = hv[3] = 0.0f;
+                // ---- chunk c = j of gate/up tile h = a1 of unit (g, jb = a0), entries e0 .. e0+ne-1
+                const int jb = a0, h = a1, c = j, u = a6 % kUnitBufs;
+                int slots[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) slots[e] = entA[e0 + (e < ne ? e : ne - 1)].x;
+                if (lane < RT) chunk_part<GT>(A, smem, tile, part, ne, c, lane, loff, tabA, slots);
+                __syncwarp();
+                __threadfence_block();
+                int last = 0;
+                if (lane == 0) last = atomicAdd(&misc[64 + 8 * slot], 1) == A.nch - 1;
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (!last) continue;
+                // the tile's last chunk: sum the partials (fixed chunk order), release the slot, write
+                // the gate/up rows and put SwiGLU(gate, up) (product rounded on its own) in the unit
+                // buffer
+                __threadfence_block();
+                float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                if (lane < RT)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (e < ne) {
+                            float sv = part[e * RT + lane];
+                            for (int cc = 1; cc < A.nch; ++cc)
+                                sv = __fadd_rn(sv, part[(cc * kMaxEntriesPerPass + e) * RT + lane]);
+                            v[e] = sv;
+                        }
+                __syncwarp();
+                if (lane == 0) {
+                    misc[64 + 8 * slot] = 0;
+                    mbar_arrive(&empty[slot]);  // partials read: the slot is free
                 }
-                // gate/up row of tile row `lane`
                 const int rowg = 32 * jb + h * half + (lane < half ? lane : lane - half + F);
-                if (ne <= kMaxEntriesPerPass && ew > 0) {
-                    // chunk warps compute and arrive on the slot's chunk-done barrier; epilogue warp k % ew
-                    // sums, releases the slot, writes the rows and keeps SwiGLU(gate, up) in its lanes
-                    int slots[4];
+                float* ub = ubuf + u * (kMaxEntriesPerPass * 32);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) slots[e] = entA[gr.e0 + (e < ne ? e : ne - 1)].x;
-                    if (cw < cwc) {
-                        if (!vmisc[1] && !mbar_wait_bounded(&full[slot], static_cast<uint32_t>(q / S) & 1u)) {
-                            set_err(A.err, MOE_ERR_TIMEOUT);
-                            vmisc[1] = 1;
-                        }
-                        const bool skip = vmisc[1] != 0;
-                        for (int c = cw; c < A.nch; c += cwc) {
-                            if (!skip && lane < RT) chunk_part<GT>(A, smem, tile, part, ne, c, lane, loff, tabA, slots);
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&cdone[slot]);
-                        }
-                    } else if (ewi < ew && k % ew == ewi) {
-                        if (!vmisc[1] && !mbar_wait_bounded(&cdone[slot], static_cast<uint32_t>(q / S) & 1u)) {
-                            set_err(A.err, MOE_ERR_TIMEOUT);
-                            vmisc[1] = 1;
-                        }
-                        const bool skip = vmisc[1] != 0;
-                        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                        if (!skip && lane < RT)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                if (e < ne) {
-                                    float sv = part[e * RT + lane];
-                                    for (int cc = 1; cc < A.nch; ++cc)
-                                        sv = __fadd_rn(sv, part[(cc * kMaxEntriesPerPass + e) * RT + lane]);
-                                    v[e] = sv;
-                                }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&empty[slot]);  // partials read: the slot is free
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            if (e >= ne) break;
-                            if (!skip && lane < RT) A.out[static_cast<int64_t>(gr.e0 + e) * gst + rowg] = v[e];
-                            const float uv = __shfl_down_sync(0xffffffffu, v[e], half);
-                            // this tile's h for j = h*half + lane (lane < half), moved to lane h*half + lane
-                            const float ht = __shfl_up_sync(0xffffffffu, swiglu_rn(v[e], uv), h * half);
-                            if (lane >= h * half && lane < (h + 1) * half) hv[e] = ht;
-                        }
-                        if (h == tpu - 1 && !skip) {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                if (e < ne) warp_q8_1(hv[e], L.hq + static_cast<int64_t>(gr.e0 + e) * L.nbj + jb, lane);
-                            __syncwarp();
-                            if (lane == 0) {
-                                __threadfence();
-                                atomicAdd(L.sync + g, 1);
-                            }
-                        }
-                    }
-                } else {
-                    // more than 4 entries (or no spare warps): every consumer warp, 4-entry batches with
-                    // barriers; the last warp of a batch sums; h of the unit from the gate/up rows once
-                    // its last tile is done
-                    for (int b0 = gr.e0; b0 < gr.e1; b0 += kMaxEntriesPerPass) {
-                        const int nb4 = gr.e1 - b0 < kMaxEntriesPerPass ? gr.e1 - b0 : kMaxEntriesPerPass;
-                        const bool lastb = b0 + kMaxEntriesPerPass >= gr.e1;
-                        if (b0 != gr.e0) named_sync(1, cnt);  // the previous batch's partials are summed
-                        if (!vmisc[1] && !mbar_wait_bounded(&full[slot], static_cast<uint32_t>(q / S) & 1u)) {
-                            set_err(A.err, MOE_ERR_TIMEOUT);
-                            vmisc[1] = 1;
-                        }
-                        const bool skip = vmisc[1] != 0;
-                        int slots[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) slots[e] = entA[b0 + (e < nb4 ? e : nb4 - 1)].x;
-                        for (int c = cw; c < A.nch; c += ncw) {
-                            if (!skip && lane < RT) chunk_part<GT>(A, smem, tile, part, nb4, c, lane, loff, tabA, slots);
-                            __syncwarp();
-                            __threadfence_block();
-                            int last = 0;
-                            if (lane == 0) last = atomicAdd(&misc[64 + 8 * slot], 1) == A.nch - 1;
-                            last = __shfl_sync(0xffffffffu, last, 0);
-                            if (!last) continue;
-                            __threadfence_block();
-                            if (!skip && lane < RT)
-                                for (int e = 0; e < nb4; ++e) {
-                                    float sv = part[e * RT + lane];
-                                    for (int cc = 1; cc < A.nch; ++cc)
-                                        sv = __fadd_rn(sv, part[(cc * kMaxEntriesPerPass + e) * RT + lane]);
-                                    A.out[static_cast<int64_t>(b0 + e) * gst + rowg] = sv;
-                                }
-                            __syncwarp();
-                            if (lane == 0) misc[64 + 8 * slot] = 0;
-                            if (!lastb) continue;
-                            // the unit's last tile to finish computes h from its gate/up rows
-                            int done = 0;
-                            if (lane == 0) {
-                                __threadfence();
-                                done = atomicAdd(&misc[16 + (k & 7)], 1) == tpu - 1;
-                            }
-                            done = __shfl_sync(0xffffffffu, done, 0);
-                            if (done) {
-                                __threadfence();
-                                if (lane == 0) misc[16 + (k & 7)] = 0;
-                            }
-                            if (done && !skip) {
-                                for (int e = gr.e0; e < gr.e1; ++e) {
-                                    const float* r = A.out + static_cast<int64_t>(e) * gst + 32 * jb + lane;
-                                    warp_q8_1(swiglu_rn(__ldcg(r), __ldcg(r + F)), L.hq + static_cast<int64_t>(e) * L.nbj + jb,
-                                              lane);
-                                }
-                                __syncwarp();
-                                if (lane == 0) {
-                                    __threadfence();
-                                    atomicAdd(L.sync + g, 1);
-                                }
-                            }
-                            if (lane == 0) {
-                                // the slot's chunk-done barrier advances once per tile of any kind
-                                mbar_arrive_cnt(&cdone[slot], A.nch);
-                                mbar_arrive(&empty[slot]);
-                            }
-                        }
-                    }
+                for (int e = 0; e < 4; ++e) {
+                    if (e >= ne) break;
+                    if (lane < RT) A.out[static_cast<int64_t>(e0 + e) * gst + rowg] = v[e];
+                    const float uv = __shfl_down_sync(0xffffffffu, v[e], half);
+                    if (lane < half) ub[e * 32 + h * half + lane] = swiglu_rn(v[e], uv);
+                }
+                __syncwarp();
+                __threadfence_block();
+                // the unit's last tile: q8_1 of its h blocks (one value per lane), the group's counter,
+                // the unit buffer free again
+                int done = 0;
+                if (lane == 0) done = atomicAdd(&misc[16 + u], 1) == tpu - 1;
+                done = __shfl_sync(0xffffffffu, done, 0);
+                if (!done) continue;
+                __threadfence_block();
+                for (int e = 0; e < ne; ++e)
+                    warp_q8_1(ub[e * 32 + lane], L.hq + static_cast<int64_t>(e0 + e) * L.nbj + jb, lane);
+                __syncwarp();
+                if (lane == 0) {
+                    misc[16 + u] = 0;
+                    __threadfence();
+                    atomicAdd(L.sync + g, 1);
+                    mbar_arrive(&ufree[u]);
                 }
             } else {
-                // ---- down tile: rows a0 .. a0+a1-1 of group g for entries e0 .. e0+ne-1, whose h
-                // rows the producer staged in slots s0 .. s0+ne-1
-                const int row0 = a0, nrows = a1, e0 = d4, ne = d5, s0 = d6;
-                const int nsb = (nrows + 31) >> 5;
-                // work items (sub-tile, chunk) numbered across the CTA's down tiles, dealt to the
-                // consumer warps in turn; the last warp of a sub-tile sums its chunks
-                const int nit = nsb * D.nch;
-                const int w0 = wbase + ((cw - wbase) % ncw + ncw) % ncw;
-                wbase += nit;
-                if (w0 < wbase) {
-                    if (!vmisc[1] && !mbar_wait_bounded(&full[slot], static_cast<uint32_t>(q / S) & 1u)) {
-                        set_err(A.err, MOE_ERR_TIMEOUT);
-                        vmisc[1] = 1;
-                    }
-                    const bool skip = vmisc[1] != 0;
-                    const int slots[4] = {s0, s0 + (ne > 1 ? 1 : 0), s0 + (ne > 2 ? 2 : ne - 1), s0 + (ne > 3 ? 3 : ne - 1)};
-                    for (int w = w0; w < wbase; w += ncw) {
-                        const int j = w - (wbase - nit), sb = j / D.nch, c = j - sb * D.nch;
-                        const int nr = nrows - sb * 32 < 32 ? nrows - sb * 32 : 32;
-                        if (!skip && lane < nr)
-                            chunk_part<DT>(D, smem, tile + static_cast<size_t>(sb) * 32 * D.row_bytes, part + sb * 32, ne, c,
-                                           lane, 0, tabD, slots);
-                        __syncwarp();
-                        __threadfence_block();
-                        int last = 0;
-                        if (lane == 0) last = atomicAdd(&misc[64 + 8 * slot + sb], 1) == D.nch - 1;
-                        last = __shfl_sync(0xffffffffu, last, 0);
-                        if (!last) continue;
-                        __threadfence_block();
-                        if (!skip) reduce_write(D, part + sb * 32, entD, e0, Tile{g, row0 + sb * 32, nr}, ne, lane);
-                        __syncwarp();
-                        if (lane == 0) {
-                            misc[64 + 8 * slot + sb] = 0;
-                            __threadfence_block();
-                            if (atomicAdd(&misc[32 + slot], 1) == nsb - 1) {
-                                misc[32 + slot] = 0;
-                                mbar_arrive_cnt(&cdone[slot], A.nch);  // once per tile of any kind
-                                mbar_arrive(&empty[slot]);
-                            }
-                        }
+                // ---- (sub-tile, chunk) item j of down tile rows a0 .. a0+a1-1 of group g for entries
+                // e0 .. e0+ne-1, whose h rows the producer staged in slots a6 .. a6+ne-1
+                const int row0 = a0, nrows = a1, s0 = a6;
+                const int nsb = (nrows + 31) >> 5, sb = j / D.nch, c = j - sb * D.nch;
+                const int nr = nrows - sb * 32 < 32 ? nrows - sb * 32 : 32;
+                const int slots[4] = {s0, s0 + (ne > 1 ? 1 : 0), s0 + (ne > 2 ? 2 : ne - 1), s0 + (ne > 3 ? 3 : ne - 1)};
+                if (lane < nr)
+                    chunk_part<DT>(D, smem, tile + static_cast<size_t>(sb) * 32 * D.row_bytes, part + sb * 32, ne, c, lane, 0,
+                                   tabD, slots);
+                __syncwarp();
+                __threadfence_block();
+                int last = 0;
+                if (lane == 0) last = atomicAdd(&misc[64 + 8 * slot + sb], 1) == D.nch - 1;
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (!last) continue;
+                __threadfence_block();
+                reduce_write(D, part + sb * 32, entD, e0, Tile{g, row0 + sb * 32, nr}, ne, lane);
+                __syncwarp();
+                if (lane == 0) {
+                    misc[64 + 8 * slot + sb] = 0;
+                    __threadfence_block();
+                    if (atomicAdd(&misc[32 + slot], 1) == nsb - 1) {
+                        misc[32 + slot] = 0;
+                        mbar_arrive(&empty[slot]);
                     }
                 }
             }
