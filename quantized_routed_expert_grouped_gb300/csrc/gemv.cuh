@@ -528,9 +528,11 @@ __device__ __forceinline__ void plain_block(const GemvArgs& a, const uint8_t* sm
     }
 }
 
-template <int TYPE, int NE, int j>
+// Sub-block j of a slot chunk (j may be a run-time index: the CB3X chunk loop is kept rolled two
+// sub-blocks at a time, which keeps the hot code small enough for the instruction caches).
+template <int TYPE, int NE>
 __device__ __forceinline__ void slot_block(const GemvArgs& a, const uint8_t* smem, const uint32_t* q, uint32_t subw,
-                                           int c, const int* slots, float acc[NE]) {
+                                           int c, int j, const int* slots, float acc[NE]) {
     uint32_t A[NE][8];
     float dx[NE], aux[NE];
     load_act<NE>(a, smem, c * 8 + j, slots, A, dx, aux);
@@ -564,23 +566,20 @@ __device__ __forceinline__ void slot_chunk(const GemvArgs& a, const uint8_t* sme
     const bool al16 = (a.row_bytes & 15) == 0;
     uint32_t q[4];
     if constexpr (TYPE == MOE_CB3X) {  // 16 bytes per sub-block
-        ld16(codes + 0, al16, q); slot_block<TYPE, NE, 0>(a, smem, q, sc.y, c, slots, acc);
-        ld16(codes + 16, al16, q); slot_block<TYPE, NE, 1>(a, smem, q, sc.y, c, slots, acc);
-        ld16(codes + 32, al16, q); slot_block<TYPE, NE, 2>(a, smem, q, sc.y, c, slots, acc);
-        ld16(codes + 48, al16, q); slot_block<TYPE, NE, 3>(a, smem, q, sc.y, c, slots, acc);
-        ld16(codes + 64, al16, q); slot_block<TYPE, NE, 4>(a, smem, q, sc.y, c, slots, acc);
-        ld16(codes + 80, al16, q); slot_block<TYPE, NE, 5>(a, smem, q, sc.y, c, slots, acc);
-        ld16(codes + 96, al16, q); slot_block<TYPE, NE, 6>(a, smem, q, sc.y, c, slots, acc);
-        ld16(codes + 112, al16, q); slot_block<TYPE, NE, 7>(a, smem, q, sc.y, c, slots, acc);
+#pragma unroll 2
+        for (int j = 0; j < 8; ++j) {
+            ld16(codes + 16 * j, al16, q);
+            slot_block<TYPE, NE>(a, smem, q, sc.y, c, j, slots, acc);
+        }
     } else {  // 8 bytes per sub-block: two sub-blocks per 16-byte load
-        ld16(codes + 0, al16, q); slot_block<TYPE, NE, 0>(a, smem, q, sc.y, c, slots, acc);
-        slot_block<TYPE, NE, 1>(a, smem, q + 2, sc.y, c, slots, acc);
-        ld16(codes + 16, al16, q); slot_block<TYPE, NE, 2>(a, smem, q, sc.y, c, slots, acc);
-        slot_block<TYPE, NE, 3>(a, smem, q + 2, sc.y, c, slots, acc);
-        ld16(codes + 32, al16, q); slot_block<TYPE, NE, 4>(a, smem, q, sc.y, c, slots, acc);
-        slot_block<TYPE, NE, 5>(a, smem, q + 2, sc.y, c, slots, acc);
-        ld16(codes + 48, al16, q); slot_block<TYPE, NE, 6>(a, smem, q, sc.y, c, slots, acc);
-        slot_block<TYPE, NE, 7>(a, smem, q + 2, sc.y, c, slots, acc);
+        ld16(codes + 0, al16, q); slot_block<TYPE, NE>(a, smem, q, sc.y, c, 0, slots, acc);
+        slot_block<TYPE, NE>(a, smem, q + 2, sc.y, c, 1, slots, acc);
+        ld16(codes + 16, al16, q); slot_block<TYPE, NE>(a, smem, q, sc.y, c, 2, slots, acc);
+        slot_block<TYPE, NE>(a, smem, q + 2, sc.y, c, 3, slots, acc);
+        ld16(codes + 32, al16, q); slot_block<TYPE, NE>(a, smem, q, sc.y, c, 4, slots, acc);
+        slot_block<TYPE, NE>(a, smem, q + 2, sc.y, c, 5, slots, acc);
+        ld16(codes + 48, al16, q); slot_block<TYPE, NE>(a, smem, q, sc.y, c, 6, slots, acc);
+        slot_block<TYPE, NE>(a, smem, q + 2, sc.y, c, 7, slots, acc);
     }
 #pragma unroll
     for (int e = 0; e < NE; ++e) acc[e] = __fmul_rn(D, acc[e]);
