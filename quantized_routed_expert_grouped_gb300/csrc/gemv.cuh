@@ -260,9 +260,9 @@ __device__ __forceinline__ void blk_decode_smem(const uint8_t* chunk, uint32_t W
     }
 }
 
-// Block j of an NL4 chunk held in registers (36 words, 16-byte aligned chunk).
+// Block j of a run of NL4 blocks held in registers (18 bytes each from a 4-byte aligned start).
 template <int j>
-__device__ __forceinline__ void nl4_decode(const uint32_t raw[36], const uint32_t tab[4], uint32_t W[8], float& d) {
+__device__ __forceinline__ void nl4_decode(const uint32_t* raw, const uint32_t tab[4], uint32_t W[8], float& d) {
     constexpr int L = 18 * j;
     constexpr int i = L >> 2;
     uint32_t qs[4];
@@ -510,6 +510,20 @@ __device__ __forceinline__ void cb_block(const GemvArgs& a, const uint8_t* smem,
     }
 }
 
+// Block j (0..3) of a 72-byte run of four NL4 blocks held in raw[18]; b: its block index in the row.
+template <int NE, int j>
+__device__ __forceinline__ void nl4_block(const GemvArgs& a, const uint8_t* smem, const uint32_t raw[18],
+                                          const uint32_t tab[4], int b, const int* slots, float acc[NE]) {
+    uint32_t A[NE][8];
+    float dx[NE], aux[NE];
+    load_act<NE>(a, smem, b, slots, A, dx, aux);
+    uint32_t W[8];
+    float dw;
+    nl4_decode<j>(raw, tab, W, dw);
+#pragma unroll
+    for (int e = 0; e < NE; ++e) acc[e] = fmaf(__fmul_rn(dw, dx[e]), static_cast<float>(dot8(W, A[e])), acc[e]);
+}
+
 template <int TYPE, int NE, int j>
 __device__ __forceinline__ void plain_block(const GemvArgs& a, const uint8_t* smem, const uint8_t* chunk,
                                             const uint32_t* raw, const uint32_t tab[4], int c, const int* slots,
@@ -607,15 +621,25 @@ __device__ __forceinline__ void lane_chunk(const GemvArgs& a, const uint8_t* sme
         cb_block<TYPE, NE, 7>(a, smem, rr, c, loff, slots, acc);
 #pragma unroll
         for (int e = 0; e < NE; ++e) acc[e] = __fmul_rn(D, acc[e]);
-    } else {
-        uint32_t raw[TYPE == MOE_NL4 ? 36 : 1];
-        if constexpr (TYPE == MOE_NL4) {
+    } else if constexpr (TYPE == MOE_NL4) {
+        // two rounds of four 18-byte blocks (72 bytes, 8-byte aligned), the loop kept rolled so the
+        // hot code stays small enough for the instruction caches
+#pragma unroll 1
+        for (int p = 0; p < 2; ++p) {
+            uint32_t raw[18];
 #pragma unroll
             for (int k = 0; k < 9; ++k) {
-                const uint4 v = *reinterpret_cast<const uint4*>(chunk + 16 * k);
-                raw[4 * k] = v.x; raw[4 * k + 1] = v.y; raw[4 * k + 2] = v.z; raw[4 * k + 3] = v.w;
+                const uint2 v = *reinterpret_cast<const uint2*>(chunk + 72 * p + 8 * k);
+                raw[2 * k] = v.x;
+                raw[2 * k + 1] = v.y;
             }
+            nl4_block<NE, 0>(a, smem, raw, tab, c * 8 + 4 * p, slots, acc);
+            nl4_block<NE, 1>(a, smem, raw, tab, c * 8 + 4 * p + 1, slots, acc);
+            nl4_block<NE, 2>(a, smem, raw, tab, c * 8 + 4 * p + 2, slots, acc);
+            nl4_block<NE, 3>(a, smem, raw, tab, c * 8 + 4 * p + 3, slots, acc);
         }
+    } else {
+        const uint32_t raw[1] = {0};
         plain_block<TYPE, NE, 0>(a, smem, chunk, raw, tab, c, slots, acc);
         plain_block<TYPE, NE, 1>(a, smem, chunk, raw, tab, c, slots, acc);
         plain_block<TYPE, NE, 2>(a, smem, chunk, raw, tab, c, slots, acc);
