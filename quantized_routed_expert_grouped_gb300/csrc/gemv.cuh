@@ -31,8 +31,9 @@
 //    per-block code sum is taken once when the activation row is staged. A sign nibble becomes a
 //    byte mask by one 32x32->64 multiply (bits to byte msbs) and one sign-replicating permute.
 //  * NL4 codes are looked up in the 16-entry table held in four registers with byte permutes
-//    (two 8-entry halves and a per-byte select on the code's top bit); the staged activation
-//    words are permuted to the permute's byte order.
+//    taking the codes' nibbles as selectors in place (two 8-entry halves and a per-byte select
+//    on the code's top bit, 11 instructions per 8 weights); the staged activation words are
+//    permuted once to the resulting nibble order.
 //  * No tensor cores: at 1-4 entries per group this is a batched GEMV, bound by HBM bandwidth
 //    and by the integer decode.
 #pragma once
@@ -209,21 +210,32 @@ __device__ __forceinline__ int cb_decode(const CBRow<TYPE>& row, const uint8_t* 
     return ls;
 }
 
-// NL4: the four 4-bit codes of one byte lane set -> table values, bytes in the order [0, 2, 1, 3].
-// sel: 3-bit codes as a permute selector; msk: 0xFF bytes where the code is >= 8.
-__device__ __forceinline__ uint32_t nl4_lookup(const uint32_t tab[4], uint32_t sel, uint32_t msk) {
-    const uint32_t lo = prmt(tab[0], tab[1], sel), hi = prmt(tab[2], tab[3], sel);
-    return (lo & ~msk) | (hi & msk);
+// NL4: one 4-byte code word Q (bytes 4k..4k+3 of a block's codes: low nibbles codes 4k..4k+3,
+// high nibbles codes 16+4k..19+4k) -> two weight words in nibble order, wa = weights (4k, 16+4k,
+// 4k+1, 17+4k) and wb = (4k+2, 18+4k, 4k+3, 19+4k); the staged activation words are permuted to
+// match (nl4_act_perm). Each code's low three bits, as byte-permute selectors (a permute reads
+// only the low four nibbles of its selector), pick from the table's two 8-entry halves held in
+// registers; a sign-replicating permute spreads each code's top bit over its byte, and that mask
+// chooses the half. 11 instructions per 8 weights.
+__device__ __forceinline__ void nl4_word(const uint32_t tab[4], uint32_t Q, uint32_t& wa, uint32_t& wb) {
+    const uint32_t s = Q & 0x77777777u, sb = s >> 16, q4 = Q << 4;
+    // top bit of nibble i: Q bit 4i+3 = msb of byte i/2 of (Q << 4) for even i, of Q for odd i
+    const uint32_t ma = prmt(q4, Q, 0xD9C8u), mb = prmt(q4, Q, 0xFBEAu);
+    const uint32_t la = prmt(tab[0], tab[1], s), ha = prmt(tab[2], tab[3], s);
+    const uint32_t lb = prmt(tab[0], tab[1], sb), hb = prmt(tab[2], tab[3], sb);
+    wa = (la & ~ma) | (ha & ma);
+    wb = (lb & ~mb) | (hb & mb);
 }
 
-// One 16-byte NL4 code word Q (codes of weights 4k..4k+3 in the low nibbles, 16+4k.. in the high)
-// -> two weight words (byte order [0, 2, 1, 3], matching the staged activations).
-__device__ __forceinline__ void nl4_word(const uint32_t tab[4], uint32_t Q, uint32_t& wlo, uint32_t& whi) {
-    const uint32_t s = Q & 0x77777777u;
-    const uint32_t sl = (s & 0x0f0fu) | ((s >> 12) & 0xf0f0u);
-    const uint32_t sh = ((s >> 4) & 0x0f0fu) | ((s >> 16) & 0xf0f0u);
-    wlo = nl4_lookup(tab, sl, prmt(Q << 4, 0u, 0xB9A8u));
-    whi = nl4_lookup(tab, sh, prmt(Q, 0u, 0xB9A8u));
+// The 8 code words x[0..7] of a q8_1 block in the order nl4_word produces the weights:
+// staged word 2k = bytes (x[k].0, x[4+k].0, x[k].1, x[4+k].1), word 2k+1 = (x[k].2, x[4+k].2,
+// x[k].3, x[4+k].3).
+__device__ __forceinline__ void nl4_act_perm(const uint32_t x[8], uint32_t p[8]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        p[2 * k] = prmt(x[k], x[4 + k], 0x5140u);
+        p[2 * k + 1] = prmt(x[k], x[4 + k], 0x7362u);
+    }
 }
 
 // Block j (32 weights) of a Q8_0 / Q4B chunk in shared memory: 8 weight words matching the
@@ -276,7 +288,7 @@ __device__ __forceinline__ void nl4_decode(const uint32_t* raw, const uint32_t t
         for (int k = 0; k < 4; ++k) qs[k] = raw[i + 1 + k];
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) nl4_word(tab, qs[k], W[k], W[4 + k]);
+    for (int k = 0; k < 4; ++k) nl4_word(tab, qs[k], W[2 * k], W[2 * k + 1]);
 }
 
 // Sub-block j (32 weights) of a slot chunk: codes -> 8 words of biased values u (one code per
@@ -402,8 +414,10 @@ __device__ __forceinline__ void stage_block(const GemvArgs& a, uint8_t* smem, in
         for (int k = 0; k < 9; ++k) w[k] = 0;
     }
     if constexpr (TYPE == MOE_NL4) {
+        uint32_t p[8];
+        nl4_act_perm(w + 1, p);
 #pragma unroll
-        for (int k = 1; k < 9; ++k) w[k] = prmt(w[k], 0u, 0x3120u);
+        for (int k = 0; k < 8; ++k) w[1 + k] = p[k];
     }
     q[(slot * 2 + 0) * a.nbp + bp] = make_int4(w[1], w[2], w[3], w[4]);
     q[(slot * 2 + 1) * a.nbp + bp] = make_int4(w[5], w[6], w[7], w[8]);
@@ -419,29 +433,6 @@ __device__ __forceinline__ void stage_block(const GemvArgs& a, uint8_t* smem, in
         aux = h2f_bits(w[0] >> 16);
     }
     q2[slot * a.nb + b] = make_float2(h2f_bits(w[0]), aux);
-}
-
-// One q8_1 block held by one thread (code words w[0..7], header hdr = d16 | s16 << 16, exact code
-// sum S) into slot `slot`, block b, in the layout stage_block writes.
-template <int TYPE>
-__device__ __forceinline__ void stage_words(const GemvArgs& a, uint8_t* smem, int slot, int b, const uint32_t w[8],
-                                            uint32_t hdr, int S) {
-    uint32_t c[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) c[k] = TYPE == MOE_NL4 ? prmt(w[k], 0u, 0x3120u) : w[k];
-    int4* q = reinterpret_cast<int4*>(smem + a.off_actq);
-    const int bp = b + (b >> 3);
-    q[(slot * 2 + 0) * a.nbp + bp] = make_int4(c[0], c[1], c[2], c[3]);
-    q[(slot * 2 + 1) * a.nbp + bp] = make_int4(c[4], c[5], c[6], c[7]);
-    float aux = 0.0f;
-    if constexpr (Fmt<TYPE>::SLOT) {
-        aux = __int_as_float(S * -(2 * Fmt<TYPE>::BIAS - 1));
-    } else if constexpr (Fmt<TYPE>::CB) {
-        aux = __int_as_float(S);
-    } else if constexpr (TYPE == MOE_Q4B) {
-        aux = h2f_bits(hdr >> 16);
-    }
-    reinterpret_cast<float2*>(smem + a.off_act2)[slot * a.nb + b] = make_float2(h2f_bits(hdr), aux);
 }
 
 // All n rows of the activation matrix into slots 0..n-1.

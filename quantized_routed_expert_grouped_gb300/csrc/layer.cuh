@@ -99,14 +99,19 @@ __device__ __forceinline__ void quad_q8_1(const float v[8], unsigned qmask, uint
 }
 
 // Quad lane j's part of a q8_1 block into staged slot `slot`, block b (the layout stage_block
-// writes): code words 2j, 2j+1; lane 0 also the (d, aux) pair.
+// writes): staged words 2j, 2j+1; lane 0 also the (d, aux) pair. qmask: the quad's lanes.
 template <int TYPE>
 __device__ __forceinline__ void stage_quad(const GemvArgs& a, uint8_t* smem, int slot, int b, int j, const uint32_t w[2],
-                                           uint32_t hdr, int S) {
+                                           uint32_t hdr, int S, unsigned qmask) {
     uint32_t c0 = w[0], c1 = w[1];
     if constexpr (TYPE == MOE_NL4) {
-        c0 = prmt(c0, 0u, 0x3120u);
-        c1 = prmt(c1, 0u, 0x3120u);
+        // staged words 2j, 2j+1 interleave code words j and 4+j (nl4_act_perm); code word i is
+        // element i & 1 of quad lane i >> 1
+        const uint32_t a0 = __shfl_sync(qmask, w[0], j >> 1, 4), a1 = __shfl_sync(qmask, w[1], j >> 1, 4);
+        const uint32_t b0 = __shfl_sync(qmask, w[0], 2 + (j >> 1), 4), b1 = __shfl_sync(qmask, w[1], 2 + (j >> 1), 4);
+        const uint32_t xa = (j & 1) ? a1 : a0, xb = (j & 1) ? b1 : b0;
+        c0 = prmt(xa, xb, 0x5140u);
+        c1 = prmt(xa, xb, 0x7362u);
     }
     const int bp = b + (b >> 3);
     *reinterpret_cast<uint2*>(smem + a.off_actq + ((slot * 2 + (j >> 1)) * a.nbp + bp) * 16 + (j & 1) * 8) =
@@ -347,7 +352,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                     uint32_t w[2], hdr;
                     int Ssum;
                     quad_q8_1(v, qmask, w, hdr, Ssum);
-                    stage_quad<GT>(A, smem, t, b, j, w, hdr, Ssum);
+                    stage_quad<GT>(A, smem, t, b, j, w, hdr, Ssum, qmask);
                     if (blockIdx.x == 0 && L.o_xq) put_quad(L.o_xq + i, j, w, hdr);
                 }
             }
