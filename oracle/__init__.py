@@ -19,9 +19,8 @@ _BUILD = os.path.join(_HERE, "_build")
 _LOCK = threading.Lock()
 _LIBS: dict = {}
 
-Q8_0, Q4B, NL4, CB2, CB3, CB3X, CB2X, NL4K, Q8_0K = 1, 2, 3, 4, 5, 6, 7, 8, 9
-TYPE_NAMES = {"Q8_0": Q8_0, "Q4B": Q4B, "NL4": NL4, "CB2": CB2, "CB3": CB3, "CB3X": CB3X, "CB2X": CB2X,
-              "NL4K": NL4K, "Q8_0K": Q8_0K}
+Q8_0, Q4B, NL4, CB2, CB3, CB3X, CB2X = 1, 2, 3, 4, 5, 6, 7
+TYPE_NAMES = {"Q8_0": Q8_0, "Q4B": Q4B, "NL4": NL4, "CB2": CB2, "CB3": CB3, "CB3X": CB3X, "CB2X": CB2X}
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -69,8 +68,6 @@ def _setup(lib):
     lib.orc_swiglu_q8_1.argtypes = [_P, _I, _I, _I, _P]
     lib.orc_transcode_row.argtypes = [_I, _P, _I, _P, _I, _P]
     lib.orc_transcode_row.restype = _I
-    lib.orc_slice_blob.argtypes = [_I, _P, _I, _I, _P]
-    lib.orc_slice_blob.restype = _I
     lib.orc_route_group.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P]
     lib.orc_route_group.restype = _I
     return lib
@@ -172,13 +169,6 @@ class Oracle:
             out[r * rb_d:(r + 1) * rb_d] = o
             bad |= rc
         return out, bad
-
-    def slice_blob(self, dst_type, blob, rows, K):
-        """K-sliced re-layout of one NL4 / Q8_0 down blob (rows x K weights); (bytes, rc)."""
-        blob = np.ascontiguousarray(blob, dtype=np.uint8)
-        out = np.zeros(blob.size, dtype=np.uint8)
-        rc = self.lib.orc_slice_blob(dst_type, _ptr(blob), rows, K, _ptr(out))
-        return out, rc
 
     # ---- grouped steps
     def grouped_gemv(self, typ, K, rows, blobs, grp_expert, grp_start, n_groups, act,

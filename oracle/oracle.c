@@ -159,8 +159,6 @@ int64_t orc_row_bytes(int type, int K) {
     case ORC_CB3: return K % 256 ? 0 : (int64_t)(K / 256) * 102;
     case ORC_CB3X: return K % 256 ? 0 : (int64_t)(K / 256) * (128 + 8);
     case ORC_CB2X: return K % 256 ? 0 : (int64_t)(K / 256) * (64 + 8);
-    case ORC_NL4K: return (int64_t)(K / 32) * 18;  /* bytes per row in aggregate (K-sliced) */
-    case ORC_Q8_0K: return (int64_t)(K / 32) * 34;
     }
     return 0;
 }
@@ -362,40 +360,6 @@ int orc_transcode_row(int src_type, const uint8_t* src, int K, const int8_t* cb,
 }
 
 /* ------------------------------------------------------------------ grouped steps */
-
-/* K-sliced down layouts: every block of every row is copied once, unchanged, to its record
- * position; no arithmetic. */
-int orc_slice_blob(int dst_type, const uint8_t* src, int rows, int K, uint8_t* dst) {
-    int nb = K / 32, bsz, rec;
-    if (rows <= 0 || rows % 32 || K <= 0 || K % 32) return -1;
-    if (dst_type == ORC_NL4K) { bsz = 18; rec = 576; }
-    else if (dst_type == ORC_Q8_0K) { bsz = 34; rec = 1088; }
-    else return -1;
-    for (int n = 0; n < rows; ++n) {
-        for (int j = 0; j < nb; ++j) {
-            const uint8_t* b = src + ((int64_t)n * nb + j) * bsz; /* native: scale, then codes */
-#ifdef ORC_PLANT_SLICE_ORDER
-            uint8_t* r = dst + ((int64_t)(n / 32) * nb + j) * rec;
-#else
-            uint8_t* r = dst + ((int64_t)j * (rows / 32) + n / 32) * rec;
-#endif
-            int i = n % 32;
-            if (dst_type == ORC_NL4K) {
-                memcpy(r + 16 * i, b + 2, 16);
-#ifdef ORC_PLANT_SLICE_SCALE
-                memcpy(r + 512 + 2 * i, b + 16, 2);
-#else
-                memcpy(r + 512 + 2 * i, b, 2);
-#endif
-            } else {
-                memcpy(r + 16 * i, b + 2, 16);
-                memcpy(r + 512 + 16 * i, b + 18, 16);
-                memcpy(r + 1024 + 2 * i, b, 2);
-            }
-        }
-    }
-    return 0;
-}
 
 int orc_grouped_gemv(int type, const int8_t* cb, int K, int rows, const uint8_t* const* w,
                      int n_experts, const int32_t* grp_expert, const int32_t* grp_start,

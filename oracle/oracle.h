@@ -33,14 +33,6 @@
  *   CB2X:  64 B of 2-bit codes per 256 weights, bias 2 (|v| <= 3). In sub-block j (8 bytes):
  *         bits 2p..2p+1 of byte i = weight 8p + i.
  * Rows of the native formats are K/32 blocks (K/256 super-blocks) packed without padding.
- * K-sliced down layouts (load-time re-layouts of NL4 / Q8_0 blobs, the same blocks moved):
- * the blob of `rows` rows (rows % 32 == 0) x K weights is K/32 slices, slice j holding block j
- * of every row; a slice is rows/32 records, record r holding rows 32r .. 32r+31:
- *   NL4K  (576 B records):  bytes 16i..16i+15 = the 16 code bytes of row 32r+i's block j,
- *                           bytes 512+2i, 513+2i = its fp16 scale.
- *   Q8_0K (1088 B records): bytes 16i..16i+15 = codes 0..15 of row 32r+i's block j,
- *                           bytes 512+16i..512+16i+15 = codes 16..31, bytes 1024+2i.. = scale.
- *   Record (j, r) starts at byte (j*rows/32 + r) * record size; blob size = that of the source.
  */
 #ifndef MOE_ORACLE_H
 #define MOE_ORACLE_H
@@ -50,8 +42,7 @@
 extern "C" {
 #endif
 
-enum { ORC_Q8_0 = 1, ORC_Q4B = 2, ORC_NL4 = 3, ORC_CB2 = 4, ORC_CB3 = 5, ORC_CB3X = 6, ORC_CB2X = 7,
-       ORC_NL4K = 8, ORC_Q8_0K = 9 };
+enum { ORC_Q8_0 = 1, ORC_Q4B = 2, ORC_NL4 = 3, ORC_CB2 = 4, ORC_CB3 = 5, ORC_CB3X = 6, ORC_CB2X = 7 };
 
 /* IEEE binary16 <-> binary32, round to nearest even (subnormals kept). */
 float orc_h2f(uint16_t h);
@@ -71,10 +62,6 @@ void orc_quantize_q8_1(const float* x, int64_t n, uint8_t* out);
 /* Transcode one row of CB2/CB3 (src_type) into the slot layout dst_type (CB3X or CB2X).
  * Returns 0, or -1 when a value does not fit the slot's code range (row left unspecified). */
 int orc_transcode_row(int src_type, const uint8_t* src, int K, const int8_t* cb, int dst_type, uint8_t* dst);
-
-/* Re-lay one down blob (rows x K weights) of NL4 (dst_type ORC_NL4K) or Q8_0 (ORC_Q8_0K) into
- * its K-sliced layout. Returns 0, or -1 for an unsupported type or rows % 32 != 0. */
-int orc_slice_blob(int dst_type, const uint8_t* src, int rows, int K, uint8_t* dst);
 
 /* Dequantize one row to fp64 (w[K]); cb is the codebook (CB2 256x8, CB3 256x4, NL4 16). */
 void orc_dequant_row(int type, const uint8_t* row, int K, const int8_t* cb, double* w);

@@ -14,8 +14,6 @@ What pins what:
   formats       -> hand-built blocks with hand-worked weights (every field, nibble order, sign
                    bit order, sub-scale nibble and 2*sub+1), one-hot activations that read out
                    one column, and brute-force fp64 dot products of dequantized operands
-  K-sliced down -> hand-worked byte positions of a tagged blob, and a byte permutation (every
-                   source byte lands exactly once)
   grouping      -> a hand-worked routing example and invariants on random routings
   grouped steps -> permutation invariants and untouched rows
 """
@@ -23,7 +21,7 @@ from __future__ import annotations
 
 import numpy as np
 
-Q8_0, Q4B, NL4, CB2, CB3, CB3X, CB2X, NL4K, Q8_0K = 1, 2, 3, 4, 5, 6, 7, 8, 9
+Q8_0, Q4B, NL4, CB2, CB3, CB3X, CB2X = 1, 2, 3, 4, 5, 6, 7
 
 
 def _h(v):
@@ -319,42 +317,6 @@ def check_slots(o):
     assert o.transcode_row(CB2, sb, 256, np.full((256, 8), 5, np.int8), CB2X)[1] == -1
 
 
-# ------------------------------------------------------------------ K-sliced down layouts
-
-def check_slices(o):
-    """The K-sliced down layouts move every block unchanged to the documented record position:
-    hand-worked offsets of tagged blocks, and every source byte lands exactly once."""
-    rows, K = 96, 64  # 3 row groups x 2 blocks
-    for typ, dst, bsz, rec in ((NL4, NL4K, 18, 576), (Q8_0, Q8_0K, 34, 1088)):
-        src = np.zeros(rows * 2 * bsz, np.uint8)
-        # row 33, block 1 (native offset (33*2 + 1) * bsz): scale bytes 0xA1 0xA2, codes 1, 2, ...
-        b = (33 * 2 + 1) * bsz
-        src[b:b + 2] = [0xA1, 0xA2]
-        src[b + 2:b + bsz] = np.arange(1, bsz - 1)
-        t, rc = o.slice_blob(dst, src, rows, K)
-        assert rc == 0 and t.size == src.size
-        # record (j = 1, r = 1) is record 1 * 3 + 1 = 4; row 33 is i = 1 in it
-        if dst == NL4K:  # record at 2304: codes at 2320..2335, scale at 2818, 2819
-            assert list(t[2320:2336]) == list(range(1, 17))
-            assert list(t[2818:2820]) == [0xA1, 0xA2]
-        else:  # record at 4352: codes 0..15 at 4368.., codes 16..31 at 4880.., scale at 5378, 5379
-            assert list(t[4368:4384]) == list(range(1, 17))
-            assert list(t[4880:4896]) == list(range(17, 33))
-            assert list(t[5378:5380]) == [0xA1, 0xA2]
-        assert int(np.count_nonzero(t)) == bsz  # nothing else written
-        # permutation: tag every byte position with its own index (mod prime sizes) in 3 planes
-        idx = np.arange(src.size)
-        got = []
-        for plane in (idx % 251, (idx // 251) % 251, idx // (251 * 251)):
-            t, rc = o.slice_blob(dst, plane.astype(np.uint8), rows, K)
-            assert rc == 0
-            got.append(t.astype(np.int64))
-        back = got[0] + 251 * got[1] + 251 * 251 * got[2]
-        assert np.array_equal(np.sort(back), idx)
-    assert o.slice_blob(NL4K, np.zeros(48 * 36, np.uint8), 48, 64)[1] == -1  # rows % 32 != 0
-    assert o.slice_blob(CB3X, np.zeros(64 * 36, np.uint8), 64, 64)[1] == -1
-
-
 # ------------------------------------------------------------------ grouping
 
 def check_route_hand(o):
@@ -451,5 +413,5 @@ def check_swiglu_q8_1(o):
 
 
 ALL_CHECKS = [check_f16, check_exp, check_silu, check_q8_1, check_formats_hand, check_formats_onehot,
-              check_formats_bruteforce, check_slots, check_slices, check_route_hand, check_route_invariants, check_grouped_invariants,
+              check_formats_bruteforce, check_slots, check_route_hand, check_route_invariants, check_grouped_invariants,
               check_swiglu_q8_1]

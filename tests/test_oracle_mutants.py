@@ -17,8 +17,6 @@ PLANTS = {
     "ORC_PLANT_ROUTE_ORDER": "entries of a group ordered by slot first",
     "ORC_PLANT_ENTRY_ROW": "gate/up reads the entry index instead of its token row",
     "ORC_PLANT_SLOT_ORDER": "4-bit slot codes read interleaved",
-    "ORC_PLANT_SLICE_ORDER": "K-sliced records ordered row group first",
-    "ORC_PLANT_SLICE_SCALE": "K-sliced NL4 scale taken from the code bytes",
 }
 
 
