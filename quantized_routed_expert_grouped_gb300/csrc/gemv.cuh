@@ -783,6 +783,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
     // producer: the first S tiles may start before the dependency wait (down kernel)
     long long pcur = rb0;
     int issued = 0;
+    const uint64_t pol = l2_evict_first();  // the weights are read once per call
     auto produce_one = [&](bool wait_empty) -> int {  // 1 issued, 0 range exhausted, -1 timeout
         while (pcur < rb1) {
             const Tile t = next_tile(pcur, rb1, rbpg, rt8);
@@ -794,8 +795,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
             }
             const uint32_t bytes = static_cast<uint32_t>(t.nrows) * static_cast<uint32_t>(a.row_bytes);
             mbar_arrive_expect_tx(&full[s], bytes);
-            bulk_g2s(smem + a.off_ring + static_cast<size_t>(s) * a.stage_bytes,
-                     g.ptr + static_cast<size_t>(t.row0) * a.row_bytes, bytes, &full[s]);
+            bulk_g2s_hint(smem + a.off_ring + static_cast<size_t>(s) * a.stage_bytes,
+                          g.ptr + static_cast<size_t>(t.row0) * a.row_bytes, bytes, &full[s], pol);
             ++issued;
             __threadfence_block();
             *reinterpret_cast<volatile int*>(misc) = issued;

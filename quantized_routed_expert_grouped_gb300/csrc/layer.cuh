@@ -427,20 +427,23 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
             mbar_arrive(&pub[d]);
             return true;
         };
+        const uint64_t pol = l2_evict_first();  // the weights are read once per call
         // copy of ring index j's tile into its slot; vmisc[6]: copies issued (lane 0)
         auto copy_tile = [&](int j, const uint8_t* src0, uint32_t b0, const uint8_t* src1, uint32_t b1) {
             uint8_t* dst = smem + A.off_ring + static_cast<size_t>(j % S) * A.stage_bytes;
             mbar_arrive_expect_tx(&full[j % S], b0 + b1);
-            bulk_g2s(dst, src0, b0, &full[j % S]);
-            if (b1) bulk_g2s(dst + b0, src1, b1, &full[j % S]);
+            bulk_g2s_hint(dst, src0, b0, &full[j % S], pol);
+            if (b1) bulk_g2s_hint(dst + b0, src1, b1, &full[j % S], pol);
             vmisc[6] = j + 1;
         };
         const uint32_t hb = static_cast<uint32_t>(half) * static_cast<uint32_t>(A.row_bytes);
         // the first item of CTA b is item b; later ones come from the counter, whose next value is
         // fetched while the current item streams
+        // (the counter's value is consumed only at the loop increment, so the atomic's round trip
+        // overlaps the item's copies instead of stalling lane 0 before them)
         int nx = 0;
-        for (int i = blockIdx.x; !stop && i < nitems; i = __shfl_sync(0xffffffffu, nx, 0)) {
-            if (lane == 0) nx = static_cast<int>(gridDim.x) + atomicAdd(work, 1);
+        for (int i = blockIdx.x; !stop && i < nitems; i = static_cast<int>(gridDim.x) + __shfl_sync(0xffffffffu, nx, 0)) {
+            if (lane == 0) nx = atomicAdd(work, 1);
             if (i < nunits) {
                 const int g = i / upg, jb = i - g * upg;
                 const GroupInfo gr = giA[g];
