@@ -500,24 +500,26 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                                 const uint8_t* src = tile_src(t, bytes);
                                 if (ok) copy_tile(issued + pre, src, bytes, nullptr, 0);
                             }
-                            // h rows of group g complete (every 4-entry batch of every unit);
                             // buffer st_n & 1 free (from the third staging on): every ring index
                             // before the last staging's first one released (indices before
                             // issued - S are, as their slots were claimed again)
-                            ok = ok && !vmisc[1] && wait_count(ready + g, upg * nbat);
                             if (st_n >= 2)
                                 for (int j = issued - S > 0 ? issued - S : 0; ok && j < st_last; ++j)
                                     ok = mbar_wait_bounded(&empty[j % S], static_cast<uint32_t>(j / S) & 1u);
-                            if (!ok && !vmisc[1]) set_err(A.err, MOE_ERR_TIMEOUT);
-                            if (!ok) vmisc[1] = 1;
                             st_last = issued;
                         }
                         ok = __shfl_sync(0xffffffffu, ok, 0);
+                        // h rows of group g complete (every 4-entry batch of every unit): every lane
+                        // polls the counter itself, so its own acquire orders its staging loads
+                        ok = __all_sync(0xffffffffu, ok && !vmisc[1] && wait_count(ready + g, upg * nbat));
                         if (!ok) {
+                            if (lane == 0) {
+                                if (!vmisc[1]) set_err(A.err, MOE_ERR_TIMEOUT);
+                                vmisc[1] = 1;
+                            }
                             stop = true;
                             break;
                         }
-                        (void)ld_acquire(ready + g);  // every lane acquires the counter lane 0 saw complete
                         stage_entries<DT, true>(D, smem, entD, b0, ne, kMaxEntriesPerPass * (st_n & 1), lane, 32);
                         __syncwarp();
                         st_g = g;
