@@ -315,6 +315,23 @@ def run_ours(args, rank, world):
     return line
 
 
+# DRAM read + write bytes of one fused layer launch at T = 4 (layer 0, 29 groups), from the ncu
+# capture summarised in profiles/layer_kernel_window48_T4.md; reported only while the kernel
+# sources hash to the ones the capture was taken on (else null: the counters are stale).
+LAYER_TRAFFIC_T4 = {"bytes": 95_377_920, "sources": ("layer.cuh", "gemv.cuh", "common.cuh", "q8_1.cuh", "route.cuh"),
+                    "sha1": "022f2532761f5e25f34e9b6a0ff1e25601ec4701"}
+
+
+def layer_traffic():
+    import hashlib
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "quantized_routed_expert_grouped_gb300", "csrc")
+    for f in LAYER_TRAFFIC_T4["sources"]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return LAYER_TRAFFIC_T4["bytes"] if h.hexdigest() == LAYER_TRAFFIC_T4["sha1"] else None
+
+
 def layer_roofline(w, bytes_t, hbm_peak, peak_kind, s, reps=10):
     """The fused layer kernel: the T = 4 window graph (48 launches, one per layer) replayed with
     CUDA events on the launching stream; duration per launch = graph time / 48 (consecutive
@@ -335,7 +352,7 @@ def layer_roofline(w, bytes_t, hbm_peak, peak_kind, s, reps=10):
         synth.blob_bytes(w.gu_type, 2 * WL.F, WL.N) / synth.blob_bytes(GU_T, 2 * WL.F, WL.N) - 1)
     return {"kernel": f"fused layer kernel ({synth.NAMES[w.gu_type]} gate/up slots of CB3, NL4 down, T=4)",
             "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
-            "frac": round(ach / hbm_peak, 4), "traffic": None, "peak_kind": peak_kind,
+            "frac": round(ach / hbm_peak, 4), "traffic": layer_traffic(), "peak_kind": peak_kind,
             "bytes_per_launch": int(per_launch), "streamed_bytes_per_launch": int(streamed),
             "streamed_GBps": round(streamed / dur_s / 1e9, 1), "us_per_launch": round(dur_s * 1e6, 2)}
 
