@@ -292,6 +292,7 @@ def run_ours(args, rank, world):
 
     # ---- end to end: pinned host inputs -> device, the window graphs, outputs -> host
     e2e = end_to_end(wins, args, s, world, dev)
+    sparse = sparse_calls(m, dev)
 
     launches = args.steps * len(TS) * launches_per_window(True)
     line = {
@@ -307,7 +308,7 @@ def run_ours(args, rank, world):
         "per_T": per_T,
         "separate_kernels": {"launch": "route + quantize + gate/up + SwiGLU/q8_1 + down per layer", "per_T": separate},
         "native_layout": {"gate_up": "CB3 (read directly), fused launches", "per_T": native},
-        "roofline": roof, "step_us_per_layer_alone": breakdown, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+        "roofline": roof, "step_us_per_layer_alone": breakdown, "second_call_cost": sparse, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
         "setup_s": round(setup_s, 1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -330,6 +331,63 @@ def layer_traffic():
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return LAYER_TRAFFIC_T4["bytes"] if h.hexdigest() == LAYER_TRAFFIC_T4["sha1"] else None
+
+
+def sparse_calls(m, dev, reps=20):
+    """Per-call cost of the second (PCIe) call of a layer on the sparse workload's geometry (64
+    experts, top-8, T = 4, n_embd 2560, n_ff 768, CB2 gate/up, NL4 down): a CUDA graph of 48
+    moe_expert_grouped calls (gate/up, SwiGLU + q8_1, down chained with PDL), each with a
+    device-side n_groups of 0 (empty) or 1 (one group of 2 entries numbered after the first call's
+    32, scattered destinations, its own expert from a 558 MB pool read cold). Microseconds per
+    call from CUDA events around graph replays."""
+    wl = synth.WORKLOADS["sparse"]
+    gu_t, dn_t = wl.pairs[0]
+    E, calls, n = 256, 48, 4 * wl.k
+    cap_e = n + 2
+    pool_gu = synth.weight_blobs(gu_t, 2 * wl.F, wl.N, E, synth.derive_key(wl.seed, 0, gu_t, 0), dev)
+    pool_dn = synth.weight_blobs(dn_t, wl.N, wl.F, E, synth.derive_key(wl.seed, 0, dn_t, 1), dev)
+    tab = lambda p: torch.tensor([p[x].data_ptr() for x in range(E)], dtype=torch.int64, device=dev)
+    tab_gu, tab_dn = tab(pool_gu), tab(pool_dn)
+    cb_gu = torch.from_numpy(synth.codebook(gu_t, wl.seed * 7 + 1).ravel().copy()).to(dev)
+    cb_dn = torch.from_numpy(synth.codebook(dn_t, wl.seed * 7 + 2).ravel().copy()).to(dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    xq = m.quantize_q8_1(torch.from_numpy(synth.activations(4, wl.N, wl.seed, 0.0)).to(dev))
+    gs = torch.tensor([n, n + 2] + [0] * (n - 1), **i32)
+    es = torch.full((cap_e,), -7, **i32)
+    ed = torch.full((cap_e,), -7, **i32)
+    es[n:n + 2] = torch.tensor([3, 1], **i32)
+    ed[n:n + 2] = torch.tensor([n + 4, 2], **i32)
+    gu = torch.zeros((cap_e, 2 * wl.F), dtype=torch.float32, device=dev)
+    hq = torch.zeros((cap_e, wl.F // 32, 36), dtype=torch.uint8, device=dev)
+    out = torch.zeros((n + 6, wl.N), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, **i32)
+    res = {}
+    for ng in (0, 1):
+        ngt = torch.full((1,), ng, **i32)
+        ges = [torch.tensor([(5 * c) % E] + [0] * (n - 1), **i32) for c in range(calls)]
+        cs = [m.ExpertCall(gu_t, cb_gu, dn_t, cb_dn, wl.N, wl.F, tab_gu, tab_dn, E, ges[c], gs, ngt, n, 0, cap_e, xq,
+                           es, ed, gu, hq, out, err, m.F_PDL) for c in range(calls)]
+        for c in cs:
+            c()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            for c in cs:
+                c()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        if int(err.item()):
+            raise RuntimeError(f"sparse calls: device error bits {int(err.item())}")
+        res["empty" if ng == 0 else "one_group_2_entries"] = round(a.elapsed_time(b) * 1e3 / (reps * calls), 2)
+    res.update({"unit": "us/call", "calls_per_graph": calls, "launches_per_call": 3})
+    return res
 
 
 def layer_roofline(w, bytes_t, hbm_peak, peak_kind, s, reps=10):
