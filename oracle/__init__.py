@@ -69,6 +69,9 @@ def _setup(lib):
     lib.orc_transcode_row.argtypes = [_I, _P, _I, _P, _I, _P]
     lib.orc_transcode_row.restype = _I
     lib.orc_route_group.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P]
+    lib.orc_router_topk.argtypes = [_P, _I, _I, _I, _P, _P]
+    lib.orc_router_topk.restype = _I
+    lib.orc_combine.argtypes = [_P, _I64, _P, _P, _I, _I, _I, _I, _P]
     lib.orc_route_group.restype = _I
     return lib
 
@@ -194,6 +197,25 @@ class Oracle:
         assert hq.dtype == np.uint8 and hq.flags.c_contiguous
         self.lib.orc_swiglu_q8_1(_ptr(gu), F, int(e0), int(e1), _ptr(hq))
         return hq
+
+    def router_topk(self, logits, k):
+        """logits fp32 [T, E] -> (topk_ids int32 [T, k], weights fp64 [T, k], rc)."""
+        logits = np.ascontiguousarray(logits, dtype=np.float32)
+        T, E = logits.shape
+        ids = np.zeros((T, k), np.int32)
+        w = np.zeros((T, k), np.float64)
+        rc = self.lib.orc_router_topk(_ptr(logits), T, E, k, _ptr(ids), _ptr(w))
+        return ids, w, rc
+
+    def combine(self, out, topk_ids, weights, n_experts):
+        """out fp32 [T*k, n_embd]; topk_ids [T, k]; weights [T, k] -> y fp64 [T, n_embd]."""
+        out = np.ascontiguousarray(out, dtype=np.float32)
+        ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+        w = np.ascontiguousarray(weights, dtype=np.float64)
+        T, k = ids.shape
+        y = np.zeros((T, out.shape[1]), np.float64)
+        self.lib.orc_combine(_ptr(out), out.shape[1], _ptr(ids), _ptr(w), T, k, int(n_experts), out.shape[1], _ptr(y))
+        return y
 
     def route_group(self, topk_ids, n_experts, entry_base=0, cap_entries=None):
         ids = np.ascontiguousarray(topk_ids, dtype=np.int32)

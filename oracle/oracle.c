@@ -442,3 +442,58 @@ int orc_route_group(const int32_t* topk_ids, int T, int k, int n_experts, int en
     free(pos);
     return dropped;
 }
+
+/* ------------------------------------------------------------------ router and combine */
+
+/* The k largest logits by repeated selection: a logit ranks above another when it is larger,
+ * or equal with the lower expert id. */
+int orc_router_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, double* weights) {
+    if (k <= 0 || k > E || T < 0) return -1;
+    char* taken = (char*)calloc((size_t)E, 1);
+    if (!taken) return -1;
+    for (int t = 0; t < T; ++t) {
+        const float* l = logits + (int64_t)t * E;
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+#ifdef ORC_PLANT_TIE_HIGH
+                if (best < 0 || l[e] >= l[best]) best = e;
+#else
+                if (best < 0 || l[e] > l[best]) best = e;
+#endif
+            }
+            taken[best] = 1;
+            topk_ids[(int64_t)t * k + j] = best;
+        }
+        double sum = 0.0;
+#ifdef ORC_PLANT_SOFTMAX_ALL
+        for (int e = 0; e < E; ++e) sum += exp((double)l[e]);
+#else
+        for (int j = 0; j < k; ++j) sum += exp((double)l[topk_ids[(int64_t)t * k + j]]);
+#endif
+        for (int j = 0; j < k; ++j) weights[(int64_t)t * k + j] = exp((double)l[topk_ids[(int64_t)t * k + j]]) / sum;
+    }
+    free(taken);
+    return 0;
+}
+
+void orc_combine(const float* out, int64_t out_stride, const int32_t* topk_ids, const double* weights, int T,
+                 int k, int E, int n_embd, double* y) {
+    for (int t = 0; t < T; ++t) {
+        for (int n = 0; n < n_embd; ++n) {
+            double acc = 0.0;
+#ifdef ORC_PLANT_COMBINE_SLOT
+            for (int j = 0; j + 1 < k; ++j) {
+#else
+            for (int j = 0; j < k; ++j) {
+#endif
+                const int x = topk_ids[(int64_t)t * k + j];
+                if (x < 0 || x >= E) continue;
+                acc += weights[(int64_t)t * k + j] * (double)out[((int64_t)t * k + j) * out_stride + n];
+            }
+            y[(int64_t)t * n_embd + n] = acc;
+        }
+    }
+}

@@ -98,6 +98,18 @@ int orc_route_group(const int32_t* topk_ids, int T, int k, int n_experts, int en
                     int32_t* grp_expert, int32_t* grp_start, int32_t* n_groups,
                     int32_t* ent_src, int32_t* ent_dst);
 
+/* The steps either side of the grouped call (the pages do not define the router; this is the
+ * plainest reading, and "the combined output" of #3455's parity check for the combine):
+ * router: for each token t, the k largest of logits[t][0..E) (ties: the lower expert id first)
+ * in descending order -> topk_ids[t][0..k); weights[t][j] = e^(l_j) / sum over the k selected
+ * of e^(l_i), in fp64 (libm exp). Returns -1 if k > E or k <= 0. */
+int orc_router_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, double* weights);
+
+/* combine: y[t][n] = sum over j < k with 0 <= topk_ids[t][j] < E of weights[t][j] * out[t*k+j][n],
+ * in fp64 (rows of n_embd values, out_stride apart). */
+void orc_combine(const float* out, int64_t out_stride, const int32_t* topk_ids, const double* weights, int T,
+                 int k, int E, int n_embd, double* y);
+
 #ifdef __cplusplus
 }
 #endif

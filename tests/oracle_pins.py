@@ -15,6 +15,12 @@ What pins what:
                    bit order, sub-scale nibble and 2*sub+1), one-hot activations that read out
                    one column, and brute-force fp64 dot products of dequantized operands
   grouping      -> a hand-worked routing example and invariants on random routings
+  router        -> a hand-worked top-k with a tie and its softmax in closed form (e/(e+2),
+                   1/(e+2)), equal logits (ids 0..k-1, weights 1/k), and on random logits: no
+                   unselected logit ranks above a selected one, weights sum to 1, weight ratios
+                   are e^(l_i - l_j)
+  combine       -> one-hot weights read out one row, identical rows give the row times the weight
+                   sum, a hand-worked 2-token example, dropped ids skipped
   grouped steps -> permutation invariants and untouched rows
 """
 from __future__ import annotations
@@ -412,6 +418,58 @@ def check_swiglu_q8_1(o):
         assert np.array_equal(hq[e], o.quantize_q8_1(h[None, :])[0])
 
 
-ALL_CHECKS = [check_f16, check_exp, check_silu, check_q8_1, check_formats_hand, check_formats_onehot,
+# ------------------------------------------------------------------ router and combine
+
+def check_router(o):
+    ids, w, rc = o.router_topk(np.array([[0.5, 2, -1, 2, 3]], np.float32), 3)
+    e = np.e
+    assert rc == 0 and ids.tolist() == [[4, 1, 3]], ids
+    assert np.allclose(w[0], [e / (e + 2), 1 / (e + 2), 1 / (e + 2)], rtol=0, atol=1e-15), w
+    ids, w, rc = o.router_topk(np.full((2, 10), 0.25, np.float32), 4)
+    assert rc == 0 and ids.tolist() == [[0, 1, 2, 3]] * 2 and np.allclose(w, 0.25, rtol=0, atol=1e-15)
+    rng = np.random.Generator(np.random.PCG64(31))
+    for E, k in ((8, 2), (64, 8), (128, 8), (40, 40)):
+        lg = rng.standard_normal((5, E)).astype(np.float32)
+        lg[0, 3] = lg[0, 7]  # a tie
+        ids, w, rc = o.router_topk(lg, k)
+        assert rc == 0
+        for t in range(5):
+            sel = list(ids[t])
+            assert len(set(sel)) == k
+            for a, b in zip(sel, sel[1:]):  # descending, ties by id
+                assert lg[t, a] > lg[t, b] or (lg[t, a] == lg[t, b] and a < b)
+            last = sel[-1]
+            for x in range(E):
+                if x not in sel:
+                    assert lg[t, x] < lg[t, last] or (lg[t, x] == lg[t, last] and x > last)
+            assert abs(w[t].sum() - 1.0) < 1e-12
+            for j in range(1, k):
+                assert abs(w[t, 0] / w[t, j] - np.exp(float(lg[t, sel[0]]) - float(lg[t, sel[j]]))) < 1e-9 * w[t, 0] / w[t, j]
+    assert o.router_topk(np.zeros((1, 4), np.float32), 5)[2] == -1
+
+
+def check_combine(o):
+    rng = np.random.Generator(np.random.PCG64(37))
+    T, k, E, N = 3, 4, 16, 64
+    out = rng.standard_normal((T * k, N)).astype(np.float32)
+    ids = np.tile(np.arange(k, dtype=np.int32), (T, 1))
+    for j in range(k):  # one-hot weights read out row t*k + j
+        w = np.zeros((T, k)); w[:, j] = 1.0
+        y = o.combine(out, ids, w, E)
+        assert np.array_equal(y, out[j::k].astype(np.float64))
+    same = np.repeat(out[:T], k, axis=0)  # rows t*k .. t*k+k-1 all equal out[t]
+    w = rng.random((T, k))
+    y = o.combine(same, ids, w, E)
+    assert np.allclose(y, out[:T].astype(np.float64) * w.sum(1, keepdims=True), rtol=1e-14, atol=0)
+    # hand-worked: 2 tokens, k = 2, N = 2
+    o2 = np.array([[1, 2], [3, 4], [5, 6], [7, 8]], np.float32)
+    y = o.combine(o2, np.array([[0, 1], [2, 3]], np.int32), np.array([[0.25, 0.75], [0.5, 0.5]]), 4)
+    assert y.tolist() == [[2.5, 3.5], [6.0, 7.0]], y
+    # a dropped id (outside [0, E)) contributes nothing
+    y = o.combine(o2, np.array([[0, -1], [9, 3]], np.int32), np.array([[0.25, 0.75], [0.5, 0.5]]), 4)
+    assert y.tolist() == [[0.25, 0.5], [3.5, 4.0]], y
+
+
+ALL_CHECKS = [check_router, check_combine, check_f16, check_exp, check_silu, check_q8_1, check_formats_hand, check_formats_onehot,
               check_formats_bruteforce, check_slots, check_route_hand, check_route_invariants, check_grouped_invariants,
               check_swiglu_q8_1]

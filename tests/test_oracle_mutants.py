@@ -17,6 +17,9 @@ PLANTS = {
     "ORC_PLANT_ROUTE_ORDER": "entries of a group ordered by slot first",
     "ORC_PLANT_ENTRY_ROW": "gate/up reads the entry index instead of its token row",
     "ORC_PLANT_SLOT_ORDER": "4-bit slot codes read interleaved",
+    "ORC_PLANT_TIE_HIGH": "router ties resolved to the higher expert id",
+    "ORC_PLANT_SOFTMAX_ALL": "router softmax over every expert instead of the selected k",
+    "ORC_PLANT_COMBINE_SLOT": "combine drops the last slot",
 }
 
 
