@@ -284,6 +284,28 @@ int64_t moe_layer_sync_ints(int T, int k, int n_ff);
 
 int moe_expert_layer(const moe_layer_call* call, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- the steps either side
+ * The router before the grouped call and the combine after it. The pages do not define the
+ * router; this library takes the plainest reading. "The combined output" is what #3455 "GP100
+ * (sm_60): 4-bit slots for resident IQ2_S / IQ3_XXS / IQ3_S gate/up experts" checks in "Passed". */
+
+/* Router: for each token t < T, the k largest of logits[t][0 .. n_experts) (fp32, finite; ties:
+ * the lower expert id first), in descending order, to topk_ids[t][0 .. k) (int32), and
+ * weights[t][j] = e^(l_j - l_0) / sum over the k selected of e^(l_i - l_0) (fp32; this library's
+ * exp, the sum in slot order, an IEEE divide). The ids feed moe_route_group / moe_expert_layer.
+ * Limits: 1 <= k <= 32, k <= n_experts <= 1024, else MOE_E_SHAPE. */
+int moe_router_topk(const float* logits, int T, int n_experts, int k, int32_t* topk_ids, float* weights,
+                    cudaStream_t stream);
+
+/* Combine: y[t][n] = sum over j < k of weights[t][j] * out[t*k + j][n] for n < n_embd, skipping
+ * slots whose topk_ids[t][j] lies outside [0, n_experts) (ids the routing dropped: their out rows
+ * are never written and never read). out rows are the entries' destination rows of the grouped
+ * call (out_row_stride floats apart), y rows y_row_stride floats apart; fp32 fused multiply-adds
+ * from zero in slot order. Errors: MOE_E_NULL, MOE_E_SHAPE (T outside [1, 65535], k <= 0, n_embd
+ * <= 0, a stride below n_embd), MOE_E_CAP (n_experts <= 0). */
+int moe_combine(const float* out, int64_t out_row_stride, const int32_t* topk_ids, const float* weights, int T, int k,
+                int n_experts, int n_embd, float* y, int64_t y_row_stride, cudaStream_t stream);
+
 /* Test hook: the per-32-block integer sums of `rows` consecutive rows of one blob (row bytes
  * apart) against one q8_1 row xq[K/32], computed by the same device decode and dot-product
  * code as the grouped kernels: isum[r][b] = sum_i w_code_i * q_i (exact int32). */

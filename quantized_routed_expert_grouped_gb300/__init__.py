@@ -18,7 +18,7 @@ __all__ = [
     "Q8_0", "Q4B", "NL4", "CB2", "CB3", "CB3X", "CB2X", "MoeError", "transcode_cb", "lib", "row_bytes", "strerror",
     "quantize_q8_1", "route_group", "grouped_gu", "swiglu_q8_1", "grouped_down",
     "expert_grouped", "ExpertCall", "STATIC_SCRATCH_BYTES", "test_block_isum", "ERR_BITS", "F_PDL",
-    "LayerCall", "layer_sync_ints",
+    "LayerCall", "layer_sync_ints", "router_topk", "combine",
 ]
 
 Q8_0, Q4B, NL4, CB2, CB3, CB3X, CB2X = 1, 2, 3, 4, 5, 6, 7
@@ -91,9 +91,11 @@ def lib():
         L.moe_expert_layer.argtypes = [ctypes.POINTER(LayerCallC), _P]
         L.moe_layer_sync_ints.argtypes = [_I, _I, _I]
         L.moe_layer_sync_ints.restype = _I64
+        L.moe_router_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P]
+        L.moe_combine.argtypes = [_P, _I64, _P, _P, _I, _I, _I, _I, _P, _I64, _P]
         for f in ("moe_quantize_q8_1", "moe_route_group", "moe_grouped_gu", "moe_swiglu_q8_1",
                   "moe_grouped_down", "moe_expert_grouped", "moe_expert_grouped_static", "moe_test_block_isum",
-                  "moe_transcode_cb", "moe_expert_layer"):
+                  "moe_transcode_cb", "moe_expert_layer", "moe_router_topk", "moe_combine"):
             getattr(L, f).restype = _I
         _LIB = L
     return _LIB
@@ -216,6 +218,28 @@ class LayerCall:
 
     def __call__(self, stream=None):
         _check(lib().moe_expert_layer(ctypes.byref(self.c), _stream(stream)))
+
+
+def router_topk(logits, k, topk_ids=None, weights=None, stream=None):
+    """logits fp32 [T, n_experts] -> (topk_ids int32 [T, k], weights fp32 [T, k]) on the device."""
+    T, E = logits.shape
+    if topk_ids is None:
+        topk_ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    if weights is None:
+        weights = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _check(lib().moe_router_topk(_dp(logits), T, E, k, _dp(topk_ids), _dp(weights), _stream(stream)))
+    return topk_ids, weights
+
+
+def combine(out, topk_ids, weights, n_experts, y=None, stream=None):
+    """out fp32 [T*k, >= n_embd] (row t*k + j = entry (t, j)); -> y fp32 [T, n_embd]."""
+    T, k = topk_ids.shape
+    N = out.shape[1]
+    if y is None:
+        y = torch.empty((T, N), dtype=torch.float32, device=out.device)
+    _check(lib().moe_combine(_dp(out), out.stride(0), _dp(topk_ids), _dp(weights), T, k, n_experts, N, _dp(y),
+                             y.stride(0), _stream(stream)))
+    return y
 
 
 def expert_grouped(*args, stream=None, **kw):

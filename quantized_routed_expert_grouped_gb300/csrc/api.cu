@@ -530,6 +530,25 @@ int moe_expert_layer(const moe_layer_call* c, cudaStream_t stream) {
     return MOE_OK;
 }
 
+int moe_router_topk(const float* logits, int T, int n_experts, int k, int32_t* topk_ids, float* weights,
+                    cudaStream_t stream) {
+    if (!logits || !topk_ids || !weights) return MOE_E_NULL;
+    if (T <= 0 || k <= 0 || k > 32 || n_experts < k || n_experts > 1024) return MOE_E_SHAPE;
+    return launch_router_topk(logits, T, n_experts, k, topk_ids, weights, stream) == cudaSuccess ? MOE_OK : MOE_E_CUDA;
+}
+
+int moe_combine(const float* out, int64_t out_row_stride, const int32_t* topk_ids, const float* weights, int T, int k,
+                int n_experts, int n_embd, float* y, int64_t y_row_stride, cudaStream_t stream) {
+    if (!out || !topk_ids || !weights || !y) return MOE_E_NULL;
+    if (T <= 0 || T > 65535 || k <= 0 || n_embd <= 0 || out_row_stride < n_embd || y_row_stride < n_embd)
+        return MOE_E_SHAPE;
+    if (n_experts <= 0) return MOE_E_CAP;
+    return launch_combine(out, out_row_stride, topk_ids, weights, T, k, n_experts, n_embd, y, y_row_stride, stream) ==
+                   cudaSuccess
+               ? MOE_OK
+               : MOE_E_CUDA;
+}
+
 int moe_transcode_cb(moe_wfmt src, int dst_type, int K, int rows, int n_blobs, const void* const* src_blobs,
                      void* const* dst_blobs, int32_t* err, cudaStream_t stream) {
     if (!cb_type(src.type) || (dst_type != MOE_CB3X && dst_type != MOE_CB2X)) return MOE_E_TYPE;

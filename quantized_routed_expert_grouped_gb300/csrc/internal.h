@@ -98,6 +98,9 @@ cudaError_t launch_route_group(const int32_t* topk_ids, int T, int k, int n_expe
                                int32_t* grp_expert, int32_t* grp_start, int32_t* n_groups, int32_t* ent_src,
                                int32_t* ent_dst, int32_t* err, cudaStream_t s);
 
+cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
+cudaError_t launch_combine(const float* out, int64_t os, const int32_t* ids, const float* w, int T, int k, int E, int N,
+                           float* y, int64_t ys, cudaStream_t s);
 cudaError_t launch_transcode_cb(int src_type, const int8_t* codebook, int dst_type, int K, int rows, int n_blobs,
                                 const void* const* src_blobs, void* const* dst_blobs, int32_t* err, cudaStream_t s);
 

@@ -66,6 +66,15 @@ def test_host_argument_errors(m):
     assert L.moe_route_group(dummy, 40, 32, 8, 0, dummy, dummy, dummy, dummy, dummy, None, None) == -3
     assert L.moe_expert_grouped(None, None) == -1
     assert L.moe_test_block_isum(W(1, None), 300, dummy, 1, dummy, dummy, None) == -3
+    # the router and the combine
+    assert L.moe_router_topk(None, 4, 128, 8, dummy, dummy, None) == -1
+    assert L.moe_router_topk(dummy, 4, 128, 33, dummy, dummy, None) == -3   # k > 32
+    assert L.moe_router_topk(dummy, 4, 4, 8, dummy, dummy, None) == -3      # k > n_experts
+    assert L.moe_router_topk(dummy, 4, 2000, 8, dummy, dummy, None) == -3   # n_experts > 1024
+    assert L.moe_combine(dummy, 2560, dummy, dummy, 4, 8, 128, 2560, None, 2560, None) == -1
+    assert L.moe_combine(dummy, 100, dummy, dummy, 4, 8, 128, 2560, dummy, 2560, None) == -3
+    assert L.moe_combine(dummy, 2560, dummy, dummy, 70000, 8, 128, 2560, dummy, 2560, None) == -3
+    assert L.moe_combine(dummy, 2560, dummy, dummy, 4, 8, 0, 2560, dummy, 2560, None) == -4
 
 
 def test_layer_call_host_errors(m):
