@@ -316,9 +316,33 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                   blockIdx.x == 0);
         __syncthreads();
     }
+    int early = 0;  // ring indices of the CTA's first item copied before the tables (warp 0, lane 0)
     if (warp == 0) {
         if (n <= 32) route_warp(L.ids, n, L.k, A.n_experts, rgx, rgs, rng, rsrc, rdst, A.err, blockIdx.x == 0, lane);
         __syncwarp();
+        // The CTA's first work item is its own index. When that is a gate/up unit, the first batch's
+        // tiles need only the group's expert id, so they are copied now, before the tables are
+        // built; the producer publishes them without copying again.
+        if (lane == 0 && static_cast<int>(blockIdx.x) < *rng * upg) {
+            const int g = static_cast<int>(blockIdx.x) / upg, jb = static_cast<int>(blockIdx.x) - g * upg;
+            const int x = rgx[g];
+            const uint8_t* pa = pcA ? pcA[x] : static_cast<const uint8_t*>(A.w[x]);
+            const uint8_t* pd = pcD ? pcD[x] : static_cast<const uint8_t*>(D.w[x]);
+            if (((reinterpret_cast<uintptr_t>(pa) | reinterpret_cast<uintptr_t>(pd)) & 15u) == 0) {  // as build_tables
+                const uint64_t pol = l2_evict_first();
+                const int half = A.RT >> 1;
+                const uint32_t hb = static_cast<uint32_t>(half) * static_cast<uint32_t>(A.row_bytes);
+                early = tpu < A.stages ? tpu : A.stages;
+                for (int h = 0; h < early; ++h) {
+                    const size_t rg = static_cast<size_t>(32 * jb + h * half);
+                    uint8_t* dst = smem + A.off_ring + static_cast<size_t>(h) * A.stage_bytes;
+                    mbar_arrive_expect_tx(&full[h], 2 * hb);
+                    bulk_g2s_hint(dst, pa + rg * A.row_bytes, hb, &full[h], pol);
+                    bulk_g2s_hint(dst + hb, pa + (rg + F) * A.row_bytes, hb, &full[h], pol);
+                }
+                vmisc[6] = early;
+            }
+        }
         build_tables<GT, DT>(L, pcA, pcD, rgx, rgs, rng, rsrc, rdst, giA, giD, entA, entD, misc, lane);
         __threadfence_block();
         bar_arrive(3, NT);  // tables ready
@@ -462,12 +486,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                             break;
                         }
                         for (int h = 0; h < tpu; ++h) {
-                            if (!slot_free(issued)) {
+                            const bool pre = issued < early;  // copied before the tables (first item)
+                            if (!pre && !slot_free(issued)) {
                                 stop = true;
                                 break;
                             }
                             const size_t rg = static_cast<size_t>(32 * jb + h * half);
-                            copy_tile(issued, gr.ptr + rg * A.row_bytes, hb, gr.ptr + (rg + F) * A.row_bytes, hb);
+                            if (!pre) copy_tile(issued, gr.ptr + rg * A.row_bytes, hb, gr.ptr + (rg + F) * A.row_bytes, hb);
                             if (!publish(0, g, jb, h, b0, ne, ku, A.nch)) {
                                 stop = true;
                                 break;
