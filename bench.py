@@ -58,6 +58,21 @@ def routing_for(layer, T):
     return synth.routing(T, WL.k, WL.E, WL.seed * 1000 + layer * 10 + T + 5)
 
 
+def job_ms(local_ms, world, device):
+    """The whole job's time: the slowest rank's (replicas run independent windows; the timed region
+    is bracketed by barriers on every rank)."""
+    if world <= 1:
+        return float(local_ms)
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def us_per_window(total_ms, windows_per_rank, world):
+    """Microseconds per window over every rank's windows (the replicas' aggregate throughput)."""
+    return total_ms * 1e3 / (windows_per_rank * world)
+
+
 def acts_for(layer, T):
     return synth.activations(T, WL.N, WL.seed * 1000 + layer * 10 + T, WL.outliers)
 
@@ -249,13 +264,9 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = job_ms(total_ms, world, dev)
     us_t = {T: float(np.median([a.elapsed_time(b) * 1e3 for a, b in per_t[T]])) for T in TS}
-    windows = args.steps * len(TS) * world
-    value = total_ms * 1e3 / windows
+    value = us_per_window(total_ms, args.steps * len(TS), world)
     bytes_t = {T: weight_bytes_per_window(T) for T in TS}
     per_T = {str(T): {"us": round(us_t[T], 2), "weight_bytes": bytes_t[T][0],
                       "GBps": round(bytes_t[T][0] / (us_t[T] * 1e-6) / 1e9, 1),
@@ -478,11 +489,8 @@ def end_to_end(wins, args, s, world, dev):
     b.record(s)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": round(ms * 1e3 / (steps * len(wins) * world), 3), "unit": "us/window",
+    ms = job_ms(ms, world, dev)
+    return {"value": round(us_per_window(ms, steps * len(wins), world), 3), "unit": "us/window",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
