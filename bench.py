@@ -349,8 +349,8 @@ def sparse_calls(m, dev, reps=20):
     experts, top-8, T = 4, n_embd 2560, n_ff 768, CB2 gate/up, NL4 down): a CUDA graph of 48
     moe_expert_grouped calls (gate/up, SwiGLU + q8_1, down chained with PDL), each with a
     device-side n_groups of 0 (empty) or 1 (one group of 2 entries numbered after the first call's
-    32, scattered destinations, its own expert from a 558 MB pool read cold). Microseconds per
-    call from CUDA events around graph replays."""
+    32, scattered destinations, its own expert from a 558 MB pool read cold), with grid_groups 0
+    (the capacity) and 1. Microseconds per call from CUDA events around graph replays."""
     wl = synth.WORKLOADS["sparse"]
     gu_t, dn_t = wl.pairs[0]
     E, calls, n = 256, 48, 4 * wl.k
@@ -373,10 +373,10 @@ def sparse_calls(m, dev, reps=20):
     out = torch.zeros((n + 6, wl.N), dtype=torch.float32, device=dev)
     err = torch.zeros(1, **i32)
     res = {}
-    for ng in (0, 1):
+    for ng, gg in ((0, 0), (1, 0), (0, 1), (1, 1)):
         ngt = torch.full((1,), ng, **i32)
         ges = [torch.tensor([(5 * c) % E] + [0] * (n - 1), **i32) for c in range(calls)]
-        cs = [m.ExpertCall(gu_t, cb_gu, dn_t, cb_dn, wl.N, wl.F, tab_gu, tab_dn, E, ges[c], gs, ngt, n, 0, cap_e, xq,
+        cs = [m.ExpertCall(gu_t, cb_gu, dn_t, cb_dn, wl.N, wl.F, tab_gu, tab_dn, E, ges[c], gs, ngt, n, gg, cap_e, xq,
                            es, ed, gu, hq, out, err, m.F_PDL) for c in range(calls)]
         for c in cs:
             c()
@@ -396,7 +396,8 @@ def sparse_calls(m, dev, reps=20):
         torch.cuda.synchronize()
         if int(err.item()):
             raise RuntimeError(f"sparse calls: device error bits {int(err.item())}")
-        res["empty" if ng == 0 else "one_group_2_entries"] = round(a.elapsed_time(b) * 1e3 / (reps * calls), 2)
+        key = ("empty" if ng == 0 else "one_group_2_entries") + ("_grid_groups_1" if gg else "")
+        res[key] = round(a.elapsed_time(b) * 1e3 / (reps * calls), 2)
     res.update({"unit": "us/call", "calls_per_graph": calls, "launches_per_call": 3})
     return res
 
