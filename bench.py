@@ -154,9 +154,12 @@ class Window:
         self.calls = [m.ExpertCall(gu_type, cb_gu, DN_T, cb_dn, WL.N, WL.F, tab_gu[l], tab_dn[l], WL.E, self.ge[l],
                                    self.gs[l], self.ng[l], n, 0, n, self.xq[l], self.es[l], self.ed[l], self.gu,
                                    self.hq, self.out[l], self.err, m.F_PDL) for l in range(L)]
-        self.sync = torch.zeros(m.layer_sync_ints(T, WL.k, WL.F), **i32)
+        # a pair of counter halves: layer l uses half l % 2 and zeroes the other (48 layers: the
+        # halves alternate across graph replays too)
+        self.sync = torch.zeros(2 * m.layer_sync_ints(T, WL.k, WL.F), **i32)
         self.lcalls = [m.LayerCall(gu_type, cb_gu, DN_T, cb_dn, WL.N, WL.F, tab_gu[l], tab_dn[l], WL.E, self.ids[l],
-                                   self.x[l], self.out[l], self.gu, self.hq, self.sync, self.err, m.F_PDL)
+                                   self.x[l], self.out[l], self.gu, self.hq, self.sync, self.err,
+                                   m.F_PDL | m.F_SYNC_PAIR | (m.F_SYNC_ODD if l % 2 else 0))
                        for l in range(L)]
         self.m = m
         self.graph = None
@@ -313,7 +316,8 @@ def run_ours(args, rank, world):
         "config": {"workload": "window48: 48 layers x 128 experts, top-8, n_embd 2560, n_ff 768, CB3 gate/up + "
                                "NL4 down (16.4 GB pool), T=1..4, one CUDA graph per T",
                    "layout": "gate/up held as CB3X slots (CB3 transcoded at load, same integers); down NL4",
-                   "launch": "one fused launch per layer (routing, q8_1, gate/up, SwiGLU + q8_1, down), PDL-chained",
+                   "launch": "one fused launch per layer (routing, q8_1, gate/up, SwiGLU + q8_1, down), PDL-chained, "
+                  "alternate counter halves",
                    "l2": "inputs larger than L2 (>= 1 GB of weights per window), no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "per_T": per_T,

@@ -179,6 +179,8 @@ int moe_grouped_down(moe_wfmt fmt, int n_embd, int n_ff, const void* const* w_do
 
 /* Flags for moe_expert_call.flags */
 #define MOE_F_PDL 1 /* chain the three kernels with programmatic dependent launch */
+#define MOE_F_SYNC_PAIR 2 /* moe_expert_layer: sync holds two halves used by alternate calls */
+#define MOE_F_SYNC_ODD 4  /* moe_expert_layer with MOE_F_SYNC_PAIR: this call uses the second half */
 
 /* One native_expert_grouped-style call (#363): gate/up, SwiGLU + q8_1, down on one stream. */
 typedef struct moe_expert_call {
@@ -243,6 +245,11 @@ int moe_expert_grouped_static(const moe_expert_call* call, cudaStream_t stream);
  *    The caller zeroes them once before the first call (e.g. cudaMemsetAsync); every call leaves
  *    them zero. A call that reported MOE_ERR_TIMEOUT may leave them non-zero: zero them again.
  *    Calls that may overlap on the GPU need separate sync arrays (and scratch).
+ *    With MOE_F_SYNC_PAIR in flags, sync holds two halves of moe_layer_sync_ints ints: the call uses
+ *    the first half (the second with MOE_F_SYNC_ODD) and zeroes the other one after its dependency
+ *    wait, instead of having its last CTA zero its own half on the way out (a device-wide fence and
+ *    an atomic per CTA less at the end of every call). Consecutive calls on one stream that share
+ *    the array must alternate halves; zero both halves before the first call.
  *  - grp_expert [T*k], grp_start [T*k+1], n_groups [1], ent_src / ent_dst [T*k], xq
  *    [T][n_embd/32]: optional (NULL = not written) copies of the grouping and of the activation
  *    q8_1, for inspection.

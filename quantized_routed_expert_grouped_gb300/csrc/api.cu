@@ -515,6 +515,13 @@ int moe_expert_layer(const moe_layer_call* c, cudaStream_t stream) {
     L.x = c->x;
     L.hq = c->hq;
     L.sync = c->sync;
+    L.sync_other = nullptr;
+    if (c->flags & MOE_F_SYNC_PAIR) {  // two halves; this call uses one and zeroes the other
+        const int64_t half = moe_layer_sync_ints(c->T, c->k, c->n_ff);
+        const bool odd = (c->flags & MOE_F_SYNC_ODD) != 0;
+        L.sync = c->sync + (odd ? half : 0);
+        L.sync_other = c->sync + (odd ? 0 : half);
+    }
     L.o_ge = c->grp_expert;
     L.o_gs = c->grp_start;
     L.o_ng = c->n_groups;

@@ -77,7 +77,8 @@ struct LayerArgs {
     const int32_t* ids;  // [T][k] top-k expert ids
     const float* x;      // [T][n_embd]
     moe_q8_1* hq;        // [n][F/32]: the q8_1 h rows (exchanged between the CTAs)
-    int32_t* sync;       // [n] per-group h-block counters, [1] exit counter
+    int32_t* sync;       // [n] per-group h-block counters, [1] exit counter, [1] work-item counter
+    int32_t* sync_other; // the other half of a sync pair (zeroed by this call; nullptr: no pair)
     int32_t *o_ge, *o_gs, *o_ng, *o_es, *o_ed;  // optional copies of the grouping (CTA 0)
     moe_q8_1* o_xq;                             // optional copy of the activation q8_1 (CTA 0)
     int T, k, n;         // n = T * k entries (and the capacity of every per-group table)

@@ -308,6 +308,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     __syncthreads();
     pdl_wait();
     pdl_trigger();
+    // a sync pair: the call that used the other half has completed; zero it for the next call
+    if (L.sync_other && blockIdx.x == 0)
+        for (int i = tid; i < n + 2; i += NT) L.sync_other[i] = 0;
 
     // ---- routing/grouping and tables: one warp when n <= 32, else the whole CTA routes and
     // warp 0 builds the tables
@@ -735,7 +738,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         for (int qq = nq - S > 0 ? nq - S : 0; qq < nq; ++qq)
             mbar_wait_bounded(&full[qq % S], static_cast<uint32_t>(qq / S) & 1u);
     }
-    // ---- exit count; the last CTA zeroes the counters for the next call
+    // ---- exit count; the last CTA zeroes the counters for the next call (with a sync pair, the
+    // next call zeroes them instead)
+    if (L.sync_other) return;
     if (tid == 0) {
         __threadfence();
         misc[2] = atomicAdd(L.sync + n, 1) == static_cast<int>(gridDim.x) - 1;

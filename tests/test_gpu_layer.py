@@ -149,6 +149,49 @@ def test_layer_repeated_calls_pdl_and_graph(m, orc):
     assert not sync.any()
 
 
+def test_layer_sync_pair_alternating_halves(m, orc):
+    """MOE_F_SYNC_PAIR: four layers at T = 4 alternate the two halves of one counter array (each
+    call zeroes the other half instead of its last CTA zeroing its own), eager with PDL and in a
+    CUDA graph replayed twice: the outputs equal the default mode's bit for bit, and after every
+    call the half the next call uses is zero."""
+    wl = synth.WORKLOADS["window48"]
+    layers = [H.transcoded(m, H.make_layer(wl, (synth.CB3, synth.NL4), 4, layer=l), synth.CB3X) for l in range(4)]
+    base = []
+    for L in layers:  # default mode, each with its own counters
+        f = Fused(m, L)
+        f.call()
+        torch.cuda.synchronize()
+        assert int(f.err.item()) == 0
+        base.append(f.out.clone())
+    half = m.layer_sync_ints(4, wl.k, wl.F)
+    pair = torch.zeros(2 * half, dtype=torch.int32, device="cuda")
+    fs = [Fused(m, L) for L in layers]
+    for i, f in enumerate(fs):
+        f.call.c.sync = pair.data_ptr()
+        f.call.c.flags = m.F_PDL | m.F_SYNC_PAIR | (m.F_SYNC_ODD if i % 2 else 0)
+    for i, f in enumerate(fs):  # one at a time: the next call's half is zero after each
+        f.call()
+        torch.cuda.synchronize()
+        nxt = pair[half:] if i % 2 == 0 else pair[:half]
+        assert not nxt.any()
+    for f, b in zip(fs, base):
+        assert int(f.err.item()) == 0
+        assert torch.equal(f.out.view(torch.int32), b.view(torch.int32))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        for f in fs:
+            f.call()
+    for _ in range(2):
+        for f in fs:
+            f.out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for f, b in zip(fs, base):
+            assert torch.equal(f.out.view(torch.int32), b.view(torch.int32))
+        assert not pair[:half].any()  # the last call (odd) zeroed the first half
+    assert all(int(f.err.item()) == 0 for f in fs)
+
+
 def test_layer_dropped_ids_and_empty(m, orc):
     wl = synth.WORKLOADS["verify"]
     L = H.make_layer(wl, (synth.CB2, synth.NL4), 4)
