@@ -124,6 +124,36 @@ class Clocks:
 
 # ------------------------------------------------------------------ our arm
 
+def make_pools(m, dev):
+    """The window's resident weights: per layer 128 experts' CB3 gate/up and NL4 down blobs (seeded,
+    16.4 GB), the gate/up pool transcoded at load into CB3X slots (12.8 GB), the pointer tables and
+    the codebooks."""
+    gu_b = synth.blob_bytes(GU_T, 2 * WL.F, WL.N)
+    dn_b = synth.blob_bytes(DN_T, WL.N, WL.F)
+    pool_gu = torch.empty((WL.layers, WL.E, gu_b), dtype=torch.uint8, device=dev)
+    pool_dn = torch.empty((WL.layers, WL.E, dn_b), dtype=torch.uint8, device=dev)
+    for l in range(WL.layers):
+        pool_gu[l] = synth.weight_blobs(GU_T, 2 * WL.F, WL.N, WL.E, synth.derive_key(WL.seed, l, GU_T, 0), dev)
+        pool_dn[l] = synth.weight_blobs(DN_T, WL.N, WL.F, WL.E, synth.derive_key(WL.seed, l, DN_T, 1), dev)
+    tab = lambda p, l: torch.tensor([p[l, x].data_ptr() for x in range(WL.E)], dtype=torch.int64, device=dev)
+    tab_gu = [tab(pool_gu, l) for l in range(WL.layers)]
+    tab_dn = [tab(pool_dn, l) for l in range(WL.layers)]
+    cb_gu = torch.from_numpy(synth.codebook(GU_T, WL.seed * 7 + 1).ravel().copy()).to(dev)
+    cb_dn = torch.from_numpy(synth.codebook(DN_T, WL.seed * 7 + 2).ravel().copy()).to(dev)
+    # load-time transcoding of the gate/up pool into the slot layout
+    xb = synth.blob_bytes(XT, 2 * WL.F, WL.N)
+    pool_gx = torch.empty((WL.layers, WL.E, xb), dtype=torch.uint8, device=dev)
+    tab_gx = [tab(pool_gx, l) for l in range(WL.layers)]
+    terr = torch.zeros(1, dtype=torch.int32, device=dev)
+    for l in range(WL.layers):
+        m.transcode_cb(GU_T, cb_gu, XT, WL.N, 2 * WL.F, tab_gu[l], tab_gx[l], terr)
+    torch.cuda.synchronize()
+    if int(terr.item()):
+        raise RuntimeError(f"transcoding error bits {int(terr.item())}")
+    return dict(pool_gu=pool_gu, pool_dn=pool_dn, pool_gx=pool_gx, tab_gu=tab_gu, tab_dn=tab_dn, tab_gx=tab_gx,
+                cb_gu=cb_gu, cb_dn=cb_dn)
+
+
 class Window:
     """Device state of one T: inputs, routing outputs, scratch and the captured 48-layer graph.
 
@@ -200,28 +230,8 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     hbm_peak, peak_kind = peaks()
     t0 = time.time()
-    gu_b = synth.blob_bytes(GU_T, 2 * WL.F, WL.N)
-    dn_b = synth.blob_bytes(DN_T, WL.N, WL.F)
-    pool_gu = torch.empty((WL.layers, WL.E, gu_b), dtype=torch.uint8, device=dev)
-    pool_dn = torch.empty((WL.layers, WL.E, dn_b), dtype=torch.uint8, device=dev)
-    for l in range(WL.layers):
-        pool_gu[l] = synth.weight_blobs(GU_T, 2 * WL.F, WL.N, WL.E, synth.derive_key(WL.seed, l, GU_T, 0), dev)
-        pool_dn[l] = synth.weight_blobs(DN_T, WL.N, WL.F, WL.E, synth.derive_key(WL.seed, l, DN_T, 1), dev)
-    tab = lambda p, l: torch.tensor([p[l, x].data_ptr() for x in range(WL.E)], dtype=torch.int64, device=dev)
-    tab_gu = [tab(pool_gu, l) for l in range(WL.layers)]
-    tab_dn = [tab(pool_dn, l) for l in range(WL.layers)]
-    cb_gu = torch.from_numpy(synth.codebook(GU_T, WL.seed * 7 + 1).ravel().copy()).to(dev)
-    cb_dn = torch.from_numpy(synth.codebook(DN_T, WL.seed * 7 + 2).ravel().copy()).to(dev)
-    # load-time transcoding of the gate/up pool into the slot layout
-    xb = synth.blob_bytes(XT, 2 * WL.F, WL.N)
-    pool_gx = torch.empty((WL.layers, WL.E, xb), dtype=torch.uint8, device=dev)
-    tab_gx = [tab(pool_gx, l) for l in range(WL.layers)]
-    terr = torch.zeros(1, dtype=torch.int32, device=dev)
-    for l in range(WL.layers):
-        m.transcode_cb(GU_T, cb_gu, XT, WL.N, 2 * WL.F, tab_gu[l], tab_gx[l], terr)
-    torch.cuda.synchronize()
-    if int(terr.item()):
-        raise RuntimeError(f"transcoding error bits {int(terr.item())}")
+    P = make_pools(m, dev)
+    tab_gu, tab_dn, tab_gx, cb_gu, cb_dn = P["tab_gu"], P["tab_dn"], P["tab_gx"], P["cb_gu"], P["cb_dn"]
     setup_s = time.time() - t0
 
     # headline: fused layer launches on the slot layout; compared: the separate-kernel window on the
