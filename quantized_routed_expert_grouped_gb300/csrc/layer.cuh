@@ -323,9 +323,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     if (warp == 0) {
         if (n <= 32) route_warp(L.ids, n, L.k, A.n_experts, rgx, rgs, rng, rsrc, rdst, A.err, blockIdx.x == 0, lane);
         __syncwarp();
-        // The CTA's first work item is its own index. When that is a gate/up unit, the first batch's
-        // tiles need only the group's expert id, so they are copied now, before the tables are
-        // built; the producer publishes them without copying again.
+        // The CTA's first work item is its own index. When that is a gate/up unit, its first tile
+        // needs only the group's expert id, so it is copied now, before the tables are built; the
+        // producer publishes it without copying again.
         if (lane == 0 && static_cast<int>(blockIdx.x) < *rng * upg) {
             const int g = static_cast<int>(blockIdx.x) / upg, jb = static_cast<int>(blockIdx.x) - g * upg;
             const int x = rgx[g];
@@ -335,7 +335,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 const uint64_t pol = l2_evict_first();
                 const int half = A.RT >> 1;
                 const uint32_t hb = static_cast<uint32_t>(half) * static_cast<uint32_t>(A.row_bytes);
-                early = tpu < A.stages ? tpu : A.stages;
+                // only the first tile: with every CTA copying at once, a smaller first burst lands
+                // sooner, and the producer loop copies the unit's other tile a little later
+                early = 1;
                 for (int h = 0; h < early; ++h) {
                     const size_t rg = static_cast<size_t>(32 * jb + h * half);
                     uint8_t* dst = smem + A.off_ring + static_cast<size_t>(h) * A.stage_bytes;
