@@ -241,19 +241,26 @@ int moe_expert_grouped_static(const moe_expert_call* call, cudaStream_t stream);
  *  - gu, hq: scratch [T*k][2*n_ff] and [T*k][n_ff/32] as in moe_expert_call, rows indexed by
  *    entry (groups by ascending expert id, entries of a group by ascending (t, slot)); after the
  *    call they hold the gate/up rows and the q8_1 h rows.
- *  - sync: moe_layer_sync_ints(T, k, n_ff) int32 counters the launch's CTAs synchronise through.
- *    The caller zeroes them once before the first call (e.g. cudaMemsetAsync); every call leaves
- *    them zero. A call that reported MOE_ERR_TIMEOUT may leave them non-zero: zero them again.
- *    Calls that may overlap on the GPU need separate sync arrays (and scratch).
- *    With MOE_F_SYNC_PAIR in flags, sync holds two halves of moe_layer_sync_ints ints: the call uses
- *    the first half (the second with MOE_F_SYNC_ODD) and zeroes the other one after its dependency
- *    wait, instead of having its last CTA zero its own half on the way out (a device-wide fence and
- *    an atomic per CTA less at the end of every call). Consecutive calls on one stream that share
- *    the array must alternate halves; zero both halves before the first call.
+ *  - sync: moe_layer_sync_ints(T, k, n_ff) int32 words (8-byte aligned, else MOE_E_ALIGN) the
+ *    launch's CTAs synchronise through: word 0 an exit counter, word 1 the work-item counter,
+ *    word 2 the call epoch, and from word 4 a flagged copy of the q8_1 h rows (per entry nine
+ *    rows of one 8-byte pair per h block: a header or code word and the writing call's flag,
+ *    epoch + 1), which
+ *    the down phase polls instead of a counter, so the gate/up side needs no fence. The caller
+ *    zeroes the array once before the first call (e.g. cudaMemsetAsync); every call leaves words
+ *    0 and 1 zero and advances the epoch, so no pair left by an earlier call carries the next
+ *    call's flag. A call that reported MOE_ERR_TIMEOUT may leave the array inconsistent: zero it
+ *    again. Calls that may overlap on the GPU need separate sync arrays (and scratch).
+ *    With MOE_F_SYNC_PAIR in flags, sync holds two halves of moe_layer_sync_ints words: the call
+ *    uses the first half (the second with MOE_F_SYNC_ODD) and resets the other one (zero counters,
+ *    epoch advanced) after its dependency wait, instead of having its last CTA reset its own half
+ *    on the way out (a device-wide fence and an atomic per CTA less at the end of every call).
+ *    Consecutive calls on one stream that share the array must alternate halves; zero both halves
+ *    before the first call.
  *  - grp_expert [T*k], grp_start [T*k+1], n_groups [1], ent_src / ent_dst [T*k], xq
  *    [T][n_embd/32]: optional (NULL = not written) copies of the grouping and of the activation
  *    q8_1, for inspection.
- *  - x and gu must be 16-byte aligned (else MOE_E_ALIGN).
+ *  - x and gu must be 16-byte aligned, sync 8-byte aligned (else MOE_E_ALIGN).
  *  - Formats: any gate/up format; down MOE_NL4 or MOE_Q8_0 (else MOE_E_TYPE).
  *  - Limits: T*k <= 512 and the T activation rows staged in shared memory (44 bytes per 32
  *    values, padded) must fit 64 KB (e.g. T <= 18 at n_embd 2560), else MOE_E_CAP; 32 rows of
@@ -274,7 +281,7 @@ typedef struct moe_layer_call {
     int64_t out_row_stride;
     float* gu;                 /* scratch [T*k][2*n_ff] */
     moe_q8_1* hq;              /* scratch [T*k][n_ff/32] */
-    int32_t* sync;             /* [moe_layer_sync_ints(T, k, n_ff)], zero before the first call */
+    int32_t* sync;             /* [moe_layer_sync_ints(T, k, n_ff)], 8-byte aligned, zero before the first call */
     int32_t* grp_expert;       /* optional */
     int32_t* grp_start;        /* optional */
     int32_t* n_groups;         /* optional */
@@ -285,8 +292,8 @@ typedef struct moe_layer_call {
     int32_t flags;             /* MOE_F_* */
 } moe_layer_call;
 
-/* Number of int32 counters moe_expert_layer needs for windows of T tokens, top-k, n_ff
- * (T*k + 2; 0 for invalid arguments). */
+/* Number of int32 sync words moe_expert_layer needs for windows of T tokens, top-k, n_ff:
+ * 4 + T*k * (n_ff/32) * 18 (always even; 0 for invalid arguments). */
 int64_t moe_layer_sync_ints(int T, int k, int n_ff);
 
 int moe_expert_layer(const moe_layer_call* call, cudaStream_t stream);

@@ -194,7 +194,8 @@ class ExpertCall:
 
 
 def layer_sync_ints(T: int, k: int, n_ff: int) -> int:
-    """int32 counters a moe_expert_layer call needs (zero them once before the first call)."""
+    """int32 sync words a moe_expert_layer call needs: counters, the call epoch and the flagged h
+    copies (zero them once before the first call; torch allocations are 8-byte aligned)."""
     return int(lib().moe_layer_sync_ints(T, k, n_ff))
 
 

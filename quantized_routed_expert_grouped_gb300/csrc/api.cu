@@ -470,7 +470,9 @@ int moe_expert_grouped(const moe_expert_call* c, cudaStream_t stream) {
 
 int64_t moe_layer_sync_ints(int T, int k, int n_ff) {
     if (T <= 0 || k <= 0 || n_ff <= 0 || n_ff % 32) return 0;
-    return static_cast<int64_t>(T) * k + 2;
+    // control words, then per entry and h block the flagged copy (kHxPairs 8-byte pairs); even, so
+    // both halves of a sync pair stay 8-byte aligned
+    return kSyncHx + static_cast<int64_t>(T) * k * (n_ff / 32) * kHxPairs * 2;
 }
 
 int moe_expert_layer(const moe_layer_call* c, cudaStream_t stream) {
@@ -485,6 +487,7 @@ int moe_expert_layer(const moe_layer_call* c, cudaStream_t stream) {
     if (c->n_experts <= 0) return MOE_E_CAP;
     if (c->out_row_stride < c->n_embd) return MOE_E_SHAPE;
     if ((reinterpret_cast<uintptr_t>(c->x) | reinterpret_cast<uintptr_t>(c->gu)) & 15u) return MOE_E_ALIGN;
+    if (reinterpret_cast<uintptr_t>(c->sync) & 7u) return MOE_E_ALIGN;
     LayerArgs L = {};
     int NT = 0, smem = 0;
     if ((rc = plan_layer(c->gu_fmt.type, c->down_fmt.type, c->n_embd, c->n_ff, c->T, c->k, c->n_experts, L, NT, smem)))

@@ -399,11 +399,11 @@ __device__ __forceinline__ void load_table(const GemvArgs& a, uint32_t tab[4]) {
 // (q2[i*nb + b]); aux = exact code sum S times the format's factor (CB: S, slots: -(2 bias - 1) S),
 // s (Q4B) or 0. Row `src` < 0 stages zeros. CG: read through L2 only (rows written earlier by
 // the same launch); otherwise through the read-only path.
+template <int TYPE>
+__device__ __forceinline__ void put_staged(const GemvArgs& a, uint8_t* smem, int slot, int b, uint32_t w[9]);
+
 template <int TYPE, bool CG = false>
 __device__ __forceinline__ void stage_block(const GemvArgs& a, uint8_t* smem, int slot, int src, int b) {
-    int4* q = reinterpret_cast<int4*>(smem + a.off_actq);
-    float2* q2 = reinterpret_cast<float2*>(smem + a.off_act2);
-    const int bp = b + (b >> 3);
     uint32_t w[9];
     if (src >= 0) {
         const uint32_t* p = reinterpret_cast<const uint32_t*>(a.act + static_cast<int64_t>(src) * a.nb + b);
@@ -413,6 +413,15 @@ __device__ __forceinline__ void stage_block(const GemvArgs& a, uint8_t* smem, in
 #pragma unroll
         for (int k = 0; k < 9; ++k) w[k] = 0;
     }
+    put_staged<TYPE>(a, smem, slot, b, w);
+}
+
+// Block b of a q8_1 row held as nine words w (header, then code words) into slot `slot`.
+template <int TYPE>
+__device__ __forceinline__ void put_staged(const GemvArgs& a, uint8_t* smem, int slot, int b, uint32_t w[9]) {
+    int4* q = reinterpret_cast<int4*>(smem + a.off_actq);
+    float2* q2 = reinterpret_cast<float2*>(smem + a.off_act2);
+    const int bp = b + (b >> 3);
     if constexpr (TYPE == MOE_NL4) {
         uint32_t p[8];
         nl4_act_perm(w + 1, p);

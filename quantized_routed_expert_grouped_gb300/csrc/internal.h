@@ -72,13 +72,20 @@ struct GemvPlan {
 };
 
 // Arguments of one fused layer launch (layer.cuh).
+// The fused layer's sync array (int32 words): the exit counter, the global work-item counter and
+// the call epoch, then from word kSyncHx the flagged copy of h: per entry, nine rows (k = 0..8) of
+// one 8-byte pair per h block (low word: the block's header for k = 0, code word k - 1 otherwise;
+// high word: the writing call's flag, epoch + 1), so that a reader polls the data itself.
+constexpr int kSyncExit = 0, kSyncWork = 1, kSyncEpoch = 2, kSyncHx = 4;
+constexpr int kHxPairs = 9;  // pairs per q8_1 block
+
 struct LayerArgs {
     GemvArgs gu, dn;     // per-phase geometry and pointers (shared ring, partials, barriers, misc)
     const int32_t* ids;  // [T][k] top-k expert ids
     const float* x;      // [T][n_embd]
     moe_q8_1* hq;        // [n][F/32]: the q8_1 h rows (exchanged between the CTAs)
-    int32_t* sync;       // [n] per-group h-block counters, [1] exit counter, [1] work-item counter
-    int32_t* sync_other; // the other half of a sync pair (zeroed by this call; nullptr: no pair)
+    int32_t* sync;       // control words (kSync*) and the flagged h copy from kSyncHx (8-byte aligned)
+    int32_t* sync_other; // the other half of a sync pair (reset by this call; nullptr: no pair)
     int32_t *o_ge, *o_gs, *o_ng, *o_es, *o_ed;  // optional copies of the grouping (CTA 0)
     moe_q8_1* o_xq;                             // optional copy of the activation q8_1 (CTA 0)
     int T, k, n;         // n = T * k entries (and the capacity of every per-group table)

@@ -24,17 +24,21 @@
 //    and arrive on the slot's chunk-done barrier; an epilogue warp per unit sums the chunk
 //    partials, releases the slot, writes the gate/up rows and keeps SwiGLU(gate, up) (product
 //    rounded on its own) in its lanes, so the unit's 32 h values per entry end up one per lane: it
-//    writes their q8_1 block to hq and adds one to the group's counter (after a fence). Every h
-//    block is computed once, and no compute warp waits on an epilogue.
+//    writes their q8_1 block to hq and a flagged copy of it to the sync array (nine 8-byte pairs
+//    of a word and the call's flag, so no fence is needed: a reader takes a pair once its flag is
+//    the call's). Every h block is computed once, and no compute warp waits on an epilogue.
 //  * The activations are staged as q8_1 by every CTA (one lane quad per block).
-//  * Down chunks: the producer copies the chunk's weight tiles into free slots first, then waits
-//    (bounded) for the group's counter to reach F/32 and stages its q8_1 h rows from hq into one
-//    of two buffers (4-entry batches; a buffer is refilled once every tile that read it has been
-//    released), then publishes the tiles. A down tile holds up to nsub 32-row sub-tiles; its
+//  * Down chunks: the producer copies the chunk's weight tiles into free slots first, then polls
+//    (bounded) the flagged copies of the group's q8_1 h rows until every pair carries the call's
+//    flag, staging them into one of two buffers as they arrive (4-entry batches; a buffer is
+//    refilled once every tile that read it has been released), then publishes the tiles. The
+//    wait and the staging are one L2 round trip, and the writers issue no fence. A down tile holds up to nsub 32-row sub-tiles; its
 //    (sub-tile, 256-weight chunk) work items are dealt to the consumer warps in turn across
 //    tiles, and the last warp of a sub-tile sums its chunks and writes the output rows.
-//  * The counters live in a caller-owned int array that must be zero before the first call; the
-//    last CTA to finish (a global exit counter) zeroes them again, so every call starts clean.
+//  * The counters and the flagged h copies live in a caller-owned int array that must be zero
+//    before the first call; the last CTA to finish (a global exit counter) zeroes the counters
+//    and advances the call epoch (the flag is epoch + 1), so every call starts clean and no pair
+//    written by an earlier call carries the current flag.
 //  * Every wait (mbarriers, group counters, the ring) has a time limit; on expiry the kernel sets
 //    MOE_ERR_TIMEOUT, the producer stops, the consumers walk the published ring indices without
 //    computing, the CTA waits (bounded) for its own copies in flight and still takes part in the
@@ -50,21 +54,60 @@ namespace moe {
 constexpr int kDescRing = 16;  // tile descriptors in flight per CTA (ring indices)
 constexpr int kUnitBufs = 4;   // gate/up units in flight per CTA (h buffers in shared memory)
 
-__device__ __forceinline__ int ld_acquire(const int32_t* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// One 8-byte pair of the flagged h copy: a naturally aligned 64-bit access is single-copy
+// atomic, so a reader that sees the flag sees the word written with it.
+__device__ __forceinline__ void st_pair(uint64_t* p, uint32_t word, uint32_t flag) {
+    const uint64_t v = (static_cast<uint64_t>(flag) << 32) | word;
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_pair(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
-// Wait until *p >= target (acquire); false after kWaitLimitNs.
-__device__ __forceinline__ bool wait_count(const int32_t* p, int target) {
-    if (ld_acquire(p) >= target) return true;
-    const unsigned long long t0 = global_ns();
-    for (uint32_t it = 1;; ++it) {
-        __nanosleep(64);
-        if (ld_acquire(p) >= target) return true;
-        if ((it & 15u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+// The q8_1 h rows of entries e0 .. e0+ne-1 (ent[e].x; < 0 stages zeros) into slots slot0 ...,
+// read from their flagged copies (hx: per row kHxPairs rows of nb pairs, pair k of every block
+// side by side, so that one pair of consecutive blocks is one coalesced load across the warp): a
+// lane reads each of its blocks until all nine flags equal `flag` (between reads it polls the
+// header pair alone), then stages it. False when a block is still missing after kWaitLimitNs.
+template <int TYPE>
+__device__ __forceinline__ bool stage_flagged(const GemvArgs& a, uint8_t* smem, const int2* ent, const uint64_t* hx,
+                                              int e0, int ne, int slot0, uint32_t flag, int lane) {
+    for (int i = lane; i < ne * a.nb; i += 32) {
+        const int s = i / a.nb, b = i - s * a.nb, row = ent[e0 + s].x;
+        uint32_t w[kHxPairs];
+        if (row >= 0) {
+            const uint64_t* p = hx + static_cast<int64_t>(row) * kHxPairs * a.nb + b;
+            unsigned long long t0 = 0;
+            for (uint32_t it = 0;; ++it) {
+                uint64_t v[kHxPairs];
+#pragma unroll
+                for (int k = 0; k < kHxPairs; ++k) v[k] = ld_pair(p + k * a.nb);
+                bool ok = true;
+#pragma unroll
+                for (int k = 0; k < kHxPairs; ++k) {
+                    ok = ok && static_cast<uint32_t>(v[k] >> 32) == flag;
+                    w[k] = static_cast<uint32_t>(v[k]);
+                }
+                if (ok) break;
+                // not there yet: wait on the header pair alone (one load per poll, not nine),
+                // then read all nine again
+                if (it == 0) t0 = global_ns();
+                else if (global_ns() - t0 > kWaitLimitNs) return false;
+                for (uint32_t j = 0;; ++j) {
+                    __nanosleep(64);
+                    if (static_cast<uint32_t>(ld_pair(p) >> 32) == flag) break;
+                    if ((j & 15u) == 15u && global_ns() - t0 > kWaitLimitNs) return false;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < kHxPairs; ++k) w[k] = 0;
+        }
+        put_staged<TYPE>(a, smem, slot0 + s, b, w);
     }
+    return true;
 }
 
 // q8_1 of one 32-value block held by the 4 lanes of an aligned lane quad (quad lane j holds
@@ -259,7 +302,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     uint64_t* dread = empty + SB;         // descriptor d passed by every consumer warp
     uint64_t* ufree = dread + kDescRing;  // unit buffer u free again (its unit's h blocks written)
     uint64_t* pub = ufree + kUnitBufs;    // descriptor d published (or the stream ended there)
-    // misc: [0] ring indices published, [1] abort flag, [2] last-CTA flag, [5] no more tiles,
+    // misc: [0] ring indices published, [1] abort flag, [2] last-CTA flag, [3] the call's flag in
+    // the flagged h copies, [5] no more tiles,
     // [6] copies issued, [7] work items published, [8] work items taken, [16 + u] tiles done of the
     // gate/up unit in buffer u, [32 + s] sub-tiles done of slot s, [64 + 8s + b] chunks done of
     // (sub-)tile b of slot s, [128 + 8d ..] descriptor d of ring index q (d = q % kDescRing)
@@ -308,9 +352,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     __syncthreads();
     pdl_wait();
     pdl_trigger();
-    // a sync pair: the call that used the other half has completed; zero it for the next call
-    if (L.sync_other && blockIdx.x == 0)
-        for (int i = tid; i < n + 2; i += NT) L.sync_other[i] = 0;
+    // a sync pair: the call that used the other half has completed; reset it for the next call
+    if (L.sync_other && blockIdx.x == 0 && tid == 0) {
+        L.sync_other[kSyncExit] = 0;
+        L.sync_other[kSyncWork] = 0;
+        L.sync_other[kSyncEpoch] += 1;
+    }
+    uint64_t* hx = reinterpret_cast<uint64_t*>(L.sync + kSyncHx);
 
     // ---- routing/grouping and tables: one warp when n <= 32, else the whole CTA routes and
     // warp 0 builds the tables
@@ -320,7 +368,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         __syncthreads();
     }
     int early = 0;  // ring indices of the CTA's first item copied before the tables (warp 0, lane 0)
+    // this call's flag in the flagged h copies (the pairs of every earlier call carry a smaller
+    // one): read once per CTA, handed to the consumer warps with the tables
+    uint32_t flag = 0;
     if (warp == 0) {
+        if (lane == 0) flag = 1u + static_cast<uint32_t>(__ldcg(L.sync + kSyncEpoch));
         if (n <= 32) route_warp(L.ids, n, L.k, A.n_experts, rgx, rgs, rng, rsrc, rdst, A.err, blockIdx.x == 0, lane);
         __syncwarp();
         // The CTA's first work item is its own index. When that is a gate/up unit, its first tile
@@ -349,6 +401,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
             }
         }
         build_tables<GT, DT>(L, pcA, pcD, rgx, rgs, rng, rsrc, rdst, giA, giD, entA, entD, misc, lane);
+        if (lane == 0) misc[3] = static_cast<int>(flag);
+        flag = __shfl_sync(0xffffffffu, flag, 0);
         __threadfence_block();
         bar_arrive(3, NT);  // tables ready
     } else {
@@ -387,9 +441,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
             }
         }
         named_sync(3, NT);  // with warp 0's arrival: tables ready, activations staged
+        flag = static_cast<uint32_t>(vmisc[3]);
     }
     const int G = *rng;
-    const int32_t* ready = L.sync;  // per group: h blocks written (complete at F/32)
     // ---- one stream of work items for the whole grid, taken in order from a global counter:
     // gate/up units (group-major), then down chunks of dchunk tiles of one group (group-major).
     // Each CTA's producer warp pulls items and streams their tiles through the ring, publishing a
@@ -405,7 +459,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     dchunk = dchunk < 1 ? 1 : dchunk > 3 ? 3 : dchunk;
     const int nunits = G * upg, cpg = (tpg + dchunk - 1) / dchunk;
     const int nitems = nunits + G * cpg;
-    int* work = L.sync + n + 1;  // global item counter
+    int* work = L.sync + kSyncWork;  // global item counter
     // per ring index q (d = q % kDescRing): [8d] kind (0 gate/up, 1 down), [8d+1] group,
     // [8d+2] jb or first row, [8d+3] h or rows, [8d+4] first entry, [8d+5] entries (<= 4),
     // [8d+6] gate/up: the CTA's unit number, down: first staging slot, [8d+7] first work item
@@ -511,7 +565,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 const GroupInfo gr = giD[g];
                 if (gr.cost == 0) continue;
                 const int t0 = c * dchunk, t1 = t0 + dchunk < tpg ? t0 + dchunk : tpg;
-                const int nbat = (gr.e1 - gr.e0 + kMaxEntriesPerPass - 1) / kMaxEntriesPerPass;
                 auto tile_src = [&](int t, uint32_t& bytes) {
                     const int row0 = t * RTD, nrows = D.rows - row0 < RTD ? D.rows - row0 : RTD;
                     bytes = static_cast<uint32_t>(nrows) * static_cast<uint32_t>(D.row_bytes);
@@ -539,9 +592,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                             st_last = issued;
                         }
                         ok = __shfl_sync(0xffffffffu, ok, 0);
-                        // h rows of group g complete (every 4-entry batch of every unit): every lane
-                        // polls the counter itself, so its own acquire orders its staging loads
-                        ok = __all_sync(0xffffffffu, ok && !vmisc[1] && wait_count(ready + g, upg * nbat));
+                        // the batch's h rows, each block staged as soon as its flagged copy is
+                        // complete (every unit of the group writes one block per entry)
+                        ok = __all_sync(0xffffffffu, ok && !vmisc[1] &&
+                                                         stage_flagged<DT>(D, smem, entD, hx, b0, ne,
+                                                                           kMaxEntriesPerPass * (st_n & 1), flag, lane));
                         if (!ok) {
                             if (lane == 0) {
                                 if (!vmisc[1]) set_err(A.err, MOE_ERR_TIMEOUT);
@@ -550,8 +605,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                             stop = true;
                             break;
                         }
-                        stage_entries<DT, true>(D, smem, entD, b0, ne, kMaxEntriesPerPass * (st_n & 1), lane, 32);
-                        __syncwarp();
+                        __syncwarp();  // every lane's staged blocks before lane 0 publishes
                         st_g = g;
                         st_b0 = b0;
                         ++st_n;
@@ -686,20 +740,31 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 }
                 __syncwarp();
                 __threadfence_block();
-                // the unit's last tile: q8_1 of its h blocks (one value per lane), the group's counter,
-                // the unit buffer free again
+                // the unit's last tile: q8_1 of its h blocks (one value per lane) to hq and to the
+                // flagged copy (pair 0 the header, pair 1 + w code word w = lanes 4w .. 4w+3), the
+                // unit buffer free again
                 int done = 0;
                 if (lane == 0) done = atomicAdd(&misc[16 + u], 1) == tpu - 1;
                 done = __shfl_sync(0xffffffffu, done, 0);
                 if (!done) continue;
                 __threadfence_block();
-                for (int e = 0; e < ne; ++e)
-                    warp_q8_1(ub[e * 32 + lane], L.hq + static_cast<int64_t>(e0 + e) * L.nbj + jb, lane);
+                for (int e = 0; e < ne; ++e) {
+                    uint32_t hdr;
+                    int Ssum;
+                    const int qv = warp_q8_1_code(ub[e * 32 + lane], hdr, Ssum);
+                    moe_q8_1* dst = L.hq + static_cast<int64_t>(e0 + e) * L.nbj + jb;
+                    dst->q[lane] = static_cast<int8_t>(qv);
+                    if (lane == 0) *reinterpret_cast<uint32_t*>(dst) = hdr;
+                    uint32_t cw = (static_cast<uint32_t>(qv) & 0xFFu) << (8 * (lane & 3));
+                    cw |= __shfl_xor_sync(0xffffffffu, cw, 1);
+                    cw |= __shfl_xor_sync(0xffffffffu, cw, 2);
+                    cw = __shfl_sync(0xffffffffu, cw, lane >= 1 && lane < kHxPairs ? 4 * (lane - 1) : 0);
+                    if (lane < kHxPairs)
+                        st_pair(hx + (static_cast<int64_t>(e0 + e) * kHxPairs + lane) * L.nbj + jb, lane == 0 ? hdr : cw, flag);
+                }
                 __syncwarp();
                 if (lane == 0) {
                     misc[16 + u] = 0;
-                    __threadfence();
-                    atomicAdd(L.sync + g, 1);
                     mbar_arrive(&ufree[u]);
                 }
             } else {
@@ -740,17 +805,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         for (int qq = nq - S > 0 ? nq - S : 0; qq < nq; ++qq)
             mbar_wait_bounded(&full[qq % S], static_cast<uint32_t>(qq / S) & 1u);
     }
-    // ---- exit count; the last CTA zeroes the counters for the next call (with a sync pair, the
-    // next call zeroes them instead)
+    // ---- exit count; the last CTA zeroes the counters and advances the epoch for the next call
+    // (with a sync pair, the next call does that instead)
     if (L.sync_other) return;
     if (tid == 0) {
         __threadfence();
-        misc[2] = atomicAdd(L.sync + n, 1) == static_cast<int>(gridDim.x) - 1;
+        misc[2] = atomicAdd(L.sync + kSyncExit, 1) == static_cast<int>(gridDim.x) - 1;
     }
     __syncthreads();
-    if (misc[2]) {
+    if (misc[2] && tid == 0) {
         __threadfence();
-        for (int i = tid; i <= n + 1; i += NT) L.sync[i] = 0;
+        L.sync[kSyncExit] = 0;
+        L.sync[kSyncWork] = 0;
+        L.sync[kSyncEpoch] += 1;
     }
 }
 

@@ -81,7 +81,8 @@ def test_layer_call_host_errors(m):
     L = m.lib()
     W = m.WFmt
     d = 16
-    assert m.layer_sync_ints(4, 8, 768) == 32 + 2
+    # control words + per entry (32) and h block (24) nine 8-byte pairs
+    assert m.layer_sync_ints(4, 8, 768) == 4 + 32 * 24 * 9 * 2
     assert m.layer_sync_ints(0, 8, 768) == 0
 
     def call(**kw):
@@ -101,4 +102,5 @@ def test_layer_call_host_errors(m):
     assert call(T=40, k=2) == -4                                 # 40 activation rows exceed the staging budget
     assert call(out_row_stride=100) == -3
     assert call(n_experts=0) == -4
+    assert call(sync=d + 4) == -6                                 # sync holds 8-byte pairs
 

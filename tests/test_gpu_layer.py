@@ -27,6 +27,13 @@ CASE_IDS = [f"{c[0]}-{synth.NAMES[c[1][0]]}-{synth.NAMES[c[1][1]]}-T{c[2]}" + (f
             for c in CASES]
 
 
+def _left_clean(sync, calls):
+    """The control words a call leaves: exit and work counters zero, the epoch advanced once per
+    call (the flagged h copies after them keep the last call's flag)."""
+    exit_, work, epoch = (int(v) for v in sync[:3].tolist())
+    assert (exit_, work, epoch) == (0, 0, calls)
+
+
 @pytest.fixture(scope="module")
 def m():
     import quantized_routed_expert_grouped_gb300 as mod
@@ -95,7 +102,7 @@ def test_layer_equals_separate_steps_and_oracle(m, orc, wname, pair, T, xt):
     torch.cuda.synchronize()
     assert int(F.err.item()) == 0 and int(B.err.item()) == 0
     _same_as_separate(F, B, n)
-    assert not F.sync.any(), "counters must be left zero"
+    _left_clean(F.sync, 1)
     ref = H.oracle_call(orc, L0)
     flips, scale_diffs = H.q8_1_code_flips(F.hq.cpu().numpy(), ref["hq"])
     assert flips <= max(2, n * wl.F // 4096) and scale_diffs <= 2, (flips, scale_diffs)
@@ -105,8 +112,9 @@ def test_layer_equals_separate_steps_and_oracle(m, orc, wname, pair, T, xt):
 
 
 def test_layer_repeated_calls_pdl_and_graph(m, orc):
-    """Several layers sharing one counter array, eager (with and without PDL) and captured in a
-    CUDA graph replayed twice: identical outputs every time, counters left zero."""
+    """Several layers sharing one sync array, eager (with and without PDL) and captured in a CUDA
+    graph replayed twice: identical outputs every time, counters left zero and the epoch advanced
+    once per call (18 calls)."""
     wl = synth.WORKLOADS["window48"]
     layers = [H.transcoded(m, H.make_layer(wl, (synth.CB3, synth.NL4), 3, layer=l), synth.CB3X) for l in range(3)]
     fs = [Fused(m, L) for L in layers]
@@ -146,14 +154,14 @@ def test_layer_repeated_calls_pdl_and_graph(m, orc):
         for f, b in zip(fs, base):
             assert torch.equal(f.out.view(torch.int32), b.view(torch.int32))
     assert all(int(f.err.item()) == 0 for f in fs)
-    assert not sync.any()
+    _left_clean(sync, 18)
 
 
 def test_layer_sync_pair_alternating_halves(m, orc):
-    """MOE_F_SYNC_PAIR: four layers at T = 4 alternate the two halves of one counter array (each
-    call zeroes the other half instead of its last CTA zeroing its own), eager with PDL and in a
-    CUDA graph replayed twice: the outputs equal the default mode's bit for bit, and after every
-    call the half the next call uses is zero."""
+    """MOE_F_SYNC_PAIR: four layers at T = 4 alternate the two halves of one sync array (each call
+    resets the other half instead of its last CTA resetting its own), eager with PDL and in a CUDA
+    graph replayed twice: the outputs equal the default mode's bit for bit, and after every call
+    the half the next call uses has zero counters and its epoch advanced once per reset."""
     wl = synth.WORKLOADS["window48"]
     layers = [H.transcoded(m, H.make_layer(wl, (synth.CB3, synth.NL4), 4, layer=l), synth.CB3X) for l in range(4)]
     base = []
@@ -169,11 +177,11 @@ def test_layer_sync_pair_alternating_halves(m, orc):
     for i, f in enumerate(fs):
         f.call.c.sync = pair.data_ptr()
         f.call.c.flags = m.F_PDL | m.F_SYNC_PAIR | (m.F_SYNC_ODD if i % 2 else 0)
-    for i, f in enumerate(fs):  # one at a time: the next call's half is zero after each
+    for i, f in enumerate(fs):  # one at a time: the next call's half is reset after each
         f.call()
         torch.cuda.synchronize()
         nxt = pair[half:] if i % 2 == 0 else pair[:half]
-        assert not nxt.any()
+        _left_clean(nxt, i // 2 + 1)
     for f, b in zip(fs, base):
         assert int(f.err.item()) == 0
         assert torch.equal(f.out.view(torch.int32), b.view(torch.int32))
@@ -181,14 +189,14 @@ def test_layer_sync_pair_alternating_halves(m, orc):
     with torch.cuda.graph(g, capture_error_mode="relaxed"):
         for f in fs:
             f.call()
-    for _ in range(2):
+    for r in range(2):
         for f in fs:
             f.out.fill_(float("nan"))
         g.replay()
         torch.cuda.synchronize()
         for f, b in zip(fs, base):
             assert torch.equal(f.out.view(torch.int32), b.view(torch.int32))
-        assert not pair[:half].any()  # the last call (odd) zeroed the first half
+        _left_clean(pair[:half], 4 + 2 * r)  # reset by every odd call: two per pass
     assert all(int(f.err.item()) == 0 for f in fs)
 
 
@@ -203,7 +211,7 @@ def test_layer_dropped_ids_and_empty(m, orc):
     F.call()
     torch.cuda.synchronize()
     assert int(F.err.item()) == 128  # MOE_ERR_ROUTE only
-    assert not F.sync.any()
+    _left_clean(F.sync, 1)
     # the separate path on the same ids
     Ld = H.Layer(**{**L.__dict__, "ids": ids})
     B = _separate(m, Ld)
@@ -219,7 +227,8 @@ def test_layer_dropped_ids_and_empty(m, orc):
     torch.cuda.synchronize()
     assert int(F2.err.item()) == 128 and int(F2.ng.item()) == 0
     assert torch.isnan(F2.out).all() and torch.isnan(F2.gu).all() and (F2.hq == 0xA5).all()
-    assert not F2.sync.any()
+    _left_clean(F2.sync, 1)
+    assert not F2.sync[4:].any()  # no h block written
 
 
 def test_layer_misaligned_expert_is_skipped(m, orc):
@@ -236,7 +245,7 @@ def test_layer_misaligned_expert_is_skipped(m, orc):
     F.call()
     torch.cuda.synchronize()
     assert int(F.err.item()) == 16
-    assert not F.sync.any()
+    _left_clean(F.sync, 1)
     out, ref = F.out.cpu().numpy(), B.out.cpu().numpy()
     for t in range(L.T):
         for s in range(wl.k):
