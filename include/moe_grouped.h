@@ -262,7 +262,7 @@ int moe_expert_grouped_static(const moe_expert_call* call, cudaStream_t stream);
  *    q8_1, for inspection.
  *  - x and gu must be 16-byte aligned, sync 8-byte aligned (else MOE_E_ALIGN).
  *  - Formats: any gate/up format; down MOE_NL4 or MOE_Q8_0 (else MOE_E_TYPE).
- *  - Limits: T*k <= 512 and the T activation rows staged in shared memory (44 bytes per 32
+ *  - Limits: 0 < n_experts <= 2^26, T*k <= 512 and the T activation rows staged in shared memory (44 bytes per 32
  *    values, padded) must fit 64 KB (e.g. T <= 18 at n_embd 2560), else MOE_E_CAP; 32 rows of
  *    either blob must fit 96 KB, else MOE_E_SHAPE.
  *  - The launch's CTAs wait on one another (bounded, ~1 s, then MOE_ERR_TIMEOUT); the grid never

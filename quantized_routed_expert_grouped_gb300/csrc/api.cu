@@ -484,7 +484,7 @@ int moe_expert_layer(const moe_layer_call* c, cudaStream_t stream) {
     if (!c->w_gu || !c->w_down || !c->topk_ids || !c->x || !c->out || !c->gu || !c->hq || !c->sync)
         return MOE_E_NULL;
     if (c->T <= 0 || c->k <= 0) return MOE_E_SHAPE;
-    if (c->n_experts <= 0) return MOE_E_CAP;
+    if (c->n_experts <= 0 || c->n_experts > (1 << 26)) return MOE_E_CAP;  // routing keys: id << 5 | lane
     if (c->out_row_stride < c->n_embd) return MOE_E_SHAPE;
     if ((reinterpret_cast<uintptr_t>(c->x) | reinterpret_cast<uintptr_t>(c->gu)) & 15u) return MOE_E_ALIGN;
     if (reinterpret_cast<uintptr_t>(c->sync) & 7u) return MOE_E_ALIGN;

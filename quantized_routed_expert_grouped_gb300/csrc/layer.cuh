@@ -7,7 +7,8 @@
 // arithmetic in the same order, so its outputs equal the separate kernels' bit for bit.
 //
 // How (GB300 design):
-//  * Every CTA groups the window's top-k ids itself (one warp: ballots and shuffles when T*k <= 32);
+//  * Every CTA groups the window's top-k ids itself (one warp: a bitonic sort of (id, lane) keys
+//    across the warp when T*k <= 32);
 //    CTA 0 also writes the grouping and the activation q8_1 rows to global memory for inspection.
 //    The expert pointer tables, like the codebooks, are read before the dependency wait.
 //  * One stream of work items for the whole grid, pulled in order from a global counter: first
@@ -181,8 +182,10 @@ __device__ __forceinline__ void put_quad(moe_q8_1* dst, int j, const uint32_t w[
 }
 
 // Routing/grouping of n <= 32 ids by one warp (lane i owns id i): the same grouping as route_cta
-// (groups by ascending expert id, entries by ascending (t, slot), numbered from 0), from ballots and
-// shuffles. Writes grp_expert, grp_start (G+1), *n_groups, ent_src, ent_dst (shared memory).
+// (groups by ascending expert id, entries by ascending (t, slot), numbered from 0). The keys
+// (id << 5 | lane; invalid ids last) are sorted across the warp by a bitonic network (15
+// compare-exchange steps), so lane r holds the entry of rank r; a group starts where the id
+// changes. Writes grp_expert, grp_start (G+1), *n_groups, ent_src, ent_dst (shared memory).
 __device__ __forceinline__ void route_warp(const int32_t* ids, int n, int k, int n_experts, int* rgx, int* rgs, int* rng,
                                            int* rsrc, int* rdst, int32_t* err, bool report, int lane) {
     int v = -1;
@@ -193,30 +196,34 @@ __device__ __forceinline__ void route_warp(const int32_t* ids, int n, int k, int
             v = -1;
         }
     }
-    const bool valid = v >= 0;
-    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-    const unsigned same = __match_any_sync(0xffffffffu, v);
-    const bool first = valid && __ffs(same) - 1 == lane;
-    const unsigned fmask = __ballot_sync(0xffffffffu, first);
-    int rank = 0, grp = 0;
+    const int nv = __popc(__ballot_sync(0xffffffffu, v >= 0));
+    uint32_t key = v >= 0 ? (static_cast<uint32_t>(v) << 5) | static_cast<uint32_t>(lane) : 0xFFFFFFFFu;
 #pragma unroll
-    for (int jl = 0; jl < 32; ++jl) {
-        const int vj = __shfl_sync(0xffffffffu, v, jl);
-        const bool lt = vj >= 0 && vj < v;
-        rank += lt || (vj == v && jl < lane);
-        grp += lt && ((fmask >> jl) & 1u);
-    }
-    if (valid) {
-        rsrc[rank] = lane / k;
-        rdst[rank] = lane;
-        if (first) {
-            rgx[grp] = v;
-            rgs[grp] = rank;
+    for (int kk = 2; kk <= 32; kk <<= 1)
+#pragma unroll
+        for (int j = kk >> 1; j > 0; j >>= 1) {
+            const uint32_t other = __shfl_xor_sync(0xffffffffu, key, j);
+            // ascending within blocks whose kk bit is clear, descending otherwise (all ascending
+            // at kk = 32); the lower lane of a pair keeps the smaller key in an ascending block
+            const bool keep_min = ((lane & kk) == 0) == ((lane & j) == 0);
+            key = keep_min ? min(key, other) : max(key, other);
+        }
+    const int ex = static_cast<int>(key >> 5), src = static_cast<int>(key & 31u);
+    const int prev = __shfl_up_sync(0xffffffffu, ex, 1);
+    const bool start = lane < nv && (lane == 0 || prev != ex);
+    const unsigned smask = __ballot_sync(0xffffffffu, start);
+    if (lane < nv) {
+        rsrc[lane] = src / k;
+        rdst[lane] = src;
+        if (start) {
+            const int grp = __popc(smask & ((1u << lane) - 1u));
+            rgx[grp] = ex;
+            rgs[grp] = lane;
         }
     }
     if (lane == 0) {
-        rgs[__popc(fmask)] = __popc(vmask);
-        *rng = __popc(fmask);
+        rgs[__popc(smask)] = nv;
+        *rng = __popc(smask);
     }
 }
 

@@ -101,6 +101,6 @@ def test_layer_call_host_errors(m):
     assert call(T=65) == -4                                      # T*k > 512
     assert call(T=40, k=2) == -4                                 # 40 activation rows exceed the staging budget
     assert call(out_row_stride=100) == -3
-    assert call(n_experts=0) == -4
+    assert call(n_experts=0) == -4 and call(n_experts=(1 << 26) + 1) == -4
     assert call(sync=d + 4) == -6                                 # sync holds 8-byte pairs
 
