@@ -40,7 +40,7 @@
 //    before the first call; the last CTA to finish (a global exit counter) zeroes the counters
 //    and advances the call epoch (the flag is epoch + 1), so every call starts clean and no pair
 //    written by an earlier call carries the current flag.
-//  * Every wait (mbarriers, group counters, the ring) has a time limit; on expiry the kernel sets
+//  * Every wait (mbarriers, the flagged h copies, the ring) has a time limit; on expiry the kernel sets
 //    MOE_ERR_TIMEOUT, the producer stops, the consumers walk the published ring indices without
 //    computing, the CTA waits (bounded) for its own copies in flight and still takes part in the
 //    exit count.
