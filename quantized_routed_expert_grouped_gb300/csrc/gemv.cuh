@@ -397,18 +397,17 @@ __device__ __forceinline__ void load_table(const GemvArgs& a, uint32_t tab[4]) {
 // Staged activations: slot i of the shared-memory act region holds one q8_1 row as 16-byte code
 // halves (q[(i*2 + h)*nbp + bp], bp = b + b/8: conflict-free 128-bit loads) and (d, aux) pairs
 // (q2[i*nb + b]); aux = exact code sum S times the format's factor (CB: S, slots: -(2 bias - 1) S),
-// s (Q4B) or 0. Row `src` < 0 stages zeros. CG: read through L2 only (rows written earlier by
-// the same launch); otherwise through the read-only path.
+// s (Q4B) or 0. Row `src` < 0 stages zeros; rows are read through the read-only path.
 template <int TYPE>
 __device__ __forceinline__ void put_staged(const GemvArgs& a, uint8_t* smem, int slot, int b, uint32_t w[9]);
 
-template <int TYPE, bool CG = false>
+template <int TYPE>
 __device__ __forceinline__ void stage_block(const GemvArgs& a, uint8_t* smem, int slot, int src, int b) {
     uint32_t w[9];
     if (src >= 0) {
         const uint32_t* p = reinterpret_cast<const uint32_t*>(a.act + static_cast<int64_t>(src) * a.nb + b);
 #pragma unroll
-        for (int k = 0; k < 9; ++k) w[k] = CG ? __ldcg(p + k) : __ldg(p + k);
+        for (int k = 0; k < 9; ++k) w[k] = __ldg(p + k);
     } else {
 #pragma unroll
         for (int k = 0; k < 9; ++k) w[k] = 0;
@@ -454,12 +453,12 @@ __device__ __forceinline__ void stage_all(const GemvArgs& a, uint8_t* smem, int 
 }
 
 // The activation rows of entries e0 .. e0+ne-1 (ent[e].x, -1 when invalid) into slots slot0 ...
-template <int TYPE, bool CG = false>
+template <int TYPE>
 __device__ __forceinline__ void stage_entries(const GemvArgs& a, uint8_t* smem, const int2* ent, int e0, int ne,
                                               int slot0, int t, int nt) {
     for (int i = t; i < ne * a.nb; i += nt) {
         const int s = i / a.nb;
-        stage_block<TYPE, CG>(a, smem, slot0 + s, ent[e0 + s].x, i - s * a.nb);
+        stage_block<TYPE>(a, smem, slot0 + s, ent[e0 + s].x, i - s * a.nb);
     }
 }
 

@@ -265,11 +265,6 @@ __device__ __forceinline__ void build_tables(const LayerArgs& L, const uint8_t* 
     __syncwarp();
 }
 
-// `count` arrivals at once on a shared-memory mbarrier.
-__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
 __device__ __forceinline__ void bar_arrive(int id, int threads) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

@@ -70,31 +70,6 @@ __device__ __forceinline__ int warp_q8_1_code(float v, uint32_t& hdr, int& S) {
     return q;
 }
 
-// The same q8_1 block computed by one thread holding all 32 values: code words w[k] = codes
-// 4k .. 4k+3 (little-endian bytes), header d16 | s16 << 16, exact code sum S. The maximum, the
-// divides and the rounding are the warp version's, so both give the same bytes.
-__device__ __forceinline__ void thread_q8_1(const float v[32], uint32_t w[8], uint32_t& hdr, int& S) {
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    const float d = __fdiv_rn(amax, 127.0f);
-    S = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int q = d == 0.0f ? 0 : static_cast<int>(roundf(__fdiv_rn(v[4 * k + b], d)));
-            S += q;
-            word |= (static_cast<uint32_t>(q) & 0xffu) << (8 * b);
-        }
-        w[k] = word;
-    }
-    const uint32_t d16 = __half_as_ushort(__float2half_rn(d));
-    const uint32_t s16 = __half_as_ushort(__float2half_rn(__fmul_rn(d, static_cast<float>(S))));
-    hdr = d16 | (s16 << 16);
-}
-
 // Quantize the warp's 32 values (lane i holds v) into one q8_1 block at dst.
 __device__ __forceinline__ void warp_q8_1(float v, moe_q8_1* dst, int lane) {
     uint32_t hdr;
