@@ -345,7 +345,7 @@ def run_ours(args, rank, world):
 # capture summarised in profiles/layer_kernel_window48_T4.md; reported only while the kernel
 # sources hash to the ones the capture was taken on (else null: the counters are stale).
 LAYER_TRAFFIC_T4 = {"bytes": 95_377_920, "sources": ("layer.cuh", "gemv.cuh", "common.cuh", "q8_1.cuh", "route.cuh"),
-                    "sha1": "97d4b52e03726e0590f6e246cb6b158181bdb815"}
+                    "sha1": "c27b16b12f9fbbf15bcea37752a3e5fbaf94adf7"}
 
 
 def layer_traffic():

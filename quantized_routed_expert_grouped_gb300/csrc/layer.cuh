@@ -33,17 +33,18 @@
 //    (bounded) the flagged copies of the group's q8_1 h rows until every pair carries the call's
 //    flag, staging them into one of two buffers as they arrive (4-entry batches; a buffer is
 //    refilled once every tile that read it has been released), then publishes the tiles. The
-//    wait and the staging are one L2 round trip, and the writers issue no fence. A down tile holds up to nsub 32-row sub-tiles; its
-//    (sub-tile, 256-weight chunk) work items are dealt to the consumer warps in turn across
-//    tiles, and the last warp of a sub-tile sums its chunks and writes the output rows.
+//    wait and the staging are one L2 round trip, and the writers issue no fence. A down tile
+//    holds up to nsub 32-row sub-tiles; its (sub-tile, 256-weight chunk) work items are dealt to
+//    the consumer warps in turn across tiles, and the last warp of a sub-tile sums its chunks
+//    and writes the output rows.
 //  * The counters and the flagged h copies live in a caller-owned int array that must be zero
 //    before the first call; the last CTA to finish (a global exit counter) zeroes the counters
 //    and advances the call epoch (the flag is epoch + 1), so every call starts clean and no pair
 //    written by an earlier call carries the current flag.
-//  * Every wait (mbarriers, the flagged h copies, the ring) has a time limit; on expiry the kernel sets
-//    MOE_ERR_TIMEOUT, the producer stops, the consumers walk the published ring indices without
-//    computing, the CTA waits (bounded) for its own copies in flight and still takes part in the
-//    exit count.
+//  * Every wait (mbarriers, the flagged h copies, the ring) has a time limit; on expiry the kernel
+//    sets MOE_ERR_TIMEOUT, the producer stops, the consumers walk the published ring indices
+//    without computing, the CTA waits (bounded) for its own copies in flight and still takes part
+//    in the exit count.
 #pragma once
 
 #include "gemv.cuh"
