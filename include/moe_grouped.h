@@ -249,7 +249,8 @@ int moe_expert_grouped_static(const moe_expert_call* call, cudaStream_t stream);
  *    the down phase polls instead of a counter, so the gate/up side needs no fence. The caller
  *    zeroes the array once before the first call (e.g. cudaMemsetAsync); every call leaves words
  *    0 and 1 zero and advances the epoch, so no pair left by an earlier call carries the next
- *    call's flag. A call that reported MOE_ERR_TIMEOUT may leave the array inconsistent: zero it
+ *    call's flag. The epoch is 32 bits: zero the array again at least every 2^32 - 2 calls on it
+ *    (after that many the flag would wrap to 0, the value of a pair never written). A call that reported MOE_ERR_TIMEOUT may leave the array inconsistent: zero it
  *    again. Calls that may overlap on the GPU need separate sync arrays (and scratch).
  *    With MOE_F_SYNC_PAIR in flags, sync holds two halves of moe_layer_sync_ints words: the call
  *    uses the first half (the second with MOE_F_SYNC_ODD) and resets the other one (zero counters,
