@@ -73,6 +73,7 @@ def _setup(lib):
     lib.orc_router_topk.restype = _I
     lib.orc_combine.argtypes = [_P, _I64, _P, _P, _I, _I, _I, _I, _P]
     lib.orc_route_group.restype = _I
+    lib.orc_qsa_block_scores.argtypes = [_P, _I, _P, _P, _I64, _P]
     return lib
 
 
@@ -216,6 +217,18 @@ class Oracle:
         y = np.zeros((T, out.shape[1]), np.float64)
         self.lib.orc_combine(_ptr(out), out.shape[1], _ptr(ids), _ptr(w), T, k, int(n_experts), out.shape[1], _ptr(y))
         return y
+
+    def qsa_block_scores(self, q, keys, scale):
+        """q fp32 [T, 4, 128]; keys int8 [n_blocks, 128]; scale fp32 [n_blocks] -> scores fp32
+        [T, n_blocks] (QSA decode block scores, the tail block + 1e9)."""
+        q = np.ascontiguousarray(q, dtype=np.float32)
+        keys = np.ascontiguousarray(keys, dtype=np.int8)
+        scale = np.ascontiguousarray(scale, dtype=np.float32)
+        T = q.shape[0]
+        assert q.shape[1:] == (4, 128) and keys.shape[1] == 128 and scale.shape == (keys.shape[0],)
+        out = np.zeros((T, keys.shape[0]), np.float32)
+        self.lib.orc_qsa_block_scores(_ptr(q), T, _ptr(keys), _ptr(scale), keys.shape[0], _ptr(out))
+        return out
 
     def route_group(self, topk_ids, n_experts, entry_base=0, cap_entries=None):
         ids = np.ascontiguousarray(topk_ids, dtype=np.int32)

@@ -497,3 +497,71 @@ void orc_combine(const float* out, int64_t out_stride, const int32_t* topk_ids, 
         }
     }
 }
+
+/* ------------------------------------------------------------------ QSA decode block scores */
+
+/* #2059 "QSA decode: the window's block scores with the queries in registers and six shuffles
+ * per block", "What changed" and "Bit for bit": the queries' head slices sit 4 floats per lane
+ * of a warp, a head's lane products are reduced with the warp sum's pairings (xor 16, 8, 4, 2,
+ * 1), the relus of the heads are summed in head order, and the tail block gets +1e9. The
+ * arithmetic is fp32 (this file is built without contraction: fmaf below is the one fused step,
+ * named on purpose). */
+static float qsa_lane_partial(const float* qh, const int8_t* kb, int lane) {
+#ifdef ORC_PLANT_QSA_LANE_INTERLEAVE
+    const int d[4] = {lane, lane + 32, lane + 64, lane + 96};
+#else
+    const int d[4] = {4 * lane, 4 * lane + 1, 4 * lane + 2, 4 * lane + 3};
+#endif
+#ifdef ORC_PLANT_QSA_NO_FMA
+    float p = qh[d[0]] * (float)kb[d[0]];
+    for (int i = 1; i < 4; ++i) p = p + qh[d[i]] * (float)kb[d[i]];
+#else
+    float p = qh[d[0]] * (float)kb[d[0]];
+    for (int i = 1; i < 4; ++i) p = fmaf(qh[d[i]], (float)kb[d[i]], p);
+#endif
+    return p;
+}
+
+static float qsa_head_dot(const float* qh, const int8_t* kb) {
+    float v[ORC_QSA_LANES];
+    for (int l = 0; l < ORC_QSA_LANES; ++l) v[l] = qsa_lane_partial(qh, kb, l);
+#ifdef ORC_PLANT_QSA_TREE_SEQ
+    float s = v[0];
+    for (int l = 1; l < ORC_QSA_LANES; ++l) s = s + v[l];
+    return s;
+#else
+    /* level j replaces every lane's value by its own plus lane (l xor j)'s; after level 1 every
+     * lane holds the same sum */
+    for (int j = ORC_QSA_LANES / 2; j >= 1; j /= 2) {
+        float w[ORC_QSA_LANES];
+        for (int l = 0; l < ORC_QSA_LANES; ++l) w[l] = v[l] + v[l ^ j];
+        memcpy(v, w, sizeof v);
+    }
+    return v[0];
+#endif
+}
+
+void orc_qsa_block_scores(const float* q, int T, const int8_t* keys, const float* scale, int64_t n_blocks,
+                          float* scores) {
+    for (int t = 0; t < T; ++t) {
+        for (int64_t b = 0; b < n_blocks; ++b) {
+            const int8_t* kb = keys + b * ORC_QSA_DIM;
+            float r[ORC_QSA_HEADS];
+            for (int h = 0; h < ORC_QSA_HEADS; ++h) {
+                const float s = qsa_head_dot(q + ((int64_t)t * ORC_QSA_HEADS + h) * ORC_QSA_DIM, kb) * scale[b];
+                r[h] = s > 0.0f ? s : 0.0f;
+            }
+#ifdef ORC_PLANT_QSA_HEAD_ORDER
+            float sc = ((r[3] + r[2]) + r[1]) + r[0];
+#else
+            float sc = ((r[0] + r[1]) + r[2]) + r[3];
+#endif
+#ifdef ORC_PLANT_QSA_TAIL_FIRST
+            if (b == 0) sc = sc + 1e9f;
+#else
+            if (b == n_blocks - 1) sc = sc + 1e9f;
+#endif
+            scores[(int64_t)t * n_blocks + b] = sc;
+        }
+    }
+}

@@ -110,6 +110,20 @@ int orc_router_topk(const float* logits, int T, int E, int k, int32_t* topk_ids,
 void orc_combine(const float* out, int64_t out_stride, const int32_t* topk_ids, const double* weights, int T,
                  int k, int E, int n_embd, double* y);
 
+/* QSA decode block scores (#2059 "QSA decode: the window's block scores with the queries in
+ * registers and six shuffles per block"): queries q[T][4 heads][128] fp32, one pooled key per
+ * block, keys[n_blocks][128] int8 with an fp32 scale[n_blocks] (> 0). For query t and block b,
+ * head h: lane l (0..31) takes the slice 4l..4l+3, p_l = q0*k0, then p_l = fma(q_i, k_i, p_l)
+ * for i = 1, 2, 3 (k exact in fp32); the 32 partials are summed with the warp sum's pairings
+ * (level j = 16, 8, 4, 2, 1: p_l <- p_l + p_(l xor j)); r_h = max(dot_h * scale_b, 0);
+ * scores[t][b] = ((r_0 + r_1) + r_2) + r_3, plus 1e9 for the tail block b = n_blocks - 1.
+ * All fp32, one rounding per operation. */
+#define ORC_QSA_HEADS 4
+#define ORC_QSA_DIM 128
+#define ORC_QSA_LANES 32
+void orc_qsa_block_scores(const float* q, int T, const int8_t* keys, const float* scale, int64_t n_blocks,
+                          float* scores);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,6 +22,10 @@ What pins what:
   combine       -> one-hot weights read out one row, identical rows give the row times the weight
                    sum, a hand-worked 2-token example, dropped ids skipped
   grouped steps -> permutation invariants and untouched rows
+  QSA scores    -> hand-worked blocks whose exact fp32 values pin each step's order (the fused
+                   in-lane products, 4 consecutive dims per lane, the warp-sum pairings, the head
+                   order, relu after the scale, +1e9 on the tail only), and fp64 brute force within
+                   a stated rounding bound; queries and non-tail blocks independent
 """
 from __future__ import annotations
 
@@ -470,6 +474,70 @@ def check_combine(o):
     assert y.tolist() == [[0.25, 0.5], [3.5, 4.0]], y
 
 
-ALL_CHECKS = [check_router, check_combine, check_f16, check_exp, check_silu, check_q8_1, check_formats_hand, check_formats_onehot,
+# ------------------------------------------------------------------ QSA block scores
+
+def check_qsa_hand(o):
+    """Hand-worked blocks, one per case, each key nonzero only in its own dims (so the queries'
+    other values meet zeros: q*0 and fma(q, 0, p) = p are exact, and the pairings add zeros):
+      block 0: lane 0 takes dims 0..3 and fuses its products: q0*k0 = -3, then fma((1 + 2^-23), 3,
+               -3) = 3 * 2^-23 exactly (a rounded product first would give 3 + 2^-21 - 3 = 2^-21)
+      block 1: dims 4, 5, 6 sit in one lane (1): 2^-24, then 2^-23, then 1 + 2^-23 exactly (in three
+               lanes the pairings would add 1 + 2^-24 first, which rounds to 1)
+      block 2: lanes 2, 3 and 19 hold 2^24, 1, 1: level 16 pairs lanes 3 and 19 (2), level 1 adds
+               2^24 + 2 = 16777218 exactly (a sum in lane order loses both ones: 16777216)
+      block 3: one dim, heads give relus 1, 2^-24, 2^-24, 0: head order ((1 + 2^-24) + 2^-24) + 0
+               = 1 (in reverse order 1 + 2^-23)
+      block 4: scale 4; head 0's dot -6 is dropped by the relu, head 1's 1.5 * 4 = 6
+      block 5: the tail, zero key: 0 + 1e9"""
+    q = np.zeros((1, 4, 128), np.float32)
+    keys = np.zeros((6, 128), np.int8)
+    scale = np.ones(6, np.float32)
+    q[0, 0, 0], q[0, 0, 1] = -1.0, 1.0 + 2.0 ** -23
+    keys[0, 0] = keys[0, 1] = 3
+    q[0, 0, 4], q[0, 0, 5], q[0, 0, 6] = 2.0 ** -24, 2.0 ** -24, 1.0
+    keys[1, 4] = keys[1, 5] = keys[1, 6] = 1
+    q[0, 0, 8], q[0, 0, 12], q[0, 0, 76] = 2.0 ** 24, 1.0, 1.0
+    keys[2, 8] = keys[2, 12] = keys[2, 76] = 1
+    q[0, :, 16] = [1.0, 2.0 ** -24, 2.0 ** -24, 0.0]
+    keys[3, 16] = 1
+    q[0, 0, 20], q[0, 1, 20] = -3.0, 0.75
+    keys[4, 20] = 2
+    scale[4] = 4.0
+    got = o.qsa_block_scores(q, keys, scale)[0]
+    want = np.array([3 * 2.0 ** -23, 1 + 2.0 ** -23, 16777218.0, 1.0, 6.0, 1e9], np.float32)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (got, want)
+
+
+def check_qsa_bruteforce(o):
+    """Random queries, keys and scales against the fp64 definition sum_h max(scale * q_h . k, 0)
+    (+ 1e9 on the tail): every fp32 result within 16 * 2^-24 of scale * sum_h sum_d |q_hd k_d| (a
+    bound on 4 in-lane steps, 5 pairing levels, the scale product and 3 head additions), plus
+    half an ulp of 1e9 on the tail; and each query's and each non-tail block's scores depend on
+    nothing else (the same bits alone and among others)."""
+    rng = np.random.Generator(np.random.PCG64(11))
+    T, nb = 4, 37
+    q = rng.standard_normal((T, 4, 128)).astype(np.float32)
+    keys = rng.integers(-127, 128, (nb, 128)).astype(np.int8)
+    scale = rng.uniform(1e-3, 1e-2, nb).astype(np.float32)
+    got = o.qsa_block_scores(q, keys, scale)
+    qk = np.einsum("thd,bd->thb", q.astype(np.float64), keys.astype(np.float64)) * scale.astype(np.float64)
+    ref = np.maximum(qk, 0.0).sum(axis=1)
+    mag = (np.einsum("thd,bd->tb", np.abs(q.astype(np.float64)), np.abs(keys.astype(np.float64)))
+           * scale.astype(np.float64))
+    ref[:, -1] += 1e9
+    bound = 16 * 2.0 ** -24 * mag
+    bound[:, -1] += 32.0
+    assert (np.abs(got.astype(np.float64) - ref) <= bound).all()
+    assert (got[:, :-1] >= 0).all()
+    # independence: one query alone, and the non-tail blocks in another order with another tail
+    assert np.array_equal(o.qsa_block_scores(q[2:3], keys, scale)[0].view(np.uint32), got[2].view(np.uint32))
+    perm = rng.permutation(nb - 1)
+    keys2 = np.concatenate([keys[:-1][perm], keys[-1:]])
+    sc2 = np.concatenate([scale[:-1][perm], scale[-1:]])
+    got2 = o.qsa_block_scores(q, keys2, sc2)
+    assert np.array_equal(got2[:, :-1].view(np.uint32), got[:, :-1][:, perm].view(np.uint32))
+
+
+ALL_CHECKS = [check_qsa_hand, check_qsa_bruteforce, check_router, check_combine, check_f16, check_exp, check_silu, check_q8_1, check_formats_hand, check_formats_onehot,
               check_formats_bruteforce, check_slots, check_route_hand, check_route_invariants, check_grouped_invariants,
               check_swiglu_q8_1]

@@ -20,6 +20,11 @@ PLANTS = {
     "ORC_PLANT_TIE_HIGH": "router ties resolved to the higher expert id",
     "ORC_PLANT_SOFTMAX_ALL": "router softmax over every expert instead of the selected k",
     "ORC_PLANT_COMBINE_SLOT": "combine drops the last slot",
+    "ORC_PLANT_QSA_LANE_INTERLEAVE": "QSA lane slices strided (l, l+32, ...) instead of 4 consecutive dims",
+    "ORC_PLANT_QSA_NO_FMA": "QSA lane products rounded before they are added",
+    "ORC_PLANT_QSA_TREE_SEQ": "QSA lane partials summed in lane order instead of the warp-sum pairings",
+    "ORC_PLANT_QSA_HEAD_ORDER": "QSA head relus summed in reverse order",
+    "ORC_PLANT_QSA_TAIL_FIRST": "QSA +1e9 on the first block instead of the tail",
 }
 
 
