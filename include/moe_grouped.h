@@ -181,6 +181,11 @@ int moe_grouped_down(moe_wfmt fmt, int n_embd, int n_ff, const void* const* w_do
 #define MOE_F_PDL 1 /* chain the three kernels with programmatic dependent launch */
 #define MOE_F_SYNC_PAIR 2 /* moe_expert_layer: sync holds two halves used by alternate calls */
 #define MOE_F_SYNC_ODD 4  /* moe_expert_layer with MOE_F_SYNC_PAIR: this call uses the second half */
+/* moe_expert_layer, test hook only: the down staging waits for a flag no call writes, so every CTA
+ * that reaches a down item gives up after the wait limit (~1 s) and the call takes its timeout
+ * path (MOE_ERR_TIMEOUT, the work left undone, the CTA's copies in flight awaited). The call's out
+ * rows are then unspecified; zero the sync array before the next call. */
+#define MOE_F_TEST_EXPIRE 8
 
 /* One native_expert_grouped-style call (#363): gate/up, SwiGLU + q8_1, down on one stream. */
 typedef struct moe_expert_call {
@@ -221,7 +226,9 @@ int moe_expert_grouped(const moe_expert_call* call, cudaStream_t stream);
  *    exceed MOE_STATIC_SCRATCH_BYTES, else MOE_E_SCRATCH is returned and nothing is launched
  *    (e.g. 32 entries at n_ff 768 need about 0.2 MB; 256 entries at n_ff 1536 about 3.6 MB).
  *  - The first call on each device looks up the buffer's device address (once per device, with
- *    that device current); make that first call before any stream capture on the device.
+ *    that device current); make that first call before any stream capture on the device. The
+ *    address is kept for the life of the process, so do not use this entry point across a
+ *    device reset (cudaDeviceReset or anything else that tears down and rebuilds the context).
  *  - Every call shares the one buffer and it keeps the previous call's contents; the call writes
  *    every scratch row it later reads, so nothing needs clearing, but calls that overlap on the
  *    GPU (other streams, other threads) race on the buffer and must be serialised by the caller.
@@ -243,21 +250,26 @@ int moe_expert_grouped_static(const moe_expert_call* call, cudaStream_t stream);
  *    call they hold the gate/up rows and the q8_1 h rows.
  *  - sync: moe_layer_sync_ints(T, k, n_ff) int32 words (8-byte aligned, else MOE_E_ALIGN) the
  *    launch's CTAs synchronise through: word 0 an exit counter, word 1 the work-item counter,
- *    word 2 the call epoch, and from word 4 a flagged copy of the q8_1 h rows (per entry nine
- *    rows of one 8-byte pair per h block: a header or code word and the writing call's flag,
- *    epoch + 1), which
- *    the down phase polls instead of a counter, so the gate/up side needs no fence. The caller
- *    zeroes the array once before the first call (e.g. cudaMemsetAsync); every call leaves words
- *    0 and 1 zero and advances the epoch, so no pair left by an earlier call carries the next
- *    call's flag. The epoch is 32 bits: zero the array again at least every 2^32 - 2 calls on it
- *    (after that many the flag would wrap to 0, the value of a pair never written). A call that reported MOE_ERR_TIMEOUT may leave the array inconsistent: zero it
- *    again. Calls that may overlap on the GPU need separate sync arrays (and scratch).
+ *    word 2 the call epoch, word 3 the largest number of h pairs a call on the array has used,
+ *    and from word 4 a flagged copy of the q8_1 h rows (per entry nine rows of one 8-byte pair
+ *    per h block: a header or code word and the writing call's flag, epoch + 1), which the down
+ *    phase polls instead of a counter, so the gate/up side needs no fence. The caller zeroes the
+ *    array once before the first call (e.g. cudaMemsetAsync); every call leaves words 0 and 1
+ *    zero and advances the epoch, so no pair left by an earlier call carries the next call's
+ *    flag. The epoch is 32 bits and skips 2^32 - 1 (whose flag would be 0, the value of a pair
+ *    never written): the call that would advance it there zeroes every pair word 3 counts and
+ *    restarts it at 0, so the array never needs zeroing again. Without MOE_F_SYNC_PAIR an array
+ *    may serve calls of different T if it is sized for the largest. A call that reported MOE_ERR_TIMEOUT may leave
+ *    the array inconsistent: zero it again. Calls that may overlap on the GPU need separate sync
+ *    arrays (and scratch).
  *    With MOE_F_SYNC_PAIR in flags, sync holds two halves of moe_layer_sync_ints words: the call
  *    uses the first half (the second with MOE_F_SYNC_ODD) and resets the other one (zero counters,
- *    epoch advanced) after its dependency wait, instead of having its last CTA reset its own half
- *    on the way out (a device-wide fence and an atomic per CTA less at the end of every call).
+ *    epoch advanced; its CTA 0 does that on the way out, the other half's last call having
+ *    completed before this call's dependency wait returned), instead of having its last CTA reset
+ *    its own half (a device-wide fence and an atomic per CTA less at the end of every call).
  *    Consecutive calls on one stream that share the array must alternate halves; zero both halves
- *    before the first call.
+ *    before the first call. The halves are located by the call's own T, k and n_ff, so every call
+ *    on a pair array has the same ones.
  *  - grp_expert [T*k], grp_start [T*k+1], n_groups [1], ent_src / ent_dst [T*k], xq
  *    [T][n_embd/32]: optional (NULL = not written) copies of the grouping and of the activation
  *    q8_1, for inspection.

@@ -18,13 +18,14 @@ __all__ = [
     "Q8_0", "Q4B", "NL4", "CB2", "CB3", "CB3X", "CB2X", "MoeError", "transcode_cb", "lib", "row_bytes", "strerror",
     "quantize_q8_1", "route_group", "grouped_gu", "swiglu_q8_1", "grouped_down",
     "expert_grouped", "ExpertCall", "STATIC_SCRATCH_BYTES", "test_block_isum", "ERR_BITS", "F_PDL",
-    "LayerCall", "layer_sync_ints", "router_topk", "combine", "F_SYNC_PAIR", "F_SYNC_ODD",
+    "LayerCall", "layer_sync_ints", "router_topk", "combine", "F_SYNC_PAIR", "F_SYNC_ODD", "F_TEST_EXPIRE",
 ]
 
 Q8_0, Q4B, NL4, CB2, CB3, CB3X, CB2X = 1, 2, 3, 4, 5, 6, 7
 F_PDL = 1
 F_SYNC_PAIR = 2  # moe_expert_layer: sync holds two halves used by alternate calls
 F_SYNC_ODD = 4   # ... and this call uses the second half
+F_TEST_EXPIRE = 8  # test hook: the down staging waits for a flag no call writes (timeout path)
 STATIC_SCRATCH_BYTES = 4 << 20
 ERR_BITS = {1: "NGROUPS", 2: "EXPERT", 4: "START", 8: "ENTRY", 16: "ALIGN", 32: "CODEBOOK",
             64: "TIMEOUT", 128: "ROUTE"}

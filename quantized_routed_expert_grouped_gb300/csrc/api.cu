@@ -531,6 +531,7 @@ int moe_expert_layer(const moe_layer_call* c, cudaStream_t stream) {
     L.o_es = c->ent_src;
     L.o_ed = c->ent_dst;
     L.o_xq = c->xq;
+    L.test_expire = (c->flags & MOE_F_TEST_EXPIRE) != 0;
     // one CTA per SM (co-resident), split on the device between the gate/up and the down roles
     const int64_t grid = sms;
     const bool pdl = (c->flags & MOE_F_PDL) != 0;

@@ -72,11 +72,12 @@ struct GemvPlan {
 };
 
 // Arguments of one fused layer launch (layer.cuh).
-// The fused layer's sync array (int32 words): the exit counter, the global work-item counter and
-// the call epoch, then from word kSyncHx the flagged copy of h: per entry, nine rows (k = 0..8) of
-// one 8-byte pair per h block (low word: the block's header for k = 0, code word k - 1 otherwise;
-// high word: the writing call's flag, epoch + 1), so that a reader polls the data itself.
-constexpr int kSyncExit = 0, kSyncWork = 1, kSyncEpoch = 2, kSyncHx = 4;
+// The fused layer's sync array (int32 words): the exit counter, the global work-item counter, the
+// call epoch and the largest number of h pairs any call on the array has used, then from word
+// kSyncHx the flagged copy of h: per entry, nine rows (k = 0..8) of one 8-byte pair per h block
+// (low word: the block's header for k = 0, code word k - 1 otherwise; high word: the writing
+// call's flag, epoch + 1), so that a reader polls the data itself.
+constexpr int kSyncExit = 0, kSyncWork = 1, kSyncEpoch = 2, kSyncExt = 3, kSyncHx = 4;
 constexpr int kHxPairs = 9;  // pairs per q8_1 block
 
 struct LayerArgs {
@@ -95,6 +96,7 @@ struct LayerArgs {
     int off_route;       // shared-memory routing scratch
     int off_unit;        // shared-memory gate/up unit buffers: [4 units][4 entries][32] h values
     int off_ptr;         // shared-memory cache of both expert pointer tables (0: not cached)
+    int test_expire;     // test hook: the down staging waits for a flag no call writes
 };
 
 cudaError_t launch_quantize_q8_1(const float* x, int64_t rows, int64_t cols, moe_q8_1* xq, cudaStream_t s,

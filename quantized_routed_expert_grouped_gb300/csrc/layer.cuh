@@ -56,6 +56,22 @@ namespace moe {
 constexpr int kDescRing = 16;  // tile descriptors in flight per CTA (ring indices)
 constexpr int kUnitBufs = 4;   // gate/up units in flight per CTA (h buffers in shared memory)
 
+// Advance a sync array's call epoch (the next call's flag is epoch + 1). The epoch never takes
+// the value 2^32 - 1, whose flag would be 0, the value of a pair never written: there every pair
+// any call on the array has used (word kSyncExt) is zeroed and the epoch restarts at 0, so no
+// pair left from the cycle before carries a flag of the new one. One thread; the array's next
+// call starts after this grid has completed.
+static __device__ __noinline__ void advance_epoch(int32_t* s) {
+    uint32_t e = static_cast<uint32_t>(s[kSyncEpoch]) + 1u;
+    if (e == 0xFFFFFFFFu) {
+        uint64_t* hx = reinterpret_cast<uint64_t*>(s + kSyncHx);
+        const int64_t np = s[kSyncExt];
+        for (int64_t i = 0; i < np; ++i) hx[i] = 0;
+        e = 0;
+    }
+    s[kSyncEpoch] = static_cast<int32_t>(e);
+}
+
 // One 8-byte pair of the flagged h copy: a naturally aligned 64-bit access is single-copy
 // atomic, so a reader that sees the flag sees the word written with it.
 __device__ __forceinline__ void st_pair(uint64_t* p, uint32_t word, uint32_t flag) {
@@ -355,12 +371,6 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     __syncthreads();
     pdl_wait();
     pdl_trigger();
-    // a sync pair: the call that used the other half has completed; reset it for the next call
-    if (L.sync_other && blockIdx.x == 0 && tid == 0) {
-        L.sync_other[kSyncExit] = 0;
-        L.sync_other[kSyncWork] = 0;
-        L.sync_other[kSyncEpoch] += 1;
-    }
     uint64_t* hx = reinterpret_cast<uint64_t*>(L.sync + kSyncHx);
 
     // ---- routing/grouping and tables: one warp when n <= 32, else the whole CTA routes and
@@ -597,9 +607,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                         ok = __shfl_sync(0xffffffffu, ok, 0);
                         // the batch's h rows, each block staged as soon as its flagged copy is
                         // complete (every unit of the group writes one block per entry)
+                        // (the test hook waits for a flag that no call writes)
+                        const uint32_t want = L.test_expire ? flag ^ 0x80000000u : flag;
                         ok = __all_sync(0xffffffffu, ok && !vmisc[1] &&
                                                          stage_flagged<DT>(D, smem, entD, hx, b0, ne,
-                                                                           kMaxEntriesPerPass * (st_n & 1), flag, lane));
+                                                                           kMaxEntriesPerPass * (st_n & 1), want, lane));
                         if (!ok) {
                             if (lane == 0) {
                                 if (!vmisc[1]) set_err(A.err, MOE_ERR_TIMEOUT);
@@ -808,9 +820,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         for (int qq = nq - S > 0 ? nq - S : 0; qq < nq; ++qq)
             mbar_wait_bounded(&full[qq % S], static_cast<uint32_t>(qq / S) & 1u);
     }
-    // ---- exit count; the last CTA zeroes the counters and advances the epoch for the next call
-    // (with a sync pair, the next call does that instead)
-    if (L.sync_other) return;
+    // the h pairs this call used, the extent an epoch wrap clears
+    const int32_t ext = n * kHxPairs * L.nbj;
+    // ---- a sync pair: the call that used the other half has completed (this one is past its
+    // dependency wait), so CTA 0 resets that half for the call after this one, and records this
+    // call's extent in its own half (read when the next call advances this half's epoch)
+    if (L.sync_other) {
+        if (blockIdx.x == 0 && tid == 0) {
+            L.sync_other[kSyncExit] = 0;
+            L.sync_other[kSyncWork] = 0;
+            advance_epoch(L.sync_other);
+            if (L.sync[kSyncExt] < ext) L.sync[kSyncExt] = ext;
+        }
+        return;
+    }
+    // ---- otherwise an exit count: the last CTA zeroes the counters and advances the epoch
     if (tid == 0) {
         __threadfence();
         misc[2] = atomicAdd(L.sync + kSyncExit, 1) == static_cast<int>(gridDim.x) - 1;
@@ -820,7 +844,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         __threadfence();
         L.sync[kSyncExit] = 0;
         L.sync[kSyncWork] = 0;
-        L.sync[kSyncEpoch] += 1;
+        if (L.sync[kSyncExt] < ext) L.sync[kSyncExt] = ext;
+        advance_epoch(L.sync);
     }
 }
 

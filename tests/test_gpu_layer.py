@@ -22,7 +22,8 @@ CASES = [("tiny", (synth.Q8_0, synth.Q8_0), 1, None), ("verify", (synth.CB2, syn
          ("verify", (synth.CB2, synth.NL4), 8, None), ("window48", (synth.CB3, synth.NL4), 6, synth.CB3X),
          ("sweep", (synth.Q4B, synth.NL4), 4, None), ("sweep", (synth.CB3, synth.Q8_0), 4, None),
          ("sweep", (synth.Q8_0, synth.Q8_0), 4, None), ("sweep", (synth.CB2, synth.NL4), 4, None),
-         ("sweep", (synth.Q4B, synth.Q8_0), 4, None), ("sweep", (synth.CB3, synth.NL4), 4, None)]
+         ("sweep", (synth.Q4B, synth.Q8_0), 4, None), ("sweep", (synth.CB3, synth.NL4), 4, None),
+         ("sweep", (synth.Q8_0, synth.NL4), 4, None), ("sweep", (synth.CB2, synth.Q8_0), 4, None)]
 CASE_IDS = [f"{c[0]}-{synth.NAMES[c[1][0]]}-{synth.NAMES[c[1][1]]}-T{c[2]}" + (f"-{synth.NAMES[c[3]]}" if c[3] else "")
             for c in CASES]
 
@@ -198,6 +199,106 @@ def test_layer_sync_pair_alternating_halves(m, orc):
             assert torch.equal(f.out.view(torch.int32), b.view(torch.int32))
         _left_clean(pair[:half], 4 + 2 * r)  # reset by every odd call: two per pass
     assert all(int(f.err.item()) == 0 for f in fs)
+
+
+def _window_layers(m, wl, T, layers):
+    return [H.transcoded(m, H.make_layer(wl, (synth.CB3, synth.NL4), T, layer=l), synth.CB3X) for l in layers]
+
+
+def test_layer_epoch_wrap(m, orc):
+    """The call epoch skips 2^32 - 1 (whose flag would be 0, the flag of a pair never written): the
+    call that would reach it zeroes every h pair a call on the array has used (word 3) and
+    restarts the epoch at 0. One array sized for T = 4 serves a T = 4 call (its pairs carry flag
+    1), then, with the epoch set just below the wrap, a T = 2 call that wraps it, then a T = 4 call
+    whose flag is 1 again. Without the clearing, that last call's down phase would take the first
+    call's stale h blocks of entries 16..31 (another layer's data) as its own."""
+    wl = synth.WORKLOADS["window48"]
+    LA, = _window_layers(m, wl, 4, [1])
+    LB, = _window_layers(m, wl, 2, [2])
+    LC, = _window_layers(m, wl, 4, [3])
+    refB, refC = _separate(m, LB), _separate(m, LC)
+    ext = 4 * wl.k * 9 * (wl.F // 32)
+    sync = torch.zeros(m.layer_sync_ints(4, wl.k, wl.F), dtype=torch.int32, device="cuda")
+    fs = [Fused(m, L) for L in (LA, LB, LC)]
+    for f in fs:
+        f.call.c.sync = sync.data_ptr()
+    fs[0].call()
+    torch.cuda.synchronize()
+    assert tuple(sync[:4].tolist()) == (0, 0, 1, ext)
+    sync[2] = -2  # epoch 2^32 - 2: the next call's flag is 2^32 - 1
+    fs[1].call()
+    torch.cuda.synchronize()
+    assert tuple(sync[:4].tolist()) == (0, 0, 0, ext)  # wrapped: epoch 0 again
+    assert not sync[4:].any()  # every pair used so far zeroed
+    assert np.array_equal(_bits(fs[1].out), _bits(refB.out))
+    fs[2].call()
+    torch.cuda.synchronize()
+    assert all(int(f.err.item()) == 0 for f in fs)
+    assert np.array_equal(_bits(fs[2].out), _bits(refC.out))
+    _same_as_separate(fs[2], refC, 4 * wl.k)
+    assert tuple(sync[:4].tolist()) == (0, 0, 1, ext)
+
+
+def test_layer_epoch_wrap_sync_pair(m, orc):
+    """The same with MOE_F_SYNC_PAIR, where a call advances the other half's epoch on its way out:
+    call 0 (first half, flag 1), the first half's epoch set just below the wrap, call 1 (second
+    half) wraps the first half and clears its pairs, call 2 (first half, flag 1 again) must not
+    take call 0's stale h blocks."""
+    wl = synth.WORKLOADS["window48"]
+    Ls = _window_layers(m, wl, 4, [4, 5, 6])
+    refs = [_separate(m, L) for L in Ls]
+    half = m.layer_sync_ints(4, wl.k, wl.F)
+    ext = 4 * wl.k * 9 * (wl.F // 32)
+    pair = torch.zeros(2 * half, dtype=torch.int32, device="cuda")
+    fs = [Fused(m, L) for L in Ls]
+    for i, f in enumerate(fs):
+        f.call.c.sync = pair.data_ptr()
+        f.call.c.flags = m.F_PDL | m.F_SYNC_PAIR | (m.F_SYNC_ODD if i % 2 else 0)
+    fs[0].call()
+    torch.cuda.synchronize()
+    # the first half keeps its counters until call 1 resets it; its extent is recorded
+    assert tuple(pair[2:4].tolist()) == (0, ext) and tuple(pair[half:half + 3].tolist()) == (0, 0, 1)
+    pair[2] = -2
+    fs[1].call()
+    torch.cuda.synchronize()
+    assert tuple(pair[:4].tolist()) == (0, 0, 0, ext) and not pair[4:half].any()
+    fs[2].call()
+    torch.cuda.synchronize()
+    for f, r in zip(fs, refs):
+        assert int(f.err.item()) == 0
+        assert np.array_equal(_bits(f.out), _bits(r.out))
+
+
+def test_layer_timeout_path(m, orc):
+    """The abort path of the fused kernel, made to run by MOE_F_TEST_EXPIRE: every CTA's down
+    staging waits for a flag that no call writes, gives up after the wait limit (~1 s), sets
+    MOE_ERR_TIMEOUT, stops its producer, lets its consumers drain and waits for its own copies in
+    flight. The call ends (no hang) and the context stays usable: with the sync array zeroed
+    again, the next call equals the separate path bit for bit."""
+    import time
+    wl = synth.WORKLOADS["verify"]
+    L = H.make_layer(wl, (synth.CB2, synth.NL4), 4)
+    n = L.T * wl.k
+    B = _separate(m, L)
+    F = Fused(m, L)
+    F.call.c.flags = m.F_TEST_EXPIRE
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    F.call()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(F.err.item()) & 64, int(F.err.item())  # MOE_ERR_TIMEOUT
+    assert 0.5 < dt < 30, dt
+    assert np.isnan(F.out.cpu().numpy()).all()  # no down row was written
+    F.sync.zero_()
+    F.err.zero_()
+    F.out.fill_(float("nan"))
+    F.call.c.flags = m.F_PDL
+    F.call()
+    torch.cuda.synchronize()
+    assert int(F.err.item()) == 0
+    _same_as_separate(F, B, n)
+    _left_clean(F.sync, 1)
 
 
 def test_layer_dropped_ids_and_empty(m, orc):

@@ -290,9 +290,30 @@ def test_second_call_after_first(m, orc):
             for i in range(n + 6):
                 assert np.isnan(out[i]).all() == (i not in own_out)
             if ng:
+                # the oracle's chain for this call's one group: gate/up (fp64) ...
                 ref = np.full((cap_e, 2 * wl.F), np.nan)
                 orc.grouped_gemv(L.gu_t, wl.N, 2 * wl.F, gub, ge[:1], gs[:2], 1, xq, ent_in=es, out=ref, cb=L.cb_gu)
                 assert H.rel_err(gu[n:n + ne], ref[n:n + ne]) <= TOL
+                # ... SwiGLU + q8_1 over the call's own entries: bit for bit on the GPU's gate/up
+                # rows (same fp32 inputs), then on the oracle's own fp32-rounded rows ...
+                hq_stage = np.zeros((cap_e, wl.F // 32, 36), np.uint8)
+                orc.swiglu_q8_1(gu, wl.F, n, n + ne, hq_stage)
+                assert (hq[n:n + ne] == hq_stage[n:n + ne]).all()
+                hq_ref = np.zeros((cap_e, wl.F // 32, 36), np.uint8)
+                orc.swiglu_q8_1(np.nan_to_num(ref).astype(np.float32), wl.F, n, n + ne, hq_ref)
+                flips, scale_diffs = H.q8_1_code_flips(hq[n:n + ne], hq_ref[n:n + ne])
+                # ... and down to the scattered rows (fp64), from the oracle's h
+                oref = np.full((n + 6, wl.N), np.nan)
+                orc.grouped_gemv(L.dn_t, wl.F, wl.N, dnb, ge[:1], gs[:2], 1, hq_ref, ent_out=ed, out=oref,
+                                 cb=L.cb_dn)
+                rows = sorted(own_out)
+                bound = TOL if flips == 0 and scale_diffs == 0 else 2e-3
+                assert H.rel_err(out[rows], oref[rows]) <= bound, (gg, ne, flips)
+                # the GPU's down on its own h against the oracle's down on the same h: 1e-5
+                oref_own = np.full((n + 6, wl.N), np.nan)
+                orc.grouped_gemv(L.dn_t, wl.F, wl.N, dnb, ge[:1], gs[:2], 1, hq, ent_out=ed, out=oref_own,
+                                 cb=L.cb_dn)
+                assert H.rel_err(out[rows], oref_own[rows]) <= TOL, (gg, ne)
 
 
 def test_device_errors_are_reported_and_skipped(m, orc):

@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 TOL = 1e-5
 
 
-def _run(m, L, B, static):
+def _run(m, L, B, static, dst=None):
     B.out.fill_(float("nan"))
     call = H.expert_call(m, L, B)
     if static:
@@ -26,7 +26,15 @@ def _run(m, L, B, static):
     else:
         call()
     torch.cuda.synchronize()
-    return B.out.clone()
+    if dst is None:
+        return B.out.clone()
+    dst.copy_(B.out)
+    torch.cuda.synchronize()
+    return dst
+
+
+def _same_bits(a, b):
+    return torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
 def test_static_scratch_call_matches_allocating_call():
@@ -39,10 +47,23 @@ def test_static_scratch_call_matches_allocating_call():
         H.gpu_route_and_quantize(m, L, B)
         ref = _run(m, L, B, static=False)
         assert not torch.isnan(ref).any()
+        got = torch.empty_like(ref)
+        # the first static call on a device may load the library's static buffer (the module is
+        # loaded lazily: its 4 MiB appear then, once, and stay until exit); it is checked too
+        _run(m, L, B, static=True, dst=got)
+        assert _same_bits(got, ref)
+        torch.cuda.synchronize()
+        free0, allocated0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
         for _ in range(2):  # two calls in a row share (and reuse) the static buffer
-            got = _run(m, L, B, static=True)
+            _run(m, L, B, static=True, dst=got)
             assert int(B.err.item()) == 0
+            # the same kernels on the same inputs, only the scratch lives elsewhere: the same
+            # bits (which is within any tolerance)
             assert H.rel_err(got.cpu().numpy(), ref.cpu().numpy()) <= TOL
+            assert _same_bits(got, ref)
+        # and the calls allocated no device memory
+        assert torch.cuda.memory_allocated() == allocated0
+        assert torch.cuda.mem_get_info()[0] >= free0
     # a second routing after the first: stale scratch from the previous call must not leak
     wl = synth.WORKLOADS["verify"]
     L2 = H.make_layer(wl, (synth.CB2, synth.NL4), 4, layer=1)
@@ -51,6 +72,7 @@ def test_static_scratch_call_matches_allocating_call():
     ref2 = _run(m, L2, B2, static=False)
     got2 = _run(m, L2, B2, static=True)
     assert H.rel_err(got2.cpu().numpy(), ref2.cpu().numpy()) <= TOL
+    assert _same_bits(got2, ref2)
 
 
 def test_static_scratch_rejects_oversize_calls():
