@@ -317,6 +317,8 @@ def run_ours(args, rank, world):
     # ---- end to end: pinned host inputs -> device, the window graphs, outputs -> host
     e2e = end_to_end(wins, args, s, world, dev)
     sparse = sparse_calls(m, dev)
+    sweep = call_sweep(m, dev, hbm_peak)
+    qsa = qsa_sweep(m, dev)
 
     launches = args.steps * len(TS) * launches_per_window(True)
     line = {
@@ -333,7 +335,7 @@ def run_ours(args, rank, world):
         "per_T": per_T,
         "separate_kernels": {"launch": "route + quantize + gate/up + SwiGLU/q8_1 + down per layer", "per_T": separate},
         "native_layout": {"gate_up": "CB3 (read directly), fused launches", "per_T": native},
-        "roofline": roof, "step_us_per_layer_alone": breakdown, "second_call_cost": sparse, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+        "roofline": roof, "step_us_per_layer_alone": breakdown, "second_call_cost": sparse, "calls": sweep, "qsa_block_scores": qsa, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
         "setup_s": round(setup_s, 1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -341,9 +343,10 @@ def run_ours(args, rank, world):
     return line
 
 
-# DRAM read + write bytes of one fused layer launch at T = 4 (layer 0, 29 groups), from the ncu
-# capture summarised in profiles/layer_kernel_window48_T4.md; reported only while the kernel
-# sources hash to the ones the capture was taken on (else null: the counters are stale).
+# DRAM read + write bytes of one fused layer launch at T = 4 (layer 0, 29 groups), from an ncu
+# capture of `bench.py --case --case-fused --case-slot` (stored here, not measured by this run);
+# reported only while the kernel sources hash to the ones the capture was taken on (else null:
+# the counters are stale).
 LAYER_TRAFFIC_T4 = {"bytes": 95_377_920, "sources": ("layer.cuh", "gemv.cuh", "common.cuh", "q8_1.cuh", "route.cuh"),
                     "sha1": "c27b16b12f9fbbf15bcea37752a3e5fbaf94adf7"}
 
@@ -416,6 +419,147 @@ def sparse_calls(m, dev, reps=20):
     return res
 
 
+def _routings(wl, calls, seed):
+    return [synth.routing(wl.T[0], wl.k, wl.E, seed * 1000 + c) for c in range(calls)]
+
+
+def _layer_graph(m, lcalls, reps):
+    """Microseconds per call of a CUDA graph of the given fused layer calls (PDL-chained,
+    alternating the halves of one counter pair), replayed `reps` times."""
+    for c in lcalls:
+        c()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        for c in lcalls:
+            c()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / (reps * len(lcalls))
+
+
+def call_sweep(m, dev, hbm_peak, reps=10, calls=16):
+    """One fused layer call (moe_expert_layer) per routing, timed in a CUDA graph of `calls`
+    calls with distinct seeded routings, on
+      - the verify workload (T = 4, 64 experts, top-8, n_embd 2560, n_ff 768, CB2 gate/up read
+        directly and as CB2X slots, NL4 down): the 139.6 MB pool replicated 8 times (1.1 GB), call
+        c on replica c % 8, so every call reads cold;
+      - the format sweep (T = 4, 256 experts, top-8, n_embd 4096, n_ff 1536, activations with 1 %
+        outliers x20): each of the 8 (gate/up, down) pairs on its own 256-expert pool (1.8-5.1 GB).
+    Per case: microseconds per call, the algorithmic weight bytes of the calls' groups (gate/up +
+    down blobs of their experts, as stored), GB/s and the fraction of the measured HBM peak."""
+    out = {}
+    i32 = dict(dtype=torch.int32, device=dev)
+
+    def run(wl, gu_t, dn_t, pools, cb_gu, cb_dn, algo_gu_t, tag):
+        n = wl.T[0] * wl.k
+        ids = _routings(wl, calls, wl.seed + 7)
+        x = [torch.from_numpy(synth.activations(wl.T[0], wl.N, wl.seed * 100 + c, wl.outliers)).to(dev)
+             for c in range(calls)]
+        idt = [torch.from_numpy(r).to(dev) for r in ids]
+        outs = torch.zeros((calls, n, wl.N), dtype=torch.float32, device=dev)
+        gu = torch.zeros((n, 2 * wl.F), dtype=torch.float32, device=dev)
+        hq = torch.zeros((n, wl.F // 32, 36), dtype=torch.uint8, device=dev)
+        sync = torch.zeros(2 * m.layer_sync_ints(wl.T[0], wl.k, wl.F), **i32)
+        err = torch.zeros(1, **i32)
+        lc = []
+        for c in range(calls):
+            tg, td = pools[c % len(pools)]
+            lc.append(m.LayerCall(gu_t, cb_gu, dn_t, cb_dn, wl.N, wl.F, tg, td, wl.E, idt[c], x[c], outs[c], gu, hq,
+                                  sync, err, m.F_PDL | m.F_SYNC_PAIR | (m.F_SYNC_ODD if c % 2 else 0)))
+        us = _layer_graph(m, lc, reps)
+        if int(err.item()):
+            raise RuntimeError(f"{tag}: device error bits {int(err.item())}")
+        per_expert = synth.blob_bytes(algo_gu_t, 2 * wl.F, wl.N) + synth.blob_bytes(dn_t, wl.N, wl.F)
+        groups = float(np.mean([len(np.unique(r)) for r in ids]))
+        by = groups * per_expert
+        out[tag] = {"us": round(us, 2), "groups": round(groups, 2), "weight_bytes": int(by),
+                    "GBps": round(by / (us * 1e-6) / 1e9, 1), "frac_of_measured_hbm": round(by / (us * 1e-6) / 1e9 / hbm_peak, 4)}
+
+    def tables(pool):
+        return torch.tensor([pool[x].data_ptr() for x in range(pool.shape[0])], dtype=torch.int64, device=dev)
+
+    # ---- the verify call (CB2 / NL4), 8 replicas of its pool
+    wl = synth.WORKLOADS["verify"]
+    gu_t, dn_t = wl.pairs[0]
+    cb_gu = torch.from_numpy(synth.codebook(gu_t, wl.seed * 7 + 1).ravel().copy()).to(dev)
+    cb_dn = torch.from_numpy(synth.codebook(dn_t, wl.seed * 7 + 2).ravel().copy()).to(dev)
+    reps8 = []
+    for r in range(8):
+        pg = synth.weight_blobs(gu_t, 2 * wl.F, wl.N, wl.E, synth.derive_key(wl.seed, r, gu_t, 0), dev)
+        pd = synth.weight_blobs(dn_t, wl.N, wl.F, wl.E, synth.derive_key(wl.seed, r, dn_t, 1), dev)
+        reps8.append((pg, pd))
+    run(wl, gu_t, dn_t, [(tables(pg), tables(pd)) for pg, pd in reps8], cb_gu, cb_dn, gu_t, "verify_CB2_NL4")
+    xs = []
+    terr = torch.zeros(1, **i32)
+    for pg, pd in reps8:
+        px = torch.empty((wl.E, synth.blob_bytes(synth.CB2X, 2 * wl.F, wl.N)), dtype=torch.uint8, device=dev)
+        m.transcode_cb(gu_t, cb_gu, synth.CB2X, wl.N, 2 * wl.F, tables(pg), tables(px), terr)
+        xs.append((px, pd))
+    torch.cuda.synchronize()
+    run(wl, synth.CB2X, dn_t, [(tables(px), tables(pd)) for px, pd in xs], None, cb_dn, gu_t,
+        "verify_CB2X_slots_NL4")
+    del reps8, xs
+    # ---- the format sweep: 8 pairs
+    wl = synth.WORKLOADS["sweep"]
+    for gu_t, dn_t in wl.pairs:
+        pg = synth.weight_blobs(gu_t, 2 * wl.F, wl.N, wl.E, synth.derive_key(wl.seed, 0, gu_t, 0), dev)
+        pd = synth.weight_blobs(dn_t, wl.N, wl.F, wl.E, synth.derive_key(wl.seed, 0, dn_t, 1), dev)
+        cg = synth.codebook(gu_t, wl.seed * 7 + 1)
+        cd = synth.codebook(dn_t, wl.seed * 7 + 2)
+        cg = None if cg is None else torch.from_numpy(np.ascontiguousarray(cg).ravel()).to(dev)
+        cd = None if cd is None else torch.from_numpy(np.ascontiguousarray(cd).ravel()).to(dev)
+        run(wl, gu_t, dn_t, [(tables(pg), tables(pd))], cg, cd, gu_t,
+            f"sweep_{synth.NAMES[gu_t]}_{synth.NAMES[dn_t]}")
+        del pg, pd
+    torch.cuda.empty_cache()
+    out["method"] = (f"CUDA graph of {calls} fused layer calls (distinct seeded routings, PDL-chained), replayed "
+                     f"{reps} times; bytes = the groups' gate/up + down blobs as stored")
+    return out
+
+
+def qsa_sweep(m, dev, reps=10, calls=32):
+    """QSA decode block scores (moe_qsa_block_scores) at the page's 131k context (32,769 blocks)
+    and at 1M tokens (262,145 blocks), T = 1..4: a CUDA graph of `calls` calls over rotating key
+    pools (264-275 MB in all, more than L2), microseconds per call and the key + scale bytes it
+    reads per microsecond."""
+    out = {}
+    for ctx, nb in synth.QSA_CONTEXTS.items():
+        npool = 8 if nb > 100000 else 64
+        pools = [synth.qsa_keys(nb, 500 + i, device=dev) for i in range(npool)]
+        for T in (1, 2, 3, 4):
+            q = torch.from_numpy(synth.qsa_queries(T, 9)).to(dev)
+            sc = torch.empty((T, nb), dtype=torch.float32, device=dev)
+            fs = [lambda i=i: m.qsa_block_scores(q, pools[i % npool][0], pools[i % npool][1], sc) for i in range(calls)]
+            for f in fs:
+                f()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="relaxed"):
+                for f in fs:
+                    f()
+            g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / (reps * calls)
+            out[f"{ctx}_T{T}"] = {"us": round(us, 2), "GBps": round(nb * 132 / (us * 1e-6) / 1e9, 1)}
+        del pools
+    out["method"] = f"CUDA graph of {calls} calls over rotating int8 key pools, replayed {reps} times"
+    return out
+
+
 def layer_roofline(w, bytes_t, hbm_peak, peak_kind, s, reps=10):
     """The fused layer kernel: the T = 4 window graph (48 launches, one per layer) replayed with
     CUDA events on the launching stream; duration per launch = graph time / 48 (consecutive
@@ -436,7 +580,9 @@ def layer_roofline(w, bytes_t, hbm_peak, peak_kind, s, reps=10):
         synth.blob_bytes(w.gu_type, 2 * WL.F, WL.N) / synth.blob_bytes(GU_T, 2 * WL.F, WL.N) - 1)
     return {"kernel": f"fused layer kernel ({synth.NAMES[w.gu_type]} gate/up slots of CB3, NL4 down, T=4)",
             "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
-            "frac": round(ach / hbm_peak, 4), "traffic": layer_traffic(), "peak_kind": peak_kind,
+            "frac": round(ach / hbm_peak, 4), "traffic": layer_traffic(),
+            "traffic_source": "stored ncu capture of one T=4 launch (dram read + write bytes), null once the "
+                              "kernel sources differ from the captured ones", "peak_kind": peak_kind,
             "bytes_per_launch": int(per_launch), "streamed_bytes_per_launch": int(streamed),
             "streamed_GBps": round(streamed / dur_s / 1e9, 1), "us_per_launch": round(dur_s * 1e6, 2)}
 
@@ -592,8 +738,8 @@ def cpu_baseline(sample_layers=1):
 
 def _reference_worker(w, cores, steps, warmup, bar, q):
     """Worker w of the reference arm: per step, layer (step x cores + w) mod 48 at T = 1..4; the
-    inputs are built first, then every worker starts the oracle at the same barrier, so the
-    step's time is the slowest worker's oracle time on a fully loaded host."""
+    inputs are built first, then every worker starts the oracle at the same barrier and reports
+    its start and end on the host's monotonic clock (shared by all processes)."""
     import oracle
     torch.set_num_threads(1)
     o = oracle.get()
@@ -601,17 +747,28 @@ def _reference_worker(w, cores, steps, warmup, bar, q):
         layer = (max(step, 0) * cores + w) % WL.layers
         inps = [oracle_inputs(o, layer, T) for T in TS]
         bar.wait(timeout=600)  # a worker that died breaks the barrier instead of stalling the rest
-        q.put((step, w, sum(oracle_run(o, inp) for inp in inps)))
+        t0 = time.monotonic()
+        for inp in inps:
+            oracle_run(o, inp)
+        q.put((step, w, t0, time.monotonic()))
+
+
+def reference_procs(requested=None):
+    """Oracle processes of the reference arm: `requested`, else the host's cores capped at 48
+    (each process holds a layer's blobs for T = 1..4, about 0.2 GB)."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    return max(1, min(requested or min(cores, 48), cores))
 
 
 def run_reference(args, rank, world):
-    """The oracle as it stands, on all of the host's cores: one spawned process per core; each
-    step evaluates `cores` consecutive layers (mod 48) at T = 1..4, one layer per process, all
-    started together. us per window = the step's slowest oracle time x 48 / (cores x 4)."""
+    """The oracle as it stands, on the host's cores: one spawned process per core (at most 48, or
+    --ref-procs); each step evaluates `procs` consecutive layers (mod 48) at T = 1..4, one layer
+    per process, all started together. The step's time is the wall time from the barrier's
+    release to the last process's end; us per window = that x 48 / (procs x 4)."""
     if rank != 0:
         return None
     import multiprocessing as mp
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    cores = reference_procs(args.ref_procs)
     ctx = mp.get_context("spawn")
     bar, q = ctx.Barrier(cores), ctx.Queue()
     procs = [ctx.Process(target=_reference_worker, args=(w, cores, args.steps, args.warmup, bar, q), daemon=True)
@@ -621,10 +778,11 @@ def run_reference(args, rank, world):
     res = [q.get(timeout=900) for _ in range(cores * (args.steps + args.warmup))]
     for p in procs:
         p.join(timeout=60)
-    walls = [max(t for st, _, t in res if st == step) for step in range(args.steps)]
+    walls = [max(t1 for st, _, _, t1 in res if st == step) - min(t0 for st, _, t0, _ in res if st == step)
+             for step in range(args.steps)]
     value = float(np.mean(walls)) * WL.layers / (cores * len(TS)) * 1e6
     sample = (f"per step: {cores} consecutive layers (mod 48) at each T=1..4, one per process, started together "
-              f"(inputs built untimed); the slowest process's time, scaled to 48 layers")
+              f"(inputs built untimed); wall time from the start to the last process's end, scaled to 48 layers")
     return {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "us/window", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(float(np.mean(walls)) * 1e3, 2),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "int32 + fp64",
@@ -698,6 +856,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-layers", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-procs", type=int, default=0,
+                    help="reference arm: oracle processes (default: the host's cores, at most 48)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -333,6 +333,26 @@ int moe_router_topk(const float* logits, int T, int n_experts, int k, int32_t* t
 int moe_combine(const float* out, int64_t out_row_stride, const int32_t* topk_ids, const float* weights, int T, int k,
                 int n_experts, int n_embd, float* y, int64_t y_row_stride, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- QSA decode block scores
+ * A second decode workload of the verify window: #2059 "QSA decode: the window's block scores
+ * with the queries in registers and six shuffles per block" ("What changed", "Bit for bit").
+ *  - q: fp32 [T][MOE_QSA_HEADS][MOE_QSA_DIM], the window's queries, 1 <= T <= 4 (16-byte aligned);
+ *  - keys: int8 [n_blocks][MOE_QSA_DIM], one pooled key per block of the context (4-byte
+ *    aligned), key_scale: fp32 [n_blocks] (finite, > 0);
+ *  - scores: fp32 [T][n_blocks].
+ * For query t, block b and head h: lane l (0..31) takes dims 4l..4l+3, p_l = q0*k0, then
+ * p_l = fma(q_i, k_i, p_l) for i = 1, 2, 3 (keys exact in fp32); the 32 partials are summed with
+ * the warp sum's pairings (level j = 16, 8, 4, 2, 1: p_l <- p_l + p_(l xor j)); r_h =
+ * max(dot_h * key_scale[b], 0); scores[t][b] = ((r_0 + r_1) + r_2) + r_3, plus 1e9 on the tail
+ * block b = n_blocks - 1 (so that a top-k selection that follows always keeps it). Each step is
+ * one fp32 rounding in that order, so the result does not depend on the launch. All pointers are
+ * device pointers owned by the caller; nothing is allocated. Errors: MOE_E_NULL, MOE_E_SHAPE (T
+ * outside [1, 4], n_blocks < 1 or > 2^40), MOE_E_ALIGN, MOE_E_CUDA. */
+#define MOE_QSA_HEADS 4
+#define MOE_QSA_DIM 128
+int moe_qsa_block_scores(const float* q, int T, const int8_t* keys, const float* key_scale, int64_t n_blocks,
+                         float* scores, cudaStream_t stream);
+
 /* Test hook: the per-32-block integer sums of `rows` consecutive rows of one blob (row bytes
  * apart) against one q8_1 row xq[K/32], computed by the same device decode and dot-product
  * code as the grouped kernels: isum[r][b] = sum_i w_code_i * q_i (exact int32). */

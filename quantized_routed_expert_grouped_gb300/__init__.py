@@ -19,6 +19,7 @@ __all__ = [
     "quantize_q8_1", "route_group", "grouped_gu", "swiglu_q8_1", "grouped_down",
     "expert_grouped", "ExpertCall", "STATIC_SCRATCH_BYTES", "test_block_isum", "ERR_BITS", "F_PDL",
     "LayerCall", "layer_sync_ints", "router_topk", "combine", "F_SYNC_PAIR", "F_SYNC_ODD", "F_TEST_EXPIRE",
+    "qsa_block_scores",
 ]
 
 Q8_0, Q4B, NL4, CB2, CB3, CB3X, CB2X = 1, 2, 3, 4, 5, 6, 7
@@ -96,9 +97,11 @@ def lib():
         L.moe_layer_sync_ints.restype = _I64
         L.moe_router_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P]
         L.moe_combine.argtypes = [_P, _I64, _P, _P, _I, _I, _I, _I, _P, _I64, _P]
+        L.moe_qsa_block_scores.argtypes = [_P, _I, _P, _P, _I64, _P, _P]
         for f in ("moe_quantize_q8_1", "moe_route_group", "moe_grouped_gu", "moe_swiglu_q8_1",
                   "moe_grouped_down", "moe_expert_grouped", "moe_expert_grouped_static", "moe_test_block_isum",
-                  "moe_transcode_cb", "moe_expert_layer", "moe_router_topk", "moe_combine"):
+                  "moe_transcode_cb", "moe_expert_layer", "moe_router_topk", "moe_combine",
+                  "moe_qsa_block_scores"):
             getattr(L, f).restype = _I
         _LIB = L
     return _LIB
@@ -244,6 +247,17 @@ def combine(out, topk_ids, weights, n_experts, y=None, stream=None):
     _check(lib().moe_combine(_dp(out), out.stride(0), _dp(topk_ids), _dp(weights), T, k, n_experts, N, _dp(y),
                              y.stride(0), _stream(stream)))
     return y
+
+
+def qsa_block_scores(q, keys, key_scale, scores=None, stream=None):
+    """QSA decode block scores: q fp32 [T, 4, 128] (T <= 4), keys int8 [n_blocks, 128], key_scale
+    fp32 [n_blocks] -> scores fp32 [T, n_blocks] on the device (the tail block + 1e9)."""
+    T = q.shape[0]
+    nb = keys.shape[0]
+    if scores is None:
+        scores = torch.empty((T, nb), dtype=torch.float32, device=q.device)
+    _check(lib().moe_qsa_block_scores(_dp(q), T, _dp(keys), _dp(key_scale), nb, _dp(scores), _stream(stream)))
+    return scores
 
 
 def expert_grouped(*args, stream=None, **kw):

@@ -560,6 +560,17 @@ int moe_combine(const float* out, int64_t out_row_stride, const int32_t* topk_id
                : MOE_E_CUDA;
 }
 
+int moe_qsa_block_scores(const float* q, int T, const int8_t* keys, const float* key_scale, int64_t n_blocks,
+                         float* scores, cudaStream_t stream) {
+    if (!q || !keys || !key_scale || !scores) return MOE_E_NULL;
+    if (T < 1 || T > 4 || n_blocks < 1 || n_blocks > (int64_t{1} << 40)) return MOE_E_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(q) & 15u) || (reinterpret_cast<uintptr_t>(keys) & 3u) ||
+        (reinterpret_cast<uintptr_t>(key_scale) & 3u) || (reinterpret_cast<uintptr_t>(scores) & 3u))
+        return MOE_E_ALIGN;
+    return launch_qsa_block_scores(q, T, keys, key_scale, n_blocks, scores, stream) == cudaSuccess ? MOE_OK
+                                                                                                   : MOE_E_CUDA;
+}
+
 int moe_transcode_cb(moe_wfmt src, int dst_type, int K, int rows, int n_blobs, const void* const* src_blobs,
                      void* const* dst_blobs, int32_t* err, cudaStream_t stream) {
     if (!cb_type(src.type) || (dst_type != MOE_CB3X && dst_type != MOE_CB2X)) return MOE_E_TYPE;

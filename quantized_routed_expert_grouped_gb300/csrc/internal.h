@@ -114,6 +114,9 @@ cudaError_t launch_combine(const float* out, int64_t os, const int32_t* ids, con
 cudaError_t launch_transcode_cb(int src_type, const int8_t* codebook, int dst_type, int K, int rows, int n_blobs,
                                 const void* const* src_blobs, void* const* dst_blobs, int32_t* err, cudaStream_t s);
 
+cudaError_t launch_qsa_block_scores(const float* q, int T, const int8_t* keys, const float* scale, long long n_blocks,
+                                    float* scores, cudaStream_t s);
+
 // Per-format grouped GEMV and test-hook launchers (one translation unit per format).
 #define MOE_DECLARE_FORMAT(NAME)                                                                       \
     cudaError_t launch_gemv_##NAME(const GemvArgs& a, int grid, int NT, int smem, cudaStream_t s, bool pdl); \

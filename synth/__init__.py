@@ -196,3 +196,29 @@ WORKLOADS = {
                       tuple((g, d) for g in (Q8_0, Q4B, CB2, CB3) for d in (NL4, Q8_0)),
                       outliers=0.01, seed=55),
 }
+
+
+# ---------------------------------------------------------------- QSA decode block scores
+QSA_HEADS, QSA_DIM = 4, 128
+# contexts of the page's measurements and a longer one: 131k tokens in blocks of 4 tokens plus
+# the tail block (32,769 blocks), and 1M tokens
+QSA_CONTEXTS = {"131k": 32769, "1M": 262145}
+
+
+def qsa_queries(T: int, seed: int) -> np.ndarray:
+    """The window's T queries, fp32 [T, 4 heads, 128], N(0, 1)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return rng.standard_normal((T, QSA_HEADS, QSA_DIM)).astype(np.float32)
+
+
+def qsa_keys(n_blocks: int, seed: int, device="cpu", first_block: int = 0):
+    """Pooled int8 keys [n_blocks, 128], uniform in [-127, 127], and fp32 scales [n_blocks],
+    uniform in [1e-3, 1e-2], from the counter-based generator (the same values on any device;
+    first_block selects a window of a larger pool)."""
+    idx = torch.arange(first_block * QSA_DIM, (first_block + n_blocks) * QSA_DIM, dtype=torch.int64, device=device)
+    z = mix64(seed, idx)
+    keys = ((_srl(z, 32) % 255) - 127).to(torch.int8).view(n_blocks, QSA_DIM)
+    bi = torch.arange(first_block, first_block + n_blocks, dtype=torch.int64, device=device)
+    u = _srl(mix64(seed ^ 0x5CA1E, bi), 40).to(torch.float64) / float(1 << 24)
+    scale = (1e-3 + u * (1e-2 - 1e-3)).to(torch.float32)
+    return keys, scale

@@ -75,6 +75,12 @@ def test_host_argument_errors(m):
     assert L.moe_combine(dummy, 100, dummy, dummy, 4, 8, 128, 2560, dummy, 2560, None) == -3
     assert L.moe_combine(dummy, 2560, dummy, dummy, 70000, 8, 128, 2560, dummy, 2560, None) == -3
     assert L.moe_combine(dummy, 2560, dummy, dummy, 4, 8, 0, 2560, dummy, 2560, None) == -4
+    # QSA block scores
+    assert L.moe_qsa_block_scores(None, 4, dummy, dummy, 100, dummy, None) == -1
+    assert L.moe_qsa_block_scores(dummy, 5, dummy, dummy, 100, dummy, None) == -3   # T > 4
+    assert L.moe_qsa_block_scores(dummy, 0, dummy, dummy, 100, dummy, None) == -3
+    assert L.moe_qsa_block_scores(dummy, 4, dummy, dummy, 0, dummy, None) == -3     # no block
+    assert L.moe_qsa_block_scores(ctypes.c_void_p(20), 4, dummy, dummy, 100, dummy, None) == -6  # q unaligned
 
 
 def test_layer_call_host_errors(m):
