@@ -181,7 +181,7 @@ __device__ __forceinline__ void stage_quad(const GemvArgs& a, uint8_t* smem, int
         float aux = 0.0f;
         if constexpr (Fmt<TYPE>::SLOT) {
             aux = __int_as_float(S * -(2 * Fmt<TYPE>::BIAS - 1));
-        } else if constexpr (Fmt<TYPE>::CB) {
+        } else if constexpr (Fmt<TYPE>::CB || TYPE == MOE_NL4) {
             aux = __int_as_float(S);
         } else if constexpr (TYPE == MOE_Q4B) {
             aux = h2f_bits(hdr >> 16);
@@ -290,7 +290,7 @@ __device__ __forceinline__ void bar_arrive(int id, int threads) {
 // part[(c*4 + e)*RT + lane] for the batch's ne entries, staged in slots[0 .. ne-1].
 template <int TYPE>
 __device__ __forceinline__ void chunk_part(const GemvArgs& a, const uint8_t* smem, const uint8_t* rows, float* part, int ne,
-                                           int c, int lane, uint32_t loff, const uint32_t tab[4], const int slots[4]) {
+                                           int c, int lane, uint32_t loff, const uint32_t tab[kTab], const int slots[4]) {
     if (ne == 1) {
         float acc[1];
         lane_chunk<TYPE, 1>(a, smem, rows, lane, c, loff, tab, slots, acc);
@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
             pcA[x] = static_cast<const uint8_t*>(A.w[x]);
             pcD[x] = static_cast<const uint8_t*>(D.w[x]);
         }
-    uint32_t tabA[4], tabD[4];
+    uint32_t tabA[kTab], tabD[kTab];
     load_table<GT>(A, tabA);
     load_table<DT>(D, tabD);
     __syncthreads();
