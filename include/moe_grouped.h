@@ -311,6 +311,36 @@ int64_t moe_layer_sync_ints(int T, int k, int n_ff);
 
 int moe_expert_layer(const moe_layer_call* call, cudaStream_t stream);
 
+/* One-launch form of moe_expert_grouped (#363 "experts: smaller and fewer launches for the
+ * verify window's PCIe call", "What changes" and "Measured": the layer's second call, with no
+ * group or with one group of two entries, should cost little). The same call - pre-built groups,
+ * a device-side n_groups, entries that may start past 0, scattered destinations, rows outside the
+ * call untouched - runs as one fused launch (gate/up, SwiGLU + q8_1 and down) instead of three, so
+ * an empty call costs one launch. Arguments as moe_expert_grouped, with:
+ *  - grid_groups ignored (one CTA per SM takes the call's work items from a device counter);
+ *  - sync: moe_grouped_fused_sync_ints(cap_groups, cap_entries, n_ff) int32 words, 8-byte aligned,
+ *    zeroed before the first call, used like moe_expert_layer's (MOE_F_SYNC_PAIR / MOE_F_SYNC_ODD
+ *    select halves the same way; the halves are located by cap_groups, cap_entries and n_ff);
+ *  - down format MOE_NL4 or MOE_Q8_0; the n_xq_rows activation rows within moe_expert_layer's
+ *    staging budget for T; max(cap_groups, cap_entries) <= 512 (else MOE_E_CAP); xq 4-byte and gu
+ *    16-byte aligned.
+ * Every gu, hq and out row of a computed group equals moe_expert_grouped's bit for bit. On bad
+ * data one thing differs: a group holding an entry whose source or destination row is out of
+ * range is skipped whole (MOE_ERR_ENTRY), where moe_expert_grouped skips that entry alone. The
+ * launch's CTAs wait on one another as moe_expert_layer's do (bounded, MOE_ERR_TIMEOUT). */
+int64_t moe_grouped_fused_sync_ints(int cap_groups, int cap_entries, int n_ff);
+int moe_expert_grouped_fused(const moe_expert_call* call, int32_t* sync, cudaStream_t stream);
+
+/* The residency split of #363 "experts: smaller and fewer launches for the verify window's PCIe
+ * call" ("What changes": one call for the experts in VRAM, one for those that come over PCIe):
+ * copy n host-resident blobs (an expert's gate/up and down blobs) into device staging slots before
+ * the second call, whose pointer tables name the slots. One cudaMemcpyAsync per blob on `stream`
+ * (host_src should be pinned for the copies to be asynchronous and capturable in a CUDA graph);
+ * dev_dst slots are 16-byte aligned device buffers of at least bytes[i] bytes, owned by the
+ * caller. Errors: MOE_E_NULL, MOE_E_SHAPE (n < 0, a size <= 0), MOE_E_ALIGN (a slot), MOE_E_CUDA. */
+int moe_stage_blobs(const void* const* host_src, void* const* dev_dst, const int64_t* bytes, int n,
+                    cudaStream_t stream);
+
 /* ---------------------------------------------------------------- the steps either side
  * The router before the grouped call and the combine after it. The pages do not define the
  * router; this library takes the plainest reading. "The combined output" is what #3455 "GP100

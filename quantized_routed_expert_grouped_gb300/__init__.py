@@ -19,7 +19,7 @@ __all__ = [
     "quantize_q8_1", "route_group", "grouped_gu", "swiglu_q8_1", "grouped_down",
     "expert_grouped", "ExpertCall", "STATIC_SCRATCH_BYTES", "test_block_isum", "ERR_BITS", "F_PDL",
     "LayerCall", "layer_sync_ints", "router_topk", "combine", "F_SYNC_PAIR", "F_SYNC_ODD", "F_TEST_EXPIRE",
-    "qsa_block_scores",
+    "qsa_block_scores", "grouped_fused_sync_ints", "stage_blobs",
 ]
 
 Q8_0, Q4B, NL4, CB2, CB3, CB3X, CB2X = 1, 2, 3, 4, 5, 6, 7
@@ -98,10 +98,14 @@ def lib():
         L.moe_router_topk.argtypes = [_P, _I, _I, _I, _P, _P, _P]
         L.moe_combine.argtypes = [_P, _I64, _P, _P, _I, _I, _I, _I, _P, _I64, _P]
         L.moe_qsa_block_scores.argtypes = [_P, _I, _P, _P, _I64, _P, _P]
+        L.moe_expert_grouped_fused.argtypes = [ctypes.POINTER(ExpertCallC), _P, _P]
+        L.moe_grouped_fused_sync_ints.argtypes = [_I, _I, _I]
+        L.moe_grouped_fused_sync_ints.restype = _I64
+        L.moe_stage_blobs.argtypes = [_P, _P, _P, _I, _P]
         for f in ("moe_quantize_q8_1", "moe_route_group", "moe_grouped_gu", "moe_swiglu_q8_1",
                   "moe_grouped_down", "moe_expert_grouped", "moe_expert_grouped_static", "moe_test_block_isum",
                   "moe_transcode_cb", "moe_expert_layer", "moe_router_topk", "moe_combine",
-                  "moe_qsa_block_scores"):
+                  "moe_qsa_block_scores", "moe_expert_grouped_fused", "moe_stage_blobs"):
             getattr(L, f).restype = _I
         _LIB = L
     return _LIB
@@ -191,10 +195,32 @@ class ExpertCall:
     def __call__(self, stream=None):
         _check(lib().moe_expert_grouped(ctypes.byref(self.c), _stream(stream)))
 
+    def call_fused(self, sync, stream=None):
+        """The same call in one fused launch (moe_expert_grouped_fused); sync: int32 device tensor
+        of grouped_fused_sync_ints(cap_groups, cap_entries, n_ff) words, zeroed before the first
+        call (flags MOE_F_SYNC_PAIR / MOE_F_SYNC_ODD in self.c.flags select its halves)."""
+        _check(lib().moe_expert_grouped_fused(ctypes.byref(self.c), _dp(sync), _stream(stream)))
+
     def call_static(self, stream=None):
         """The same call through moe_expert_grouped_static: gu/hq are ignored and the library's
         static device scratch buffer is used instead (nothing is allocated)."""
         _check(lib().moe_expert_grouped_static(ctypes.byref(self.c), _stream(stream)))
+
+
+def stage_blobs(host_blobs, dev_slots, stream=None):
+    """Copy host-resident blobs (pinned uint8 CPU tensors) into device staging slots (uint8 CUDA
+    tensors, at least as large), one cudaMemcpyAsync each (moe_stage_blobs)."""
+    n = len(host_blobs)
+    assert len(dev_slots) == n and all(d.numel() >= h.numel() for h, d in zip(host_blobs, dev_slots))
+    src = (ctypes.c_void_p * n)(*[h.data_ptr() for h in host_blobs])
+    dst = (ctypes.c_void_p * n)(*[d.data_ptr() for d in dev_slots])
+    by = (ctypes.c_int64 * n)(*[h.numel() * h.element_size() for h in host_blobs])
+    _check(lib().moe_stage_blobs(src, dst, by, n, _stream(stream)))
+
+
+def grouped_fused_sync_ints(cap_groups: int, cap_entries: int, n_ff: int) -> int:
+    """int32 sync words a moe_expert_grouped_fused call needs (zero them before the first call)."""
+    return int(lib().moe_grouped_fused_sync_ints(cap_groups, cap_entries, n_ff))
 
 
 def layer_sync_ints(T: int, k: int, n_ff: int) -> int:

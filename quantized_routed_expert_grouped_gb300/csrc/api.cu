@@ -254,8 +254,10 @@ constexpr int kUnitBytes = 4 * 4 * 32 * 4;  // gate/up unit buffers (4 units x 4
 constexpr int kLayerThreads = 512;   // producer warp + 15 consumer warps
 constexpr int kBatch = 4;            // entries staged per down batch
 
-int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, int& NT, int& smem) {
-    const int n = T * k;
+// T activation rows; tables for n_tables entries and groups (0: T * k, a routed window's)
+int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, int& NT, int& smem,
+               int n_tables = 0) {
+    const int n = n_tables > 0 ? n_tables : T * k;
     if (n <= 0 || n > kLayerMaxEntries) return MOE_E_CAP;
     GemvArgs& A = L.gu;
     GemvArgs& D = L.dn;
@@ -475,6 +477,50 @@ int64_t moe_layer_sync_ints(int T, int k, int n_ff) {
     return kSyncHx + static_cast<int64_t>(T) * k * (n_ff / 32) * kHxPairs * 2;
 }
 
+// The fused launch shared by moe_expert_layer (routed from ids) and moe_expert_grouped_fused
+// (pre-built groups): formats, pointers and geometry already checked.
+static int launch_fused(moe_wfmt gu_fmt, moe_wfmt down_fmt, int n_embd, int n_ff, int n_experts, const void* const* w_gu,
+                        const void* const* w_down, LayerArgs& L, int NT, int smem, float* gu, int64_t gu_rows,
+                        const moe_q8_1* act, float* out, int64_t out_rows, int64_t out_row_stride, moe_q8_1* hq,
+                        int32_t* sync, int64_t half, int32_t* err, int32_t flags, cudaStream_t stream) {
+    int ctas = 0;
+    if (layer_occupancy(gu_fmt.type, down_fmt.type, NT, smem, &ctas) != cudaSuccess || ctas < 1) return MOE_E_CUDA;
+    const int sms = sm_count();
+    if (sms <= 0) return MOE_E_CUDA;
+    GemvArgs& A = L.gu;
+    GemvArgs& D = L.dn;
+    A.w = w_gu;
+    D.w = w_down;
+    A.n_experts = D.n_experts = n_experts;
+    A.codebook = gu_fmt.codebook;
+    D.codebook = down_fmt.codebook;
+    A.err = D.err = err;
+    A.act = act;
+    A.n_act_rows = L.T;
+    A.out = gu;
+    A.out_rows = gu_rows;
+    A.out_stride = 2 * static_cast<int64_t>(n_ff);
+    D.act = hq;
+    D.n_act_rows = L.n;
+    D.out = out;
+    D.out_rows = out_rows;
+    D.out_stride = out_row_stride;
+    L.hq = hq;
+    L.sync = sync;
+    L.sync_other = nullptr;
+    if (flags & MOE_F_SYNC_PAIR) {  // two halves; this call uses one and zeroes the other
+        const bool odd = (flags & MOE_F_SYNC_ODD) != 0;
+        L.sync = sync + (odd ? half : 0);
+        L.sync_other = sync + (odd ? 0 : half);
+    }
+    L.test_expire = (flags & MOE_F_TEST_EXPIRE) != 0;
+    // one CTA per SM (co-resident), split on the device between the gate/up and the down roles
+    const bool pdl = (flags & MOE_F_PDL) != 0;
+    if (launch_layer(gu_fmt.type, down_fmt.type, L, sms, NT, smem, stream, pdl) != cudaSuccess) return MOE_E_CUDA;
+    (void)n_embd;
+    return MOE_OK;
+}
+
 int moe_expert_layer(const moe_layer_call* c, cudaStream_t stream) {
     if (!c) return MOE_E_NULL;
     int rc;
@@ -492,52 +538,73 @@ int moe_expert_layer(const moe_layer_call* c, cudaStream_t stream) {
     int NT = 0, smem = 0;
     if ((rc = plan_layer(c->gu_fmt.type, c->down_fmt.type, c->n_embd, c->n_ff, c->T, c->k, c->n_experts, L, NT, smem)))
         return rc;
-    int ctas = 0;
-    if (layer_occupancy(c->gu_fmt.type, c->down_fmt.type, NT, smem, &ctas) != cudaSuccess || ctas < 1)
-        return MOE_E_CUDA;
-    const int sms = sm_count();
-    if (sms <= 0) return MOE_E_CUDA;
-    GemvArgs& A = L.gu;
-    GemvArgs& D = L.dn;
-    A.w = c->w_gu;
-    D.w = c->w_down;
-    A.n_experts = D.n_experts = c->n_experts;
-    A.codebook = c->gu_fmt.codebook;
-    D.codebook = c->down_fmt.codebook;
-    A.err = D.err = c->err;
-    A.n_act_rows = c->T;
-    A.out = c->gu;
-    A.out_rows = L.n;
-    A.out_stride = 2 * static_cast<int64_t>(c->n_ff);
-    D.act = c->hq;
-    D.n_act_rows = L.n;
-    D.out = c->out;
-    D.out_rows = L.n;
-    D.out_stride = c->out_row_stride;
     L.ids = c->topk_ids;
     L.x = c->x;
-    L.hq = c->hq;
-    L.sync = c->sync;
-    L.sync_other = nullptr;
-    if (c->flags & MOE_F_SYNC_PAIR) {  // two halves; this call uses one and zeroes the other
-        const int64_t half = moe_layer_sync_ints(c->T, c->k, c->n_ff);
-        const bool odd = (c->flags & MOE_F_SYNC_ODD) != 0;
-        L.sync = c->sync + (odd ? half : 0);
-        L.sync_other = c->sync + (odd ? 0 : half);
-    }
     L.o_ge = c->grp_expert;
     L.o_gs = c->grp_start;
     L.o_ng = c->n_groups;
     L.o_es = c->ent_src;
     L.o_ed = c->ent_dst;
     L.o_xq = c->xq;
-    L.test_expire = (c->flags & MOE_F_TEST_EXPIRE) != 0;
-    // one CTA per SM (co-resident), split on the device between the gate/up and the down roles
-    const int64_t grid = sms;
-    const bool pdl = (c->flags & MOE_F_PDL) != 0;
-    if (launch_layer(c->gu_fmt.type, c->down_fmt.type, L, static_cast<int>(grid), NT, smem, stream, pdl) !=
-        cudaSuccess)
-        return MOE_E_CUDA;
+    return launch_fused(c->gu_fmt, c->down_fmt, c->n_embd, c->n_ff, c->n_experts, c->w_gu, c->w_down, L, NT, smem,
+                        c->gu, L.n, nullptr, c->out, L.n, c->out_row_stride, c->hq, c->sync,
+                        moe_layer_sync_ints(c->T, c->k, c->n_ff), c->err, c->flags, stream);
+}
+
+int64_t moe_grouped_fused_sync_ints(int cap_groups, int cap_entries, int n_ff) {
+    if (cap_groups <= 0 || cap_entries <= 0) return 0;
+    return moe_layer_sync_ints(cap_groups > cap_entries ? cap_groups : cap_entries, 1, n_ff);
+}
+
+int moe_expert_grouped_fused(const moe_expert_call* c, int32_t* sync, cudaStream_t stream) {
+    if (!c) return MOE_E_NULL;
+    int rc;
+    if ((rc = check_fmt(c->gu_fmt)) || (rc = check_fmt(c->down_fmt))) return rc;
+    if (c->down_fmt.type != MOE_NL4 && c->down_fmt.type != MOE_Q8_0) return MOE_E_TYPE;
+    if ((rc = check_dims(c->n_embd, c->n_ff))) return rc;
+    if (!c->w_gu || !c->w_down || !c->grp_expert || !c->grp_start || !c->n_groups || !c->xq || !c->ent_src ||
+        !c->ent_dst || !c->gu || !c->hq || !c->out || !sync)
+        return MOE_E_NULL;
+    if (c->n_experts <= 0 || c->n_experts > (1 << 26) || c->cap_groups <= 0 || c->cap_entries <= 0 ||
+        c->n_xq_rows <= 0 || c->out_rows <= 0)
+        return MOE_E_CAP;
+    if (c->out_row_stride < c->n_embd) return MOE_E_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(c->xq) & 3u) || (reinterpret_cast<uintptr_t>(c->gu) & 15u)) return MOE_E_ALIGN;
+    if (reinterpret_cast<uintptr_t>(sync) & 7u) return MOE_E_ALIGN;
+    const int n = c->cap_groups > c->cap_entries ? c->cap_groups : c->cap_entries;
+    LayerArgs L = {};
+    int NT = 0, smem = 0;
+    if ((rc = plan_layer(c->gu_fmt.type, c->down_fmt.type, c->n_embd, c->n_ff, c->n_xq_rows, 1, c->n_experts, L, NT,
+                         smem, n)))
+        return rc;
+    L.given = 1;
+    L.g_expert = c->grp_expert;
+    L.g_start = c->grp_start;
+    L.g_ng = c->n_groups;
+    L.g_src = c->ent_src;
+    L.g_dst = c->ent_dst;
+    L.g_cap_groups = c->cap_groups;
+    L.g_cap_entries = c->cap_entries;
+    L.g_out_rows = c->out_rows;
+    return launch_fused(c->gu_fmt, c->down_fmt, c->n_embd, c->n_ff, c->n_experts, c->w_gu, c->w_down, L, NT, smem,
+                        c->gu, c->cap_entries, c->xq, c->out, c->out_rows, c->out_row_stride, c->hq, sync,
+                        moe_grouped_fused_sync_ints(c->cap_groups, c->cap_entries, c->n_ff), c->err, c->flags,
+                        stream);
+}
+
+int moe_stage_blobs(const void* const* host_src, void* const* dev_dst, const int64_t* bytes, int n,
+                    cudaStream_t stream) {
+    if (n < 0) return MOE_E_SHAPE;
+    if (n > 0 && (!host_src || !dev_dst || !bytes)) return MOE_E_NULL;
+    for (int i = 0; i < n; ++i) {
+        if (!host_src[i] || !dev_dst[i]) return MOE_E_NULL;
+        if (bytes[i] <= 0) return MOE_E_SHAPE;
+        if (reinterpret_cast<uintptr_t>(dev_dst[i]) & 15u) return MOE_E_ALIGN;
+    }
+    for (int i = 0; i < n; ++i)
+        if (cudaMemcpyAsync(dev_dst[i], host_src[i], static_cast<size_t>(bytes[i]), cudaMemcpyHostToDevice, stream) !=
+            cudaSuccess)
+            return MOE_E_CUDA;
     return MOE_OK;
 }
 

@@ -97,6 +97,12 @@ struct LayerArgs {
     int off_unit;        // shared-memory gate/up unit buffers: [4 units][4 entries][32] h values
     int off_ptr;         // shared-memory cache of both expert pointer tables (0: not cached)
     int test_expire;     // test hook: the down staging waits for a flag no call writes
+    // pre-built groups (moe_expert_grouped_fused): given = 1 reads the grouping and the activation
+    // q8_1 rows from these instead of routing ids and quantizing x
+    int given;
+    const int32_t *g_expert, *g_start, *g_ng, *g_src, *g_dst;
+    int g_cap_groups, g_cap_entries;
+    int64_t g_out_rows;
 };
 
 cudaError_t launch_quantize_q8_1(const float* x, int64_t rows, int64_t cols, moe_q8_1* xq, cudaStream_t s,

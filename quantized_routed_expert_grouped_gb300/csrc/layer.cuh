@@ -282,6 +282,71 @@ __device__ __forceinline__ void build_tables(const LayerArgs& L, const uint8_t* 
     __syncwarp();
 }
 
+// Pre-built groups of a grouped call (warp 0), checked as the separate kernels check them: the
+// count clamped to [0, cap_groups] (MOE_ERR_NGROUPS); a group is skipped when its expert id is out
+// of range (MOE_ERR_EXPERT), its entries do not lie in [grp_start[0], cap_entries] in order
+// (MOE_ERR_START), its weight pointers are misaligned (MOE_ERR_ALIGN) or one of its entries has a
+// source row outside the activation rows or a destination outside the output rows
+// (MOE_ERR_ENTRY; the whole group, where the separate kernels skip the entry alone). The tables
+// number entries from grp_start[0] (*ebase), like a routed call's from 0.
+template <int GT, int DT>
+__device__ __forceinline__ void load_groups(const LayerArgs& L, const uint8_t* const* pcA, const uint8_t* const* pcD,
+                                            GroupInfo* giA, GroupInfo* giD, int2* entA, int2* entD, int* rng,
+                                            int* ebase, int lane) {
+    const GemvArgs& A = L.gu;
+    const GemvArgs& D = L.dn;
+    const bool report = blockIdx.x == 0;
+    int G = *L.g_ng;
+    if (G < 0 || G > L.g_cap_groups) {
+        if (report && lane == 0) set_err(A.err, MOE_ERR_NGROUPS);
+        G = G < 0 ? 0 : L.g_cap_groups;
+    }
+    const int base = G > 0 ? L.g_start[0] : 0;
+    for (int g = lane; g < G; g += 32) {
+        const int x = L.g_expert[g], e0 = L.g_start[g], e1 = L.g_start[g + 1];
+        bool ok = true;
+        const uint8_t* pa = nullptr;
+        const uint8_t* pd = nullptr;
+        if (x < 0 || x >= A.n_experts) {
+            ok = false;
+            if (report) set_err(A.err, MOE_ERR_EXPERT);
+        } else if (base < 0 || e0 < base || e1 < e0 || e1 > L.g_cap_entries || e1 - base > L.n) {
+            ok = false;
+            if (report) set_err(A.err, MOE_ERR_START);
+        } else if (e1 == e0) {
+            ok = false;
+        } else {
+            pa = pcA ? pcA[x] : static_cast<const uint8_t*>(A.w[x]);
+            pd = pcD ? pcD[x] : static_cast<const uint8_t*>(D.w[x]);
+            if ((reinterpret_cast<uintptr_t>(pa) | reinterpret_cast<uintptr_t>(pd)) & 15u) {
+                ok = false;
+                if (report) set_err(A.err, MOE_ERR_ALIGN);
+            } else {
+                for (int e = e0; e < e1; ++e) {
+                    const int sr = L.g_src[e], ds = L.g_dst[e];
+                    if (sr < 0 || sr >= L.T || ds < 0 || ds >= L.g_out_rows) {
+                        ok = false;
+                        if (report) set_err(A.err, MOE_ERR_ENTRY);
+                        break;
+                    }
+                }
+            }
+        }
+        giA[g] = GroupInfo{pa, x, e0 - base, e1 - base, ok ? 1 : 0};
+        giD[g] = GroupInfo{pd, x, e0 - base, e1 - base, ok ? 1 : 0};
+        if (ok)
+            for (int e = e0; e < e1; ++e) {
+                entA[e - base] = make_int2(L.g_src[e], e - base);
+                entD[e - base] = make_int2(e - base, L.g_dst[e]);
+            }
+    }
+    if (lane == 0) {
+        *rng = G;
+        *ebase = base;
+    }
+    __syncwarp();
+}
+
 __device__ __forceinline__ void bar_arrive(int id, int threads) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -308,7 +373,10 @@ __device__ __forceinline__ void chunk_part(const GemvArgs& a, const uint8_t* sme
     }
 }
 
-template <int GT, int DT>
+// GIVEN: the grouping and the activation q8_1 come from the caller (moe_expert_grouped_fused)
+// instead of routing ids and quantizing x (moe_expert_layer); a template parameter, so that each
+// form's kernel carries only its own code.
+template <int GT, int DT, bool GIVEN>
 __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const GemvArgs& A = L.gu;
@@ -322,7 +390,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     uint64_t* ufree = dread + kDescRing;  // unit buffer u free again (its unit's h blocks written)
     uint64_t* pub = ufree + kUnitBufs;    // descriptor d published (or the stream ended there)
     // misc: [0] ring indices published, [1] abort flag, [2] last-CTA flag, [3] the call's flag in
-    // the flagged h copies, [5] no more tiles,
+    // the flagged h copies, [5] no more tiles, [12] the first entry of pre-built groups,
     // [6] copies issued, [7] work items published, [8] work items taken, [16 + u] tiles done of the
     // gate/up unit in buffer u, [32 + s] sub-tiles done of slot s, [64 + 8s + b] chunks done of
     // (sub-)tile b of slot s, [128 + 8d ..] descriptor d of ring index q (d = q % kDescRing)
@@ -375,7 +443,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
 
     // ---- routing/grouping and tables: one warp when n <= 32, else the whole CTA routes and
     // warp 0 builds the tables
-    if (n > 32) {
+    if (!GIVEN && n > 32) {
         route_cta(L.ids, n, L.k, A.n_experts, 0, sid, sfirst, scount, rgx, rgs, rng, rsrc, rdst, A.err,
                   blockIdx.x == 0);
         __syncthreads();
@@ -386,12 +454,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     uint32_t flag = 0;
     if (warp == 0) {
         if (lane == 0) flag = 1u + static_cast<uint32_t>(__ldcg(L.sync + kSyncEpoch));
-        if (n <= 32) route_warp(L.ids, n, L.k, A.n_experts, rgx, rgs, rng, rsrc, rdst, A.err, blockIdx.x == 0, lane);
+        if (!GIVEN && n <= 32)
+            route_warp(L.ids, n, L.k, A.n_experts, rgx, rgs, rng, rsrc, rdst, A.err, blockIdx.x == 0, lane);
         __syncwarp();
         // The CTA's first work item is its own index. When that is a gate/up unit, its first tile
         // needs only the group's expert id, so it is copied now, before the tables are built; the
         // producer publishes it without copying again.
-        if (lane == 0 && static_cast<int>(blockIdx.x) < *rng * upg) {
+        if (!GIVEN && lane == 0 && static_cast<int>(blockIdx.x) < *rng * upg) {
             const int g = static_cast<int>(blockIdx.x) / upg, jb = static_cast<int>(blockIdx.x) - g * upg;
             const int x = rgx[g];
             const uint8_t* pa = pcA ? pcA[x] : static_cast<const uint8_t*>(A.w[x]);
@@ -413,7 +482,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 vmisc[6] = early;
             }
         }
-        build_tables<GT, DT>(L, pcA, pcD, rgx, rgs, rng, rsrc, rdst, giA, giD, entA, entD, misc, lane);
+        if constexpr (GIVEN) load_groups<GT, DT>(L, pcA, pcD, giA, giD, entA, entD, rng, &misc[12], lane);
+        else build_tables<GT, DT>(L, pcA, pcD, rgx, rgs, rng, rsrc, rdst, giA, giD, entA, entD, misc, lane);
         if (lane == 0) misc[3] = static_cast<int>(flag);
         flag = __shfl_sync(0xffffffffu, flag, 0);
         __threadfence_block();
@@ -422,7 +492,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         // meanwhile the consumer warps quantize the activations (independent of the grouping)
         const int ct = tid - 32, cnt = NT - 32;
         // ---- activations: x -> q8_1 of all T tokens, staged in slot t; one lane quad per block
-        {
+        // (pre-built groups: the caller's q8_1 rows, staged as they are)
+        if constexpr (GIVEN) {
+            for (int i = ct; i < L.T * A.nb; i += cnt) {
+                const int r = i / A.nb;
+                stage_block<GT>(A, smem, r, r, i - r * A.nb);
+            }
+        } else {
             const int nb = A.nb, j = ct & 3, nq = cnt >> 2, tot = L.T * nb;
             const unsigned qmask = 0xFu << (lane & 28);
             for (int i0 = ct >> 2; i0 < tot; i0 += 4 * nq) {
@@ -457,6 +533,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         flag = static_cast<uint32_t>(vmisc[3]);
     }
     const int G = *rng;
+    // global index of the tables' entry 0 (pre-built groups: grp_start[0]), for the scratch rows
+    const int ebase = GIVEN ? misc[12] : 0;
     // ---- one stream of work items for the whole grid, taken in order from a global counter:
     // gate/up units (group-major), then down chunks of dchunk tiles of one group (group-major).
     // Each CTA's producer warp pulls items and streams their tiles through the ring, publishing a
@@ -749,7 +827,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     if (e >= ne) break;
-                    if (lane < RT) A.out[static_cast<int64_t>(e0 + e) * gst + rowg] = v[e];
+                    if (lane < RT) A.out[static_cast<int64_t>(ebase + e0 + e) * gst + rowg] = v[e];
                     const float uv = __shfl_down_sync(0xffffffffu, v[e], half);
                     if (lane < half) ub[e * 32 + h * half + lane] = swiglu_rn(v[e], uv);
                 }
@@ -767,7 +845,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                     uint32_t hdr;
                     int Ssum;
                     const int qv = warp_q8_1_code(ub[e * 32 + lane], hdr, Ssum);
-                    moe_q8_1* dst = L.hq + static_cast<int64_t>(e0 + e) * L.nbj + jb;
+                    moe_q8_1* dst = L.hq + static_cast<int64_t>(ebase + e0 + e) * L.nbj + jb;
                     dst->q[lane] = static_cast<int8_t>(qv);
                     if (lane == 0) *reinterpret_cast<uint32_t*>(dst) = hdr;
                     uint32_t cw = (static_cast<uint32_t>(qv) & 0xFFu) << (8 * (lane & 3));
@@ -849,21 +927,29 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     }
 }
 
-template <int GT, int DT>
-cudaError_t launch_layer_t(const LayerArgs& args, int grid, int NT, int smem, cudaStream_t s, bool pdl) {
+template <int GT, int DT, bool GIVEN>
+cudaError_t launch_layer_g(const LayerArgs& args, int grid, int NT, int smem, cudaStream_t s, bool pdl) {
     LayerArgs a = args;
     a.gu.alpha = Fmt<GT>::ALPHA;
     a.dn.alpha = Fmt<DT>::ALPHA;
-    cudaError_t e = cudaFuncSetAttribute(layer_kernel<GT, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(layer_kernel<GT, DT, GIVEN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_kernel(layer_kernel<GT, DT>, dim3(grid), dim3(NT), static_cast<size_t>(smem), s, pdl, a);
+    return launch_kernel(layer_kernel<GT, DT, GIVEN>, dim3(grid), dim3(NT), static_cast<size_t>(smem), s, pdl, a);
+}
+
+template <int GT, int DT>
+cudaError_t launch_layer_t(const LayerArgs& args, int grid, int NT, int smem, cudaStream_t s, bool pdl) {
+    return args.given ? launch_layer_g<GT, DT, true>(args, grid, NT, smem, s, pdl)
+                      : launch_layer_g<GT, DT, false>(args, grid, NT, smem, s, pdl);
 }
 
 template <int GT, int DT>
 cudaError_t layer_occupancy_t(int NT, int smem, int* ctas) {
-    cudaError_t e = cudaFuncSetAttribute(layer_kernel<GT, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(layer_kernel<GT, DT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, layer_kernel<GT, DT>, NT, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, layer_kernel<GT, DT, false>, NT, smem);
 }
 
 }  // namespace moe
