@@ -367,7 +367,10 @@ def sparse_calls(m, dev, reps=20):
     moe_expert_grouped calls (gate/up, SwiGLU + q8_1, down chained with PDL), each with a
     device-side n_groups of 0 (empty) or 1 (one group of 2 entries numbered after the first call's
     32, scattered destinations, its own expert from a 558 MB pool read cold), with grid_groups 0
-    (the capacity) and 1. Microseconds per call from CUDA events around graph replays."""
+    (the capacity) and 1; then ("fused") the same calls as one moe_expert_grouped_fused launch
+    each, and the residency split: each call's expert copied from pinned host memory into a device
+    staging slot (moe_stage_blobs) before its call, copies and calls in one graph. Microseconds per
+    call from CUDA events around graph replays."""
     wl = synth.WORKLOADS["sparse"]
     gu_t, dn_t = wl.pairs[0]
     E, calls, n = 256, 48, 4 * wl.k
@@ -416,6 +419,60 @@ def sparse_calls(m, dev, reps=20):
         key = ("empty" if ng == 0 else "one_group_2_entries") + ("_grid_groups_1" if gg else "")
         res[key] = round(a.elapsed_time(b) * 1e3 / (reps * calls), 2)
     res.update({"unit": "us/call", "calls_per_graph": calls, "launches_per_call": 3})
+
+    def graph_us(run):
+        run()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            run()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        if int(err.item()):
+            raise RuntimeError(f"sparse calls: device error bits {int(err.item())}")
+        return round(a.elapsed_time(b) * 1e3 / (reps * calls), 2)
+
+    # the same calls in one fused launch each (moe_expert_grouped_fused, alternate sync halves)
+    sync = torch.zeros(2 * m.grouped_fused_sync_ints(n, cap_e, wl.F), **i32)
+    fused = {}
+    for ng in (0, 1):
+        ngt = torch.full((1,), ng, **i32)
+        ges = [torch.tensor([(5 * c) % E] + [0] * (n - 1), **i32) for c in range(calls)]
+        cs = [m.ExpertCall(gu_t, cb_gu, dn_t, cb_dn, wl.N, wl.F, tab_gu, tab_dn, E, ges[c], gs, ngt, n, 0, cap_e, xq,
+                           es, ed, gu, hq, out, err, m.F_PDL | m.F_SYNC_PAIR | (m.F_SYNC_ODD if c % 2 else 0))
+              for c in range(calls)]
+        fused["empty" if ng == 0 else "one_group_2_entries"] = graph_us(lambda: [c.call_fused(sync) for c in cs])
+    # the residency split: each call's expert is host-resident (pinned), copied into a device
+    # staging slot (one cudaMemcpyAsync per blob) before its one-launch call, all in the graph
+    host_gu = [synth.weight_blobs(gu_t, 2 * wl.F, wl.N, 1, synth.derive_key(wl.seed, 0, gu_t, 0), "cpu",
+                                  first_blob=(7 * c) % E)[0].pin_memory() for c in range(calls)]
+    host_dn = [synth.weight_blobs(dn_t, wl.N, wl.F, 1, synth.derive_key(wl.seed, 0, dn_t, 1), "cpu",
+                                  first_blob=(7 * c) % E)[0].pin_memory() for c in range(calls)]
+    slot_gu = torch.empty(host_gu[0].numel(), dtype=torch.uint8, device=dev)
+    slot_dn = torch.empty(host_dn[0].numel(), dtype=torch.uint8, device=dev)
+    stab_gu = torch.full((E,), slot_gu.data_ptr(), dtype=torch.int64, device=dev)
+    stab_dn = torch.full((E,), slot_dn.data_ptr(), dtype=torch.int64, device=dev)
+    ngt = torch.ones(1, **i32)
+    ges = [torch.tensor([(7 * c) % E] + [0] * (n - 1), **i32) for c in range(calls)]
+    cs = [m.ExpertCall(gu_t, cb_gu, dn_t, cb_dn, wl.N, wl.F, stab_gu, stab_dn, E, ges[c], gs, ngt, n, 0, cap_e, xq,
+                       es, ed, gu, hq, out, err, m.F_PDL | m.F_SYNC_PAIR | (m.F_SYNC_ODD if c % 2 else 0))
+          for c in range(calls)]
+
+    def staged():
+        for c in range(calls):
+            m.stage_blobs([host_gu[c], host_dn[c]], [slot_gu, slot_dn])
+            cs[c].call_fused(sync)
+    fused["host_staged_one_group_2_entries"] = graph_us(staged)
+    fused["host_staged_bytes_per_call"] = int(host_gu[0].numel() + host_dn[0].numel())
+    fused.update({"unit": "us/call", "calls_per_graph": calls, "launches_per_call": 1})
+    res["fused"] = fused
     return res
 
 
@@ -839,9 +896,27 @@ def run_case(args):
         m.quantize_q8_1(x, xq)
         call()
     torch.cuda.synchronize()
+    extra = {}
+    if args.case_aux:
+        # the kernels around the path, once per step each on the same layer's shapes: router top-k
+        # (T x 128 logits), the weighted combine (T x 8 rows of 2560), the load-time transcoding of
+        # the layer's 128 CB3 gate/up blobs to CB3X (200 MB read), and QSA block scores at 1M tokens
+        logits = torch.from_numpy(np.random.default_rng(3).standard_normal((T, WL.E)).astype(np.float32)).to(dev)
+        pool_tx = torch.empty((WL.E, synth.blob_bytes(XT, 2 * WL.F, WL.N)), dtype=torch.uint8, device=dev)
+        nb = synth.QSA_CONTEXTS["1M"]
+        qk, qs = synth.qsa_keys(nb, 77, device=dev)
+        qq = torch.from_numpy(synth.qsa_queries(T, 5)).to(dev)
+        for _ in range(args.steps):
+            tid, tw = m.router_topk(logits, WL.k)
+            y = m.combine(out, tid, tw, WL.E)
+            m.transcode_cb(GU_T, cb_gu, XT, WL.N, 2 * WL.F, tab(pool_gu), tab(pool_tx), err)
+            sc = m.qsa_block_scores(qq, qk, qs)
+        torch.cuda.synchronize()
+        extra = {"aux": "router_topk, combine, transcode (CB3 -> CB3X, 128 experts), qsa (1M tokens)",
+                 "y_finite": bool(torch.isfinite(y).all().item()), "scores": int(sc.numel())}
     print(json.dumps({"case": f"one layer of window48 at T={T}" + (" (fused)" if args.case_fused else ""),
                       "err": int(err.item()),
-                      "groups": int(ng.item())}))
+                      "groups": int(ng.item()), **extra}))
 
 
 def main():
@@ -850,6 +925,8 @@ def main():
     ap.add_argument("--case-t", type=int, default=4)
     ap.add_argument("--case-slot", action="store_true", help="profiling case with the gate/up pool in slot layout")
     ap.add_argument("--case-fused", action="store_true", help="profiling case with the fused layer launch")
+    ap.add_argument("--case-aux", action="store_true",
+                    help="profiling case: also run the router, combine, transcoding and QSA kernels")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
