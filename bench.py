@@ -158,11 +158,13 @@ class Window:
     """Device state of one T: inputs, routing outputs, scratch and the captured 48-layer graph.
 
     fused: each layer is one moe_expert_layer launch (routing, q8_1, gate/up, SwiGLU + q8_1, down);
-    otherwise each layer is moe_route_group + moe_quantize_q8_1 + moe_expert_grouped (5 launches)."""
+    otherwise each layer is moe_route_group + moe_quantize_q8_1 + moe_expert_grouped (5 launches),
+    or, with grouped_fused, moe_route_group + moe_quantize_q8_1 + moe_expert_grouped_fused (3)."""
 
-    def __init__(self, m, T, tab_gu, tab_dn, cb_gu, cb_dn, dev, gu_type=GU_T, fused=True):
+    def __init__(self, m, T, tab_gu, tab_dn, cb_gu, cb_dn, dev, gu_type=GU_T, fused=True, grouped_fused=False):
         self.T = T
         self.fused = fused
+        self.grouped_fused = grouped_fused
         L, n = WL.layers, T * WL.k
         i32 = dict(dtype=torch.int32, device=dev)
         self.ids_h = torch.from_numpy(np.stack([routing_for(l, T) for l in range(L)])).pin_memory()
@@ -187,6 +189,10 @@ class Window:
         # a pair of counter halves: layer l uses half l % 2 and zeroes the other (48 layers: the
         # halves alternate across graph replays too)
         self.sync = torch.zeros(2 * m.layer_sync_ints(T, WL.k, WL.F), **i32)
+        if grouped_fused:  # one-launch expert calls on alternate halves of their own sync pair
+            self.gsync = torch.zeros(2 * m.grouped_fused_sync_ints(n, n, WL.F), **i32)
+            for l, c in enumerate(self.calls):
+                c.c.flags = m.F_PDL | m.F_SYNC_PAIR | (m.F_SYNC_ODD if l % 2 else 0)
         self.lcalls = [m.LayerCall(gu_type, cb_gu, DN_T, cb_dn, WL.N, WL.F, tab_gu[l], tab_dn[l], WL.E, self.ids[l],
                                    self.x[l], self.out[l], self.gu, self.hq, self.sync, self.err,
                                    m.F_PDL | m.F_SYNC_PAIR | (m.F_SYNC_ODD if l % 2 else 0))
@@ -204,7 +210,10 @@ class Window:
             m.route_group(self.ids[l], WL.E, 0, self.ge[l], self.gs[l], self.ng[l], self.es[l], self.ed[l],
                           self.err, stream=stream)
             m.quantize_q8_1(self.x[l], self.xq[l], stream=stream)
-            self.calls[l](stream)
+            if self.grouped_fused:
+                self.calls[l].call_fused(self.gsync, stream)
+            else:
+                self.calls[l](stream)
 
     def capture(self):
         self.run_layers()
@@ -238,8 +247,9 @@ def run_ours(args, rank, world):
     # same layout, and the fused window reading CB3 directly
     wins = {T: Window(m, T, tab_gx, tab_dn, None, cb_dn, dev, gu_type=XT) for T in TS}
     sepv = {T: Window(m, T, tab_gx, tab_dn, None, cb_dn, dev, gu_type=XT, fused=False) for T in TS}
+    gfv = {T: Window(m, T, tab_gx, tab_dn, None, cb_dn, dev, gu_type=XT, fused=False, grouped_fused=True) for T in TS}
     natv = {T: Window(m, T, tab_gu, tab_dn, cb_gu, cb_dn, dev) for T in TS}
-    every = list(wins.values()) + list(sepv.values()) + list(natv.values())
+    every = list(wins.values()) + list(sepv.values()) + list(gfv.values()) + list(natv.values())
     for w in every:
         w.capture()
     torch.cuda.synchronize()
@@ -249,6 +259,8 @@ def run_ours(args, rank, world):
     for T in TS:  # the fused window reproduces the separate kernels bit for bit
         if not torch.equal(wins[T].out.view(torch.int32), sepv[T].out.view(torch.int32)):
             raise RuntimeError(f"fused and separate windows differ at T={T}")
+        if not torch.equal(gfv[T].out.view(torch.int32), sepv[T].out.view(torch.int32)):
+            raise RuntimeError(f"one-launch and three-launch expert calls differ at T={T}")
 
     s = torch.cuda.current_stream()
     ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -308,6 +320,7 @@ def run_ours(args, rank, world):
         return res
 
     separate = time_windows(sepv)
+    grouped_fused = time_windows(gfv)
     native = time_windows(natv)
 
     # ---- dominant kernel: the fused layer kernel (T = 4 window: 48 launches per graph)
@@ -334,6 +347,8 @@ def run_ours(args, rank, world):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "per_T": per_T,
         "separate_kernels": {"launch": "route + quantize + gate/up + SwiGLU/q8_1 + down per layer", "per_T": separate},
+        "grouped_fused_call": {"launch": "route + quantize + moe_expert_grouped_fused (one launch) per layer",
+                               "per_T": grouped_fused},
         "native_layout": {"gate_up": "CB3 (read directly), fused launches", "per_T": native},
         "roofline": roof, "step_us_per_layer_alone": breakdown, "second_call_cost": sparse, "calls": sweep, "qsa_block_scores": qsa, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
         "setup_s": round(setup_s, 1),
@@ -347,8 +362,8 @@ def run_ours(args, rank, world):
 # capture of `bench.py --case --case-fused --case-slot` (stored here, not measured by this run);
 # reported only while the kernel sources hash to the ones the capture was taken on (else null:
 # the counters are stale).
-LAYER_TRAFFIC_T4 = {"bytes": 95_377_920, "sources": ("layer.cuh", "gemv.cuh", "common.cuh", "q8_1.cuh", "route.cuh"),
-                    "sha1": "c27b16b12f9fbbf15bcea37752a3e5fbaf94adf7"}
+LAYER_TRAFFIC_T4 = {"bytes": 95_270_400, "sources": ("layer.cuh", "gemv.cuh", "common.cuh", "q8_1.cuh", "route.cuh"),
+                    "sha1": "897dd97ffdcad6d4d8f39ae5281a77405e52deb3"}
 
 
 def layer_traffic():
