@@ -115,9 +115,11 @@ typedef struct moe_wfmt {
 /* Load-time transcoding of CB2/CB3 blobs into a slot layout (MOE_CB3X or MOE_CB2X). For every
  * blob b < n_blobs: dst_blobs[b] (rows x row_bytes(dst_type, K)) = the slot form of
  * src_blobs[b] (rows x row_bytes(src.type, K)). src_blobs / dst_blobs: device arrays of device
- * pointers (16-byte aligned blobs). A value outside the slot's range (|v| > 15 for CB3X, > 3 for
- * CB2X) sets MOE_ERR_CODEBOOK; check *err before using the result. The integer dot products and
- * scales of the slot form equal the source's exactly. */
+ * pointers. A source blob must be 2-byte and a destination blob 8-byte aligned (the decode
+ * kernels want slot blobs 16-byte aligned); a blob off its boundary sets MOE_ERR_ALIGN and is
+ * left unwritten. A value outside the slot's range (|v| > 15 for CB3X, > 3 for CB2X) sets
+ * MOE_ERR_CODEBOOK; check *err before using the result. The integer dot products and scales of
+ * the slot form equal the source's exactly. */
 int moe_transcode_cb(moe_wfmt src, int dst_type, int K, int rows, int n_blobs,
                      const void* const* src_blobs, void* const* dst_blobs, int32_t* err,
                      cudaStream_t stream);

@@ -66,10 +66,13 @@ def test_block_isum_bitexact(m, orc, typ, K):
 
 # ------------------------------------------------------------------ load-time transcoding
 
-@pytest.mark.parametrize("src,dst,K", [(synth.CB3, synth.CB3X, 2560), (synth.CB2, synth.CB2X, 768),
-                                       (synth.CB2, synth.CB3X, 512), (synth.CB3, synth.CB3X, 768)])
-def test_transcode_bitexact(m, orc, src, dst, K):
-    rows, nb = 16, 3
+# rows: one run of whole rows per CTA (256 / (K / 256) rows), so 60 rows of K = 2560 take three
+# CTAs (25, 25, 10) and 100 rows of K = 768 two (85, 15)
+@pytest.mark.parametrize("src,dst,K,rows", [(synth.CB3, synth.CB3X, 2560, 16), (synth.CB2, synth.CB2X, 768, 16),
+                                            (synth.CB2, synth.CB3X, 512, 16), (synth.CB3, synth.CB3X, 768, 16),
+                                            (synth.CB3, synth.CB3X, 2560, 60), (synth.CB2, synth.CB2X, 768, 100)])
+def test_transcode_bitexact(m, orc, src, dst, K, rows):
+    nb = 3
     blobs = synth.weight_blobs(src, rows, K, nb, synth.derive_key(src, dst, K), "cuda")
     cb = synth.codebook(src, 5 + K)
     cbd = torch.from_numpy(np.ascontiguousarray(cb).ravel()).cuda()
@@ -88,6 +91,19 @@ def test_transcode_bitexact(m, orc, src, dst, K):
     m.transcode_cb(src, torch.from_numpy(np.ascontiguousarray(bad).ravel()).cuda(), dst, K, rows,
                    H.pointer_table(blobs), H.pointer_table(out), err)
     assert int(err.item()) & 32
+    # a destination pointer off the 8-byte boundary: that blob is reported and left unwritten (the
+    # offset keeps every byte the kernel could write inside the buffer)
+    out.zero_()
+    err.zero_()
+    tab = H.pointer_table(out)
+    tab[0] += 4
+    m.transcode_cb(src, cbd, dst, K, rows, H.pointer_table(blobs), tab, err)
+    got = out.cpu().numpy()
+    assert int(err.item()) == 16
+    assert not got[0].any()
+    for b in range(1, nb):
+        want, _ = orc.transcode_blob(src, blobs[b].cpu().numpy(), K, rows, cb, dst)
+        assert np.array_equal(got[b], want), b
 
 
 # ------------------------------------------------------------------ a0: routing
