@@ -318,7 +318,8 @@ int moe_expert_layer(const moe_layer_call* call, cudaStream_t stream);
  * group or with one group of two entries, should cost little). The same call - pre-built groups,
  * a device-side n_groups, entries that may start past 0, scattered destinations, rows outside the
  * call untouched - runs as one fused launch (gate/up, SwiGLU + q8_1 and down) instead of three, so
- * an empty call costs one launch. Arguments as moe_expert_grouped, with:
+ * an empty call costs one launch: with *n_groups == 0 it reads nothing else and writes only the
+ * sync words. Arguments as moe_expert_grouped, with:
  *  - grid_groups ignored (one CTA per SM takes the call's work items from a device counter);
  *  - sync: moe_grouped_fused_sync_ints(cap_groups, cap_entries, n_ff) int32 words, 8-byte aligned,
  *    zeroed before the first call, used like moe_expert_layer's (MOE_F_SYNC_PAIR / MOE_F_SYNC_ODD

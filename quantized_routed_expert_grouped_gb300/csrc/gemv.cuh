@@ -390,16 +390,21 @@ __device__ __forceinline__ long long locate(const GroupInfo* gi, const long long
 
 // The codebook in shared memory at offset 0: CB3 256 x 32 lane replicas of 4 bytes, CB2 256 x 16
 // replicas of 8 bytes, both in x-form and both 32 KB with entry idx at offset idx*128.
+// t, nt: this thread's index among nt participating threads (whole warps, warp-aligned).
 template <int TYPE>
 __device__ __forceinline__ void stage_codebook(const GemvArgs& a, uint8_t* smem, int t, int nt) {
     if constexpr (Fmt<TYPE>::CB) {
-        // one 4-byte grid word per thread and iteration (all loads independent), converted to
-        // x-form bytewise and written to its 32 (CB3) or 16 (CB2, two words per entry) replicas
+        // a warp takes 32 consecutive grid words at a time (one coalesced load), converts them to
+        // x-form bytewise and writes whole 128-byte entry rows, lane l word l of a row, so that the
+        // replica stores hit 32 different banks: a CB3 entry is one word (32 replicas), a CB2 entry
+        // two (16 replicas of the pair, word h of the entry at bytes 4h..4h+3 of each)
         constexpr int kWords = TYPE == MOE_CB2 ? 512 : 256;
         const uint32_t* cbw = reinterpret_cast<const uint32_t*>(a.codebook);
+        uint32_t* rows = reinterpret_cast<uint32_t*>(smem);
+        const int lane = t & 31;
         bool even = false;
-        for (int i = t; i < kWords; i += nt) {
-            const uint32_t g = __ldg(cbw + i);
+        for (int w0 = t - lane; w0 < kWords; w0 += nt) {
+            const uint32_t g = __ldg(cbw + w0 + lane);
             even |= (g & 0x01010101u) != 0x01010101u;
             uint32_t v = 0;
 #pragma unroll
@@ -408,15 +413,12 @@ __device__ __forceinline__ void stage_codebook(const GemvArgs& a, uint8_t* smem,
                 v |= (static_cast<uint32_t>((x - 1) >> 1) & 0xffu) << (8 * bb);
             }
             if constexpr (TYPE == MOE_CB3) {
-                uint4* dst = reinterpret_cast<uint4*>(smem + i * 128);
-                const uint4 u = make_uint4(v, v, v, v);
-#pragma unroll
-                for (int part = 0; part < 8; ++part) dst[part] = u;
-            } else {  // word h of entry idx goes to bytes 4h..4h+3 of every 8-byte replica
-                const int idx = i >> 1, h = i & 1;
-                uint32_t* dst = reinterpret_cast<uint32_t*>(smem + idx * 128) + h;
-#pragma unroll
-                for (int rep = 0; rep < 16; ++rep) dst[2 * rep] = v;
+#pragma unroll 8
+                for (int j = 0; j < 32; ++j) rows[(w0 + j) * 32 + lane] = __shfl_sync(0xffffffffu, v, j);
+            } else {
+#pragma unroll 8
+                for (int j = 0; j < 16; ++j)
+                    rows[((w0 >> 1) + j) * 32 + lane] = __shfl_sync(0xffffffffu, v, 2 * j + (lane & 1));
             }
         }
         if (even) set_err(a.err, MOE_ERR_CODEBOOK);

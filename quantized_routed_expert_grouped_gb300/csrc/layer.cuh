@@ -373,6 +373,37 @@ __device__ __forceinline__ void chunk_part(const GemvArgs& a, const uint8_t* sme
     }
 }
 
+// The end of a call, once the CTA's work (if any) is done. The call used the h pairs of its L.n
+// entries, the extent an epoch wrap clears. With a sync pair, the call that used the other half
+// has completed (this one is past its dependency wait), so CTA 0 resets that half for the call
+// after this one and records this call's extent in its own half (read when the next call advances
+// this half's epoch). Otherwise an exit count: the last CTA zeroes the counters and advances the
+// epoch. Every thread of the CTA calls it.
+__device__ __forceinline__ void end_call(const LayerArgs& L, int* misc, int tid) {
+    const int32_t ext = L.n * kHxPairs * L.nbj;
+    if (L.sync_other) {
+        if (blockIdx.x == 0 && tid == 0) {
+            L.sync_other[kSyncExit] = 0;
+            L.sync_other[kSyncWork] = 0;
+            advance_epoch(L.sync_other);
+            if (L.sync[kSyncExt] < ext) L.sync[kSyncExt] = ext;
+        }
+        return;
+    }
+    if (tid == 0) {
+        __threadfence();
+        misc[2] = atomicAdd(L.sync + kSyncExit, 1) == static_cast<int>(gridDim.x) - 1;
+    }
+    __syncthreads();
+    if (misc[2] && tid == 0) {
+        __threadfence();
+        L.sync[kSyncExit] = 0;
+        L.sync[kSyncWork] = 0;
+        if (L.sync[kSyncExt] < ext) L.sync[kSyncExt] = ext;
+        advance_epoch(L.sync);
+    }
+}
+
 // GIVEN: the grouping and the activation q8_1 come from the caller (moe_expert_grouped_fused)
 // instead of routing ids and quantizing x (moe_expert_layer); a template parameter, so that each
 // form's kernel carries only its own code.
@@ -439,6 +470,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     __syncthreads();
     pdl_wait();
     pdl_trigger();
+    // pre-built groups and none in this call (the same value for every thread): nothing to stage
+    // or stream, only the end-of-call words
+    if constexpr (GIVEN) {
+        if (__ldcg(L.g_ng) == 0) {
+            end_call(L, misc, tid);
+            return;
+        }
+    }
     uint64_t* hx = reinterpret_cast<uint64_t*>(L.sync + kSyncHx);
 
     // ---- routing/grouping and tables: one warp when n <= 32, else the whole CTA routes and
@@ -898,33 +937,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         for (int qq = nq - S > 0 ? nq - S : 0; qq < nq; ++qq)
             mbar_wait_bounded(&full[qq % S], static_cast<uint32_t>(qq / S) & 1u);
     }
-    // the h pairs this call used, the extent an epoch wrap clears
-    const int32_t ext = n * kHxPairs * L.nbj;
-    // ---- a sync pair: the call that used the other half has completed (this one is past its
-    // dependency wait), so CTA 0 resets that half for the call after this one, and records this
-    // call's extent in its own half (read when the next call advances this half's epoch)
-    if (L.sync_other) {
-        if (blockIdx.x == 0 && tid == 0) {
-            L.sync_other[kSyncExit] = 0;
-            L.sync_other[kSyncWork] = 0;
-            advance_epoch(L.sync_other);
-            if (L.sync[kSyncExt] < ext) L.sync[kSyncExt] = ext;
-        }
-        return;
-    }
-    // ---- otherwise an exit count: the last CTA zeroes the counters and advances the epoch
-    if (tid == 0) {
-        __threadfence();
-        misc[2] = atomicAdd(L.sync + kSyncExit, 1) == static_cast<int>(gridDim.x) - 1;
-    }
-    __syncthreads();
-    if (misc[2] && tid == 0) {
-        __threadfence();
-        L.sync[kSyncExit] = 0;
-        L.sync[kSyncWork] = 0;
-        if (L.sync[kSyncExt] < ext) L.sync[kSyncExt] = ext;
-        advance_epoch(L.sync);
-    }
+    end_call(L, misc, tid);
 }
 
 template <int GT, int DT, bool GIVEN>

@@ -134,6 +134,45 @@ def test_fused_sync_pair_alternating(m, orc):
         assert np.array_equal(_bits(B.out), _bits(r))
 
 
+def test_fused_empty_calls_in_a_sync_pair(m, orc):
+    """Empty calls (n_groups 0, which end right after the dependency wait) between real calls on
+    alternating halves of one sync pair: each real call equals its three-launch call, the empty
+    calls write nothing, and every counter is zero again at the end."""
+    wl = synth.WORKLOADS["verify"]
+    Ls = [H.make_layer(wl, (synth.CB2, synth.NL4), 4, layer=l) for l in range(4)]
+    Bs = [H.make_bufs(L) for L in Ls]
+    refs = []
+    for L, B in zip(Ls, Bs):
+        H.gpu_route_and_quantize(m, L, B)
+        H.expert_call(m, L, B)()
+        torch.cuda.synchronize()
+        refs.append(B.out.clone())
+    E0 = H.make_bufs(Ls[0])
+    E0.grp_expert.copy_(Bs[0].grp_expert); E0.grp_start.copy_(Bs[0].grp_start)
+    E0.ent_src.copy_(Bs[0].ent_src); E0.ent_dst.copy_(Bs[0].ent_dst); E0.xq.copy_(Bs[0].xq)
+    E0.n_groups.fill_(0)
+    sync = _sync(m, Bs[0], wl, pair=True)
+    # halves: L0 even, empty odd, L1 even, empty odd, L2 even, L3 odd
+    seq = [(Ls[0], Bs[0]), (Ls[0], E0), (Ls[1], Bs[1]), (Ls[0], E0), (Ls[2], Bs[2]), (Ls[3], Bs[3])]
+    for B in Bs:
+        B.out.fill_(float("nan"))
+    for i, (L, B) in enumerate(seq):
+        c = H.expert_call(m, L, B, flags=m.F_PDL | m.F_SYNC_PAIR | (m.F_SYNC_ODD if i % 2 else 0))
+        c.call_fused(sync)
+    torch.cuda.synchronize()
+    for B, r in zip(Bs, refs):
+        assert int(B.err.item()) == 0
+        assert np.array_equal(_bits(B.out), _bits(r))
+    assert int(E0.err.item()) == 0
+    assert torch.isnan(E0.out).all() and torch.isnan(E0.gu).all()
+    # the last call (odd half) reset the even half; its own counters are zeroed by the next call,
+    # and its exit count is not used in pair mode
+    half = sync.numel() // 2
+    s = sync.cpu().numpy()
+    assert s[0] == 0 and s[1] == 0
+    assert s[half] == 0
+
+
 def test_fused_bad_groups_are_reported_and_skipped(m, orc):
     """n_groups above cap is clamped (MOE_ERR_NGROUPS); a group with an expert id out of range
     (MOE_ERR_EXPERT) or an entry whose source row is out of range (MOE_ERR_ENTRY) is skipped and
