@@ -19,17 +19,20 @@
 //    (q_h, q_h+1) so that one packed fp32x2 fused multiply-add (fma.rn.f32x2) computes two
 //    heads' products per instruction; the key value is converted exactly (a byte permute into
 //    2^23 + (k + 128), then one subtraction) and used in both halves.
-//  * The pairings need every lane's partial of a value. Instead of shuffles, each lane writes
-//    its 32 partial pairs of the chunk into a padded shared-memory tile (row = value pair,
-//    column = lane; 272-byte rows keep both the 8-byte writes and the 16-byte reads free of bank
-//    conflicts), and lane j then reads row j and adds it up in the pairing order with packed
-//    fp32x2 additions (31 per pair of values). Packed arithmetic rounds each half on its own, so
-//    nothing changes in the bits.
+//  * The pairings need every lane's partial of a value. The first level (lane l with lane l xor
+//    16) is one shuffle exchange: lanes 16-31 take the chunk's blocks in swapped halves, so the
+//    first half of every lane's steps gives the values it keeps and the second half the ones its
+//    partner keeps, sent over and added (the same two operands as the definition's, and fp32
+//    addition commutes). Each lane then writes its 16 kept pair sums into a padded shared-memory
+//    tile (row = value pair, column = lane mod 16; 144-byte rows keep the 8-byte writes and the
+//    16-byte reads free of bank conflicts), and lane j reads row j and adds it up in the pairing
+//    order (levels 8, 4, 2, 1) with packed fp32x2 additions. Packed arithmetic rounds each half
+//    on its own, so nothing changes in the bits.
 //  * The lanes holding heads 0-1 and 2-3 of one (block, query) meet with two shuffles for the
 //    head-order sum; the score is stored by the even lane.
-//  * Bound: the fp32 pipe (about 70 instructions per block at T = 4: 32 packed multiply-adds, 12
-//    for the key conversion, 8 shared-memory writes and about 16 for the reduction), not HBM
-//    (128 bytes per block).
+//  * Bound: instruction issue and the fp32 pipe at T = 3-4 (about 100 warp-instructions per block:
+//    32 packed multiply-adds, the key conversion, the exchange, 4 shared-memory writes and the
+//    reduction), not HBM (132 bytes per block).
 #include <atomic>
 
 #include "common.cuh"
@@ -39,8 +42,8 @@ namespace moe {
 
 namespace {
 
-constexpr int kQsaWarps = 4;          // warps per CTA (a 8.7 KB tile each)
-constexpr int kQsaRow = 34;           // float2 per shared-memory row (32 lanes + 16 bytes of padding)
+constexpr int kQsaWarps = 4;          // warps per CTA (a 4.6 KB tile each)
+constexpr int kQsaRow = 18;           // float2 per shared-memory row (16 lane pairs + 16 bytes of padding)
 constexpr int kQsaRows = 32;          // value pairs per chunk
 constexpr float kQsaTail = 1e9f;      // added to the tail block's score
 constexpr float kByteBias = 8388736.0f;  // 2^23 + 128
@@ -153,14 +156,21 @@ __global__ void __launch_bounds__(kQsaWarps * 32) qsa_kernel(const float* __rest
             qp[t][hp][2] = make_float2(a.z, b.z);
             qp[t][hp][3] = make_float2(a.w, b.w);
         }
+    // lanes 16-31 take the chunk's blocks in swapped halves (step b: block b xor NB/2)
+    const int hb = lane >= 16 ? NB / 2 : 0;
     int st = 0;
     for (long long ch = ch0; ch < n_chunks; ch += warps) {
         const long long b0 = ch * NB;
         cp_wait<D - 1>();  // this lane's copies of chunk ch have landed (it reads only those)
         uint32_t kw[NB];
 #pragma unroll
-        for (int b = 0; b < NB; ++b) kw[b] = *reinterpret_cast<const uint32_t*>(ring + (st * NB + b) * 128 + 4 * lane);
-        // ---- the lane's partials: pair row (b * TQ + t) * 2 + hp, column = lane
+        for (int b = 0; b < NB; ++b)
+            kw[b] = *reinterpret_cast<const uint32_t*>(ring + (st * NB + (b ^ hb)) * 128 + 4 * lane);
+        // ---- the lane's partials, step b: block b (lanes 0-15) or block b xor NB/2 (lanes 16-31).
+        // Pairing level 16 (slice l with slice l xor 16) by one exchange: the first NB/2 steps
+        // give the blocks the lane keeps, the last NB/2 the ones its partner keeps, sent to it
+        // and added (the same two operands as the definition's; fp32 addition commutes)
+        float2 kp[NB / 2][TQ][2];
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
             const uint32_t wx = kw[b] ^ 0x80808080u;
@@ -173,16 +183,29 @@ __global__ void __launch_bounds__(kQsaWarps * 32) qsa_kernel(const float* __rest
                     p = fma2(qp[t][hp][1], k1, p);
                     p = fma2(qp[t][hp][2], k2, p);
                     p = fma2(qp[t][hp][3], k3, p);
-                    tl[(b * TQ + t) * 2 + hp][lane] = p;
+                    if (b < NB / 2) {
+                        kp[b][t][hp] = p;
+                    } else {
+                        const float2 r = make_float2(__shfl_xor_sync(0xffffffffu, p.x, 16),
+                                                     __shfl_xor_sync(0xffffffffu, p.y, 16));
+                        kp[b - NB / 2][t][hp] = add2(kp[b - NB / 2][t][hp], r);
+                    }
                 }
         }
-        __syncwarp();  // every lane's partials (and scale copies) before the reduction reads them
-        // ---- lane j sums pair row j over the 32 lanes in the warp sum's order:
-        // level 16 adds columns c and c + 16, then 8, 4, 2, 1 on the results
-        float2 x[32];
+        // the kept sums: pair row (block * TQ + t) * 2 + hp of the lane's blocks, column = lane % 16
+#pragma unroll
+        for (int b = 0; b < NB / 2; ++b)
+#pragma unroll
+            for (int t = 0; t < TQ; ++t)
+#pragma unroll
+                for (int hp = 0; hp < 2; ++hp) tl[((b + hb) * TQ + t) * 2 + hp][lane & 15] = kp[b][t][hp];
+        __syncwarp();  // every lane's sums (and scale copies) before the reduction reads them
+        // ---- lane j sums pair row j over the 16 columns in the warp sum's order: level 8 adds
+        // columns c and c + 8, then 4, 2, 1 on the results
+        float2 x[16];
         const float4* row = reinterpret_cast<const float4*>(tl[lane]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
             const float4 v = row[i];
             x[2 * i] = make_float2(v.x, v.y);
             x[2 * i + 1] = make_float2(v.z, v.w);
@@ -200,7 +223,7 @@ __global__ void __launch_bounds__(kQsaWarps * 32) qsa_kernel(const float* __rest
         }
         st = st + 1 == D ? 0 : st + 1;
 #pragma unroll
-        for (int j = 16; j >= 1; j >>= 1)
+        for (int j = 8; j >= 1; j >>= 1)
 #pragma unroll
             for (int c = 0; c < j; ++c) x[c] = add2(x[c], x[c + j]);
         const float s0 = __fmul_rn(x[0].x, sc), s1 = __fmul_rn(x[0].y, sc);
