@@ -271,18 +271,19 @@ int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, 
     phase_warps(A.nch, A);
     phase_warps(D.nch, D);
     A.RT = 32 * rbA <= 96 * 1024 ? 32 : 16;
-    // activations: T token rows (gate/up role) and two buffers of 4 entry rows (down role, staged
-    // by the producer warp while the consumers work on the other buffer), separate regions
+    // activations: T token rows (gate/up role) and nbuf buffers of 4 entry rows (down role, staged
+    // by the producer warp while the consumers work on the others; three where they fit without
+    // a shallower ring, else two), separate regions
     const int actqA = round_up(T * 2 * A.nbp * 16, 128), act2A = round_up(T * A.nb * 8, 128);
-    const int actqD = round_up(2 * kBatch * 2 * D.nbp * 16, 128);
-    const int act2D = round_up(2 * kBatch * D.nb * 8, 128);
     if (actqA + act2A > 64 * 1024) return MOE_E_CAP;
-    const int act = actqA + act2A + actqD + act2D;
+    auto act_bytes = [&](int nbuf) {
+        return actqA + act2A + round_up(nbuf * kBatch * 2 * D.nbp * 16, 128) + round_up(nbuf * kBatch * D.nb * 8, 128);
+    };
     const int grp = round_up(24 * n + 4 * (n + 1), 128), entb = round_up(8 * n, 128);
     const int route = round_up(4 * (6 * n + 4), 128);
     const int cbb = cb_type(gt) ? 32768 : 0;
     const int ptrs = E <= kLayerPtrCache ? round_up(16 * E, 128) : 0;
-    const int fixed = cbb + act + 2 * grp + 2 * entb + route + ptrs + kUnitBytes + 512 + 1024;
+    const int fixed2 = cbb + act_bytes(2) + 2 * grp + 2 * entb + route + ptrs + kUnitBytes + 512 + 1024;
     // one ring for both phases: a slot holds a gate/up tile (RT rows) or a down tile of nsub 32-row
     // sub-tiles; per stage a slot and its partial sums
     const int64_t tileA = A.RT * rbA;
@@ -293,9 +294,12 @@ int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, 
     const int stage = round_up(static_cast<int>(tile) + 16, 128);
     const int pA = A.nch * 4 * A.RT, pD = D.nch * 4 * D.RT;
     const int part = 4 * (pA > pD ? pA : pD);
-    int S = (kSmemPerSm - 1024 - fixed) / (stage + part);
+    int S = (kSmemPerSm - 1024 - fixed2) / (stage + part);
     S = S > 8 ? 8 : S;
     if (S < 2) return MOE_E_SHAPE;
+    const int nbuf = (kSmemPerSm - 1024 - (fixed2 - act_bytes(2) + act_bytes(3))) / (stage + part) >= S ? 3 : 2;
+    const int act = act_bytes(nbuf);
+    const int actqD = round_up(nbuf * kBatch * 2 * D.nbp * 16, 128);
     int off = cbb;  // the gate/up codebook sits at offset 0
     A.off_ring = D.off_ring = off;
     off += S * stage;
@@ -321,14 +325,14 @@ int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, 
     L.off_ptr = ptrs ? off : 0;
     off += ptrs;
     A.off_bar = D.off_bar = off;
-    off += 512;  // 2 x 8 ring mbarriers, 2 x 16 descriptor mbarriers, 4 unit mbarriers
+    off += 512;  // 2 x 8 ring mbarriers, 2 x 16 descriptor mbarriers, 4 unit mbarriers (416 bytes)
     A.off_misc = D.off_misc = off;
     off += 1024;
     A.stages = D.stages = S;
     A.stage_bytes = D.stage_bytes = stage;
     A.part_bytes = D.part_bytes = part;
     A.act_cap = T;
-    D.act_cap = 2 * kBatch;
+    D.act_cap = nbuf * kBatch;
     A.cap_groups = A.cap_entries = D.cap_groups = D.cap_entries = n;
     L.T = T;
     L.k = k;

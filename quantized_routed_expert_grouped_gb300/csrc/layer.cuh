@@ -602,7 +602,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         int nwork = 0;                           // work items published (lane 0)
         int ku = 0;                              // gate/up units (4-entry batches) issued (lane 0)
         int st_g = -1, st_b0 = -1, st_n = 0;     // staged group and batch, stagings so far
-        int st_last = 0;                         // first ring index of the last staging (lane 0)
+        const int nbuf = D.act_cap / kMaxEntriesPerPass;  // h buffers (2 or 3), used in turn
+        int st_buf = nbuf - 1;                   // buffer of the last staging
+        int st_p1 = 0, st_p2 = 0;                // first ring index of the last / second-last staging (lane 0)
         bool stop = false;
         // ring slot j % S free for index j: the tile S indices earlier released (lane 0)
         auto slot_free = [&](int j) -> bool {
@@ -713,13 +715,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                                 const uint8_t* src = tile_src(t, bytes);
                                 if (ok) copy_tile(issued + pre, src, bytes, nullptr, 0);
                             }
-                            // buffer st_n & 1 free (from the third staging on): every ring index
-                            // before the last staging's first one released (indices before
+                            // the next buffer free (from staging nbuf on): every ring index before
+                            // the first one of staging st_n - nbuf + 1 released (indices before
                             // issued - S are, as their slots were claimed again)
-                            if (st_n >= 2)
-                                for (int j = issued - S > 0 ? issued - S : 0; ok && j < st_last; ++j)
+                            if (st_n >= nbuf) {
+                                const int lim = nbuf == 3 ? st_p2 : st_p1;
+                                for (int j = issued - S > 0 ? issued - S : 0; ok && j < lim; ++j)
                                     ok = mbar_wait_bounded(&empty[j % S], static_cast<uint32_t>(j / S) & 1u);
-                            st_last = issued;
+                            }
+                            st_p2 = st_p1;
+                            st_p1 = issued;
                         }
                         ok = __shfl_sync(0xffffffffu, ok, 0);
                         // the batch's h rows, each block staged as soon as its flagged copy is
@@ -728,7 +733,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                         const uint32_t want = L.test_expire ? flag ^ 0x80000000u : flag;
                         ok = __all_sync(0xffffffffu, ok && !vmisc[1] &&
                                                          stage_flagged<DT>(D, smem, entD, hx, b0, ne,
-                                                                           kMaxEntriesPerPass * (st_n & 1), want, lane));
+                                                                           kMaxEntriesPerPass * (st_buf + 1 == nbuf ? 0 : st_buf + 1),
+                                                                           want, lane));
                         if (!ok) {
                             if (lane == 0) {
                                 if (!vmisc[1]) set_err(A.err, MOE_ERR_TIMEOUT);
@@ -741,8 +747,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                         st_g = g;
                         st_b0 = b0;
                         ++st_n;
+                        st_buf = st_buf + 1 == nbuf ? 0 : st_buf + 1;
                     }
-                    const int s0 = kMaxEntriesPerPass * ((st_n - 1) & 1);
+                    const int s0 = kMaxEntriesPerPass * st_buf;
                     if (lane == 0)
                         for (int t = t0; t < t1; ++t) {
                             if (t - t0 >= pre) {
