@@ -250,9 +250,9 @@ void phase_warps(int nch, GemvArgs& a) {
 // Geometry and shared-memory layout of one fused layer launch. The ring slot holds a gate/up
 // tile (32 rows, or 16 when 32 rows exceed 96 KB) or a down tile of nsub x 32 rows.
 constexpr int kLayerPtrCache = 256;  // experts whose pointers are cached in shared memory
-constexpr int kUnitBytes = 4 * 4 * 32 * 4;  // gate/up unit buffers (4 units x 4 entries x 32 floats)
+constexpr int kUnitBytes = 4 * kLayerBatch * 32 * 4;  // gate/up unit buffers (4 units x kLayerBatch entries x 32 floats)
 constexpr int kLayerThreads = 512;   // producer warp + 15 consumer warps
-constexpr int kBatch = 4;            // entries staged per down batch
+constexpr int kBatch = kLayerBatch;  // entries staged per down batch
 
 // T activation rows; tables for n_tables entries and groups (0: T * k, a routed window's)
 int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, int& NT, int& smem,
@@ -271,9 +271,9 @@ int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, 
     phase_warps(A.nch, A);
     phase_warps(D.nch, D);
     A.RT = 32 * rbA <= 96 * 1024 ? 32 : 16;
-    // activations: T token rows (gate/up role) and nbuf buffers of 4 entry rows (down role, staged
-    // by the producer warp while the consumers work on the others; three where they fit without
-    // a shallower ring, else two), separate regions
+    // activations: T token rows (gate/up role) and nbuf buffers of kLayerBatch entry rows (down
+    // role, staged by the producer warp while the consumers work on the others; as many as fit, up
+    // to kMaxHBufs, without a shallower ring, at least two), separate regions
     const int actqA = round_up(T * 2 * A.nbp * 16, 128), act2A = round_up(T * A.nb * 8, 128);
     if (actqA + act2A > 64 * 1024) return MOE_E_CAP;
     auto act_bytes = [&](int nbuf) {
@@ -292,12 +292,14 @@ int plan_layer(int gt, int dt, int N, int F, int T, int k, int E, LayerArgs& L, 
     D.RT = 32 * nsub;
     const int64_t tile = tileA > D.RT * rbD ? tileA : D.RT * rbD;
     const int stage = round_up(static_cast<int>(tile) + 16, 128);
-    const int pA = A.nch * 4 * A.RT, pD = D.nch * 4 * D.RT;
+    const int pA = A.nch * kLayerBatch * A.RT, pD = D.nch * kLayerBatch * D.RT;
     const int part = 4 * (pA > pD ? pA : pD);
     int S = (kSmemPerSm - 1024 - fixed2) / (stage + part);
     S = S > 8 ? 8 : S;
     if (S < 2) return MOE_E_SHAPE;
-    const int nbuf = (kSmemPerSm - 1024 - (fixed2 - act_bytes(2) + act_bytes(3))) / (stage + part) >= S ? 3 : 2;
+    int nbuf = 2;  // the most (up to kMaxHBufs) that keep the ring as deep as with two
+    while (nbuf < kMaxHBufs && (kSmemPerSm - 1024 - (fixed2 - act_bytes(2) + act_bytes(nbuf + 1))) / (stage + part) >= S)
+        ++nbuf;
     const int act = act_bytes(nbuf);
     const int actqD = round_up(nbuf * kBatch * 2 * D.nbp * 16, 128);
     int off = cbb;  // the gate/up codebook sits at offset 0

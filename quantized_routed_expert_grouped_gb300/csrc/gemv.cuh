@@ -765,6 +765,8 @@ __device__ __forceinline__ void compute_batch(const GemvArgs& a, const uint8_t* 
 
 // Fixed-order sum over the chunks (c = 0 .. nch-1) of each (row, entry), written to the entry's
 // output row.
+// STRIDE: entries per chunk in the partials layout (part[(c*STRIDE + e)*RT + row]).
+template <int STRIDE = kMaxEntriesPerPass>
 __device__ __forceinline__ void reduce_write(const GemvArgs& a, const float* part, const int2* ent, int b0,
                                              const Tile& t, int ne, int lane) {
     if (lane >= t.nrows) return;
@@ -772,7 +774,7 @@ __device__ __forceinline__ void reduce_write(const GemvArgs& a, const float* par
         const int2 en = ent[b0 + e];
         if (en.x < 0) continue;
         float s = part[e * a.RT + lane];
-        for (int c = 1; c < a.nch; ++c) s = __fadd_rn(s, part[(c * kMaxEntriesPerPass + e) * a.RT + lane]);
+        for (int c = 1; c < a.nch; ++c) s = __fadd_rn(s, part[(c * STRIDE + e) * a.RT + lane]);
         a.out[static_cast<int64_t>(en.y) * a.out_stride + t.row0 + lane] = s;
     }
 }

@@ -79,6 +79,11 @@ struct GemvPlan {
 // call's flag, epoch + 1), so that a reader polls the data itself.
 constexpr int kSyncExit = 0, kSyncWork = 1, kSyncEpoch = 2, kSyncExt = 3, kSyncHx = 4;
 constexpr int kHxPairs = 9;  // pairs per q8_1 block
+// Entries of a group the fused layer kernel applies per pass over its weights (a group of more
+// streams them once per batch; at T <= 4 and top-8 of 64 or more experts a group of three or
+// four entries is rare)
+constexpr int kLayerBatch = 2;
+constexpr int kMaxHBufs = 6;  // the fused layer kernel's down h-staging buffers at most
 
 struct LayerArgs {
     GemvArgs gu, dn;     // per-phase geometry and pointers (shared ring, partials, barriers, misc)

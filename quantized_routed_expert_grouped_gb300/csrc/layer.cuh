@@ -352,24 +352,20 @@ __device__ __forceinline__ void bar_arrive(int id, int threads) {
 }
 
 // One warp's partial sums for one 256-weight chunk c of 32 rows at `rows` (lane = row):
-// part[(c*4 + e)*RT + lane] for the batch's ne entries, staged in slots[0 .. ne-1].
+// part[(c*kLayerBatch + e)*RT + lane] for the batch's ne (1 or 2) entries, staged in slots[0 .. ne-1].
 template <int TYPE>
 __device__ __forceinline__ void chunk_part(const GemvArgs& a, const uint8_t* smem, const uint8_t* rows, float* part, int ne,
-                                           int c, int lane, uint32_t loff, const uint32_t tab[kTab], const int slots[4]) {
+                                           int c, int lane, uint32_t loff, const uint32_t tab[kTab],
+                                           const int slots[kLayerBatch]) {
     if (ne == 1) {
         float acc[1];
         lane_chunk<TYPE, 1>(a, smem, rows, lane, c, loff, tab, slots, acc);
-        part[c * kMaxEntriesPerPass * a.RT + lane] = acc[0];
-    } else if (ne == 2) {
+        part[c * kLayerBatch * a.RT + lane] = acc[0];
+    } else {
         float acc[2];
         lane_chunk<TYPE, 2>(a, smem, rows, lane, c, loff, tab, slots, acc);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) part[(c * kMaxEntriesPerPass + e) * a.RT + lane] = acc[e];
-    } else {  // 3 entries run the 4-entry code (the fourth slot repeats the third)
-        float acc[4];
-        lane_chunk<TYPE, 4>(a, smem, rows, lane, c, loff, tab, slots, acc);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) part[(c * kMaxEntriesPerPass + e) * a.RT + lane] = acc[e];
+        for (int e = 0; e < 2; ++e) part[(c * kLayerBatch + e) * a.RT + lane] = acc[e];
     }
 }
 
@@ -602,9 +598,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         int nwork = 0;                           // work items published (lane 0)
         int ku = 0;                              // gate/up units (4-entry batches) issued (lane 0)
         int st_g = -1, st_b0 = -1, st_n = 0;     // staged group and batch, stagings so far
-        const int nbuf = D.act_cap / kMaxEntriesPerPass;  // h buffers (2 or 3), used in turn
+        const int nbuf = D.act_cap / kLayerBatch;  // h buffers, used in turn
         int st_buf = nbuf - 1;                   // buffer of the last staging
-        int st_p1 = 0, st_p2 = 0;                // first ring index of the last / second-last staging (lane 0)
+        // first ring index of the last, second-last, ... staging (lane 0; kMaxHBufs - 1 of them)
+        int st_p0 = 0, st_p1 = 0, st_p2 = 0, st_p3 = 0, st_p4 = 0;
+        static_assert(kMaxHBufs == 6, "the staging history holds kMaxHBufs - 1 indices");
         bool stop = false;
         // ring slot j % S free for index j: the tile S indices earlier released (lane 0)
         auto slot_free = [&](int j) -> bool {
@@ -664,8 +662,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 const GroupInfo gr = giA[g];
                 if (gr.cost == 0) continue;
                 if (lane == 0)
-                    for (int b0 = gr.e0; b0 < gr.e1 && !stop; b0 += kMaxEntriesPerPass) {
-                        const int ne = gr.e1 - b0 < kMaxEntriesPerPass ? gr.e1 - b0 : kMaxEntriesPerPass;
+                    for (int b0 = gr.e0; b0 < gr.e1 && !stop; b0 += kLayerBatch) {
+                        const int ne = gr.e1 - b0 < kLayerBatch ? gr.e1 - b0 : kLayerBatch;
                         // unit buffer ku % kUnitBufs free: the unit kUnitBufs earlier has written its h
                         // blocks
                         if (vmisc[1] || (ku >= kUnitBufs &&
@@ -702,8 +700,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                     bytes = static_cast<uint32_t>(nrows) * static_cast<uint32_t>(D.row_bytes);
                     return gr.ptr + static_cast<size_t>(row0) * D.row_bytes;
                 };
-                for (int b0 = gr.e0; b0 < gr.e1 && !stop; b0 += kMaxEntriesPerPass) {
-                    const int ne = gr.e1 - b0 < kMaxEntriesPerPass ? gr.e1 - b0 : kMaxEntriesPerPass;
+                for (int b0 = gr.e0; b0 < gr.e1 && !stop; b0 += kLayerBatch) {
+                    const int ne = gr.e1 - b0 < kLayerBatch ? gr.e1 - b0 : kLayerBatch;
                     int pre = 0;  // tiles of this batch copied ahead of the h wait (lane 0)
                     if (g != st_g || b0 != st_b0) {
                         int ok = 1;
@@ -719,12 +717,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                             // the first one of staging st_n - nbuf + 1 released (indices before
                             // issued - S are, as their slots were claimed again)
                             if (st_n >= nbuf) {
-                                const int lim = nbuf == 3 ? st_p2 : st_p1;
+                                const int lim = nbuf == 2 ? st_p0 : nbuf == 3 ? st_p1 : nbuf == 4 ? st_p2 : nbuf == 5 ? st_p3 : st_p4;
                                 for (int j = issued - S > 0 ? issued - S : 0; ok && j < lim; ++j)
                                     ok = mbar_wait_bounded(&empty[j % S], static_cast<uint32_t>(j / S) & 1u);
                             }
+                            st_p4 = st_p3;
+                            st_p3 = st_p2;
                             st_p2 = st_p1;
-                            st_p1 = issued;
+                            st_p1 = st_p0;
+                            st_p0 = issued;
                         }
                         ok = __shfl_sync(0xffffffffu, ok, 0);
                         // the batch's h rows, each block staged as soon as its flagged copy is
@@ -733,7 +734,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                         const uint32_t want = L.test_expire ? flag ^ 0x80000000u : flag;
                         ok = __all_sync(0xffffffffu, ok && !vmisc[1] &&
                                                          stage_flagged<DT>(D, smem, entD, hx, b0, ne,
-                                                                           kMaxEntriesPerPass * (st_buf + 1 == nbuf ? 0 : st_buf + 1),
+                                                                           kLayerBatch * (st_buf + 1 == nbuf ? 0 : st_buf + 1),
                                                                            want, lane));
                         if (!ok) {
                             if (lane == 0) {
@@ -749,7 +750,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                         ++st_n;
                         st_buf = st_buf + 1 == nbuf ? 0 : st_buf + 1;
                     }
-                    const int s0 = kMaxEntriesPerPass * st_buf;
+                    const int s0 = kLayerBatch * st_buf;
                     if (lane == 0)
                         for (int t = t0; t < t1; ++t) {
                             if (t - t0 >= pre) {
@@ -839,9 +840,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
             if (kind == 0) {
                 // ---- chunk c = j of gate/up tile h = a1 of unit (g, jb = a0), entries e0 .. e0+ne-1
                 const int jb = a0, h = a1, c = j, u = a6 % kUnitBufs;
-                int slots[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) slots[e] = entA[e0 + (e < ne ? e : ne - 1)].x;
+                const int slots[kLayerBatch] = {entA[e0].x, entA[e0 + (ne > 1 ? 1 : 0)].x};
                 if (lane < RT) chunk_part<GT>(A, smem, tile, part, ne, c, lane, loff, tabA, slots);
                 __syncwarp();
                 __threadfence_block();
@@ -853,14 +852,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 // the gate/up rows and put SwiGLU(gate, up) (product rounded on its own) in the unit
                 // buffer
                 __threadfence_block();
-                float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                float v[kLayerBatch] = {0.0f, 0.0f};
                 if (lane < RT)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
+                    for (int e = 0; e < kLayerBatch; ++e)
                         if (e < ne) {
                             float sv = part[e * RT + lane];
-                            for (int cc = 1; cc < A.nch; ++cc)
-                                sv = __fadd_rn(sv, part[(cc * kMaxEntriesPerPass + e) * RT + lane]);
+                            for (int cc = 1; cc < A.nch; ++cc) sv = __fadd_rn(sv, part[(cc * kLayerBatch + e) * RT + lane]);
                             v[e] = sv;
                         }
                 __syncwarp();
@@ -869,9 +867,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                     mbar_arrive(&empty[slot]);  // partials read: the slot is free
                 }
                 const int rowg = 32 * jb + h * half + (lane < half ? lane : lane - half + F);
-                float* ub = ubuf + u * (kMaxEntriesPerPass * 32);
+                float* ub = ubuf + u * (kLayerBatch * 32);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
+                for (int e = 0; e < kLayerBatch; ++e) {
                     if (e >= ne) break;
                     if (lane < RT) A.out[static_cast<int64_t>(ebase + e0 + e) * gst + rowg] = v[e];
                     const float uv = __shfl_down_sync(0xffffffffu, v[e], half);
@@ -912,7 +910,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 const int row0 = a0, nrows = a1, s0 = a6;
                 const int nsb = (nrows + 31) >> 5, sb = j / D.nch, c = j - sb * D.nch;
                 const int nr = nrows - sb * 32 < 32 ? nrows - sb * 32 : 32;
-                const int slots[4] = {s0, s0 + (ne > 1 ? 1 : 0), s0 + (ne > 2 ? 2 : ne - 1), s0 + (ne > 3 ? 3 : ne - 1)};
+                const int slots[kLayerBatch] = {s0, s0 + (ne > 1 ? 1 : 0)};
                 if (lane < nr)
                     chunk_part<DT>(D, smem, tile + static_cast<size_t>(sb) * 32 * D.row_bytes, part + sb * 32, ne, c, lane, 0,
                                    tabD, slots);
@@ -923,7 +921,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 last = __shfl_sync(0xffffffffu, last, 0);
                 if (!last) continue;
                 __threadfence_block();
-                reduce_write(D, part + sb * 32, entD, e0, Tile{g, row0 + sb * 32, nr}, ne, lane);
+                reduce_write<kLayerBatch>(D, part + sb * 32, entD, e0, Tile{g, row0 + sb * 32, nr}, ne, lane);
                 __syncwarp();
                 if (lane == 0) {
                     misc[64 + 8 * slot + sb] = 0;
