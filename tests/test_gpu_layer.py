@@ -93,7 +93,20 @@ def _same_as_separate(F, B, ntot):
 
 @pytest.mark.parametrize("wname,pair,T,xt", CASES, ids=CASE_IDS)
 def test_layer_equals_separate_steps_and_oracle(m, orc, wname, pair, T, xt):
-    wl = synth.WORKLOADS[wname]
+    _check_layer(m, orc, synth.WORKLOADS[wname], pair, T, xt)
+
+
+# The fused call at its entry capacity (T*k = 512) on small shapes: 64 tokens, top-8 of 64
+# experts, so about eight entries per group (four batches of two each), CB3 gate/up read directly
+# (its codebook staged in shared memory) and NL4 down.
+CAP = synth.Workload("cap512", 1, (64,), 64, 8, 512, 256, ((synth.CB3, synth.NL4),), seed=66)
+
+
+def test_layer_at_entry_capacity(m, orc):
+    _check_layer(m, orc, CAP, CAP.pairs[0], 64, None)
+
+
+def _check_layer(m, orc, wl, pair, T, xt):
     L0 = H.make_layer(wl, pair, T)
     L = H.transcoded(m, L0, xt) if xt else L0
     n = T * wl.k

@@ -39,7 +39,7 @@ def test_quantize_q8_1_bitexact(m, orc):
 # ------------------------------------------------------------------ a2/a4 integer block sums
 
 @pytest.mark.parametrize("typ", [synth.Q8_0, synth.Q4B, synth.NL4, synth.CB2, synth.CB3, synth.CB3X, synth.CB2X])
-@pytest.mark.parametrize("K", [256, 768, 2560])
+@pytest.mark.parametrize("K", [256, 768, 2560, 8192])
 def test_block_isum_bitexact(m, orc, typ, K):
     rows = 24
     src = {synth.CB3X: synth.CB3, synth.CB2X: synth.CB2}.get(typ, typ)
