@@ -70,14 +70,21 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
-// Wait for phase `parity` of `bar` to complete; false if it has not after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The retries of mbar_wait_bounded, out of line: the first try_wait sleeps until the phase
+// completes (or its time hint runs out), so the loop is cold code that need not sit in the callers'
+// hot loops.
+static __device__ __noinline__ bool mbar_wait_retry(uint64_t* bar, uint32_t parity) {
     const unsigned long long t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 15u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
     }
+}
+
+// Wait for phase `parity` of `bar` to complete; false if it has not after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_retry(bar, parity);
 }
 
 // 1-D bulk copy global -> shared (TMA engine), completion counted on `bar` in bytes.
