@@ -84,6 +84,41 @@ __device__ __forceinline__ uint64_t ld_pair(const uint64_t* p) {
     return v;
 }
 
+// A block whose flagged copy was not complete at the first read: wait (bounded) until all nine
+// flags equal `flag`, between reads polling the header pair alone, then stage it into `slot`.
+// Out of line, since the common case finds the block complete at once (p: its header pair, the
+// other pairs nb apart; the staging layout's offsets passed as they are in GemvArgs).
+template <int TYPE>
+static __device__ __noinline__ bool stage_flagged_wait(uint8_t* smem, int off_actq, int off_act2, int nbp, int nb,
+                                                     int slot, int b, const uint64_t* p, uint32_t flag) {
+    GemvArgs g;
+    g.off_actq = off_actq;
+    g.off_act2 = off_act2;
+    g.nbp = nbp;
+    g.nb = nb;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        for (uint32_t j = 0;; ++j) {
+            __nanosleep(64);
+            if (static_cast<uint32_t>(ld_pair(p) >> 32) == flag) break;
+            if ((j & 15u) == 15u && global_ns() - t0 > kWaitLimitNs) return false;
+        }
+        uint32_t w[kHxPairs];
+        bool ok = true;
+#pragma unroll
+        for (int k = 0; k < kHxPairs; ++k) {
+            const uint64_t v = ld_pair(p + k * nb);
+            ok = ok && static_cast<uint32_t>(v >> 32) == flag;
+            w[k] = static_cast<uint32_t>(v);
+        }
+        if (ok) {
+            put_staged<TYPE>(g, smem, slot, b, w);
+            return true;
+        }
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
 // The q8_1 h rows of entries e0 .. e0+ne-1 (ent[e].x; < 0 stages zeros) into slots slot0 ...,
 // read from their flagged copies (hx: per row kHxPairs rows of nb pairs, pair k of every block
 // side by side, so that one pair of consecutive blocks is one coalesced load across the warp): a
@@ -97,27 +132,17 @@ __device__ __forceinline__ bool stage_flagged(const GemvArgs& a, uint8_t* smem, 
         uint32_t w[kHxPairs];
         if (row >= 0) {
             const uint64_t* p = hx + static_cast<int64_t>(row) * kHxPairs * a.nb + b;
-            unsigned long long t0 = 0;
-            for (uint32_t it = 0;; ++it) {
-                uint64_t v[kHxPairs];
+            bool ok = true;
 #pragma unroll
-                for (int k = 0; k < kHxPairs; ++k) v[k] = ld_pair(p + k * a.nb);
-                bool ok = true;
-#pragma unroll
-                for (int k = 0; k < kHxPairs; ++k) {
-                    ok = ok && static_cast<uint32_t>(v[k] >> 32) == flag;
-                    w[k] = static_cast<uint32_t>(v[k]);
-                }
-                if (ok) break;
-                // not there yet: wait on the header pair alone (one load per poll, not nine),
-                // then read all nine again
-                if (it == 0) t0 = global_ns();
-                else if (global_ns() - t0 > kWaitLimitNs) return false;
-                for (uint32_t j = 0;; ++j) {
-                    __nanosleep(64);
-                    if (static_cast<uint32_t>(ld_pair(p) >> 32) == flag) break;
-                    if ((j & 15u) == 15u && global_ns() - t0 > kWaitLimitNs) return false;
-                }
+            for (int k = 0; k < kHxPairs; ++k) {
+                const uint64_t v = ld_pair(p + k * a.nb);
+                ok = ok && static_cast<uint32_t>(v >> 32) == flag;
+                w[k] = static_cast<uint32_t>(v);
+            }
+            if (!ok) {  // not there yet
+                if (!stage_flagged_wait<TYPE>(smem, a.off_actq, a.off_act2, a.nbp, a.nb, slot0 + s, b, p, flag))
+                    return false;
+                continue;
             }
         } else {
 #pragma unroll
