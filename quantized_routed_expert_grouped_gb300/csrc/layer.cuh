@@ -659,7 +659,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
             dd[7] = nwork;
             ++issued;
             nwork += items;
-            __threadfence_block();
+            // (mbarrier.arrive releases at CTA scope, the consumers' waits acquire: the descriptor
+            // and the counts are ordered before the arrival without a fence, which would also wait
+            // for the work counter's atomic still in flight)
             vmisc[0] = issued;
             vmisc[7] = nwork;
             mbar_arrive(&pub[d]);
@@ -808,8 +810,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 set_err(A.err, MOE_ERR_TIMEOUT);
                 vmisc[1] = 1;
             }
-            __threadfence_block();
-            mbar_arrive(&pub[d]);
+            mbar_arrive(&pub[d]);  // releases vmisc[5] with it
         }
     } else {
         const uint32_t loff = GT == MOE_CB3 ? lane * 4u : (lane & 15u) * 8u;
