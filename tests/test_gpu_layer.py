@@ -106,6 +106,19 @@ def test_layer_at_entry_capacity(m, orc):
     _check_layer(m, orc, CAP, CAP.pairs[0], 64, None)
 
 
+# Degenerate shapes: one expert (every token's only id: one group of T entries, two batches),
+# two experts with top-2 (two groups of T entries each, an odd batch), the smallest layer
+# (n_embd = n_ff = 256, one chunk per row).
+DEGENERATE = [synth.Workload("one_expert", 1, (4,), 1, 1, 256, 256, ((synth.Q8_0, synth.NL4),), seed=71),
+              synth.Workload("two_experts", 1, (3,), 2, 2, 512, 256, ((synth.CB2, synth.Q8_0),), seed=72),
+              synth.Workload("min_shape", 1, (1,), 4, 2, 256, 256, ((synth.CB3, synth.NL4),), seed=73)]
+
+
+@pytest.mark.parametrize("wl", DEGENERATE, ids=[w.name for w in DEGENERATE])
+def test_layer_degenerate_shapes(m, orc, wl):
+    _check_layer(m, orc, wl, wl.pairs[0], wl.T[0], None)
+
+
 def _check_layer(m, orc, wl, pair, T, xt):
     L0 = H.make_layer(wl, pair, T)
     L = H.transcoded(m, L0, xt) if xt else L0
