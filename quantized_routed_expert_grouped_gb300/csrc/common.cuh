@@ -127,6 +127,13 @@ __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
     return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
 }
 
+// dp4a with a's bytes unsigned (0..255) and b's signed.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 __device__ __forceinline__ float h2f_bits(uint32_t h16) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(h16 & 0xffffu)));
 }

@@ -637,13 +637,37 @@ __device__ __forceinline__ void slot_block(const GemvArgs& a, const uint8_t* sme
     uint32_t A[NE][8];
     float dx[NE], aux[NE];
     load_act<NE>(a, smem, c * 8 + j, slots, A, dx, aux);
-    uint32_t W[8];
-    slot_decode<TYPE>(q, W);
     const int ls = 2 * static_cast<int>((subw >> (8 * (j >> 1) + 4 * (j & 1))) & 15u) + 1;
+    if constexpr (TYPE == MOE_CB3X) {
+        // The low nibbles (weights 4k..4k+3 of word k) go into dp4a as they are; the high ones
+        // (weights 16+4k..) stay in place as 16 x code, through the unsigned-by-signed dp4a, and
+        // the sum's factor 16 comes off with one shift (exact: it is a multiple of 16), so no
+        // nibble is shifted down: 2 (low + high) = 2 low + high16 / 8.
+        uint32_t lo[4], hi[4];
 #pragma unroll
-    for (int e = 0; e < NE; ++e) {
-        const int isum = 2 * dot8(W, A[e]) + __float_as_int(aux[e]);
-        acc[e] = fmaf(static_cast<float>(ls * isum), dx[e], acc[e]);
+        for (int k = 0; k < 4; ++k) {
+            lo[k] = q[k] & 0x0f0f0f0fu;
+            hi[k] = q[k] & 0xf0f0f0f0u;
+        }
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+            int dl = 0, dh = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                dl = dp4a(lo[k], A[e][k], dl);
+                dh = dp4a_us(hi[k], A[e][4 + k], dh);
+            }
+            const int isum = 2 * dl + (dh >> 3) + __float_as_int(aux[e]);
+            acc[e] = fmaf(static_cast<float>(ls * isum), dx[e], acc[e]);
+        }
+    } else {
+        uint32_t W[8];
+        slot_decode<TYPE>(q, W);
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+            const int isum = 2 * dot8(W, A[e]) + __float_as_int(aux[e]);
+            acc[e] = fmaf(static_cast<float>(ls * isum), dx[e], acc[e]);
+        }
     }
 }
 
