@@ -465,7 +465,8 @@ def sparse_calls(m, dev, reps=20):
               for c in range(calls)]
         fused["empty" if ng == 0 else "one_group_2_entries"] = graph_us(lambda: [c.call_fused(sync) for c in cs])
     # the residency split: each call's expert is host-resident (pinned), copied into a device
-    # staging slot (one cudaMemcpyAsync per blob) before its one-launch call, all in the graph
+    # staging slot (moe_stage_blobs: the copy kernel for these pinned blobs) before its one-launch
+    # call, all in the graph
     host_gu = [synth.weight_blobs(gu_t, 2 * wl.F, wl.N, 1, synth.derive_key(wl.seed, 0, gu_t, 0), "cpu",
                                   first_blob=(7 * c) % E)[0].pin_memory() for c in range(calls)]
     host_dn = [synth.weight_blobs(dn_t, wl.N, wl.F, 1, synth.derive_key(wl.seed, 0, dn_t, 1), "cpu",

@@ -337,10 +337,14 @@ int moe_expert_grouped_fused(const moe_expert_call* call, int32_t* sync, cudaStr
 /* The residency split of #363 "experts: smaller and fewer launches for the verify window's PCIe
  * call" ("What changes": one call for the experts in VRAM, one for those that come over PCIe):
  * copy n host-resident blobs (an expert's gate/up and down blobs) into device staging slots before
- * the second call, whose pointer tables name the slots. One cudaMemcpyAsync per blob on `stream`
- * (host_src should be pinned for the copies to be asynchronous and capturable in a CUDA graph);
- * dev_dst slots are 16-byte aligned device buffers of at least bytes[i] bytes, owned by the
- * caller. Errors: MOE_E_NULL, MOE_E_SHAPE (n < 0, a size <= 0), MOE_E_ALIGN (a slot), MOE_E_CUDA. */
+ * the second call, whose pointer tables name the slots. Blobs in pinned (page-locked,
+ * device-accessible) host memory that are 16-byte aligned with sizes a multiple of 16 are copied
+ * by one kernel on `stream` that reads them over the CPU-GPU link through unified addressing (so
+ * the expert call that follows may be launched with MOE_F_PDL and overlap its prologue with the
+ * copy); any other blob by cudaMemcpyAsync (host_src should be pinned for the copies to be
+ * asynchronous and capturable in a CUDA graph). dev_dst slots are 16-byte aligned device buffers
+ * of at least bytes[i] bytes, owned by the caller. Errors: MOE_E_NULL, MOE_E_SHAPE (n < 0, a size
+ * <= 0), MOE_E_ALIGN (a slot), MOE_E_CUDA. */
 int moe_stage_blobs(const void* const* host_src, void* const* dev_dst, const int64_t* bytes, int n,
                     cudaStream_t stream);
 

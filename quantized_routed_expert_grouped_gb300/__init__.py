@@ -208,8 +208,8 @@ class ExpertCall:
 
 
 def stage_blobs(host_blobs, dev_slots, stream=None):
-    """Copy host-resident blobs (pinned uint8 CPU tensors) into device staging slots (uint8 CUDA
-    tensors, at least as large), one cudaMemcpyAsync each (moe_stage_blobs)."""
+    """Copy host-resident blobs (uint8 CPU tensors, pinned for the copy kernel) into device staging
+    slots (uint8 CUDA tensors, at least as large) with moe_stage_blobs."""
     n = len(host_blobs)
     assert len(dev_slots) == n and all(d.numel() >= h.numel() for h, d in zip(host_blobs, dev_slots))
     src = (ctypes.c_void_p * n)(*[h.data_ptr() for h in host_blobs])

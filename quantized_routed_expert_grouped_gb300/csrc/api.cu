@@ -607,10 +607,35 @@ int moe_stage_blobs(const void* const* host_src, void* const* dev_dst, const int
         if (bytes[i] <= 0) return MOE_E_SHAPE;
         if (reinterpret_cast<uintptr_t>(dev_dst[i]) & 15u) return MOE_E_ALIGN;
     }
-    for (int i = 0; i < n; ++i)
-        if (cudaMemcpyAsync(dev_dst[i], host_src[i], static_cast<size_t>(bytes[i]), cudaMemcpyHostToDevice, stream) !=
-            cudaSuccess)
+    // pinned (device-accessible) 16-byte aligned blobs of whole 16-byte words: one copy kernel
+    // that reads them through unified addressing; any other blob: cudaMemcpyAsync (a kernel must
+    // never dereference pageable host memory)
+    const void* ksrc[kStageMax];
+    void* kdst[kStageMax];
+    int64_t kbytes[kStageMax];
+    int nk = 0;
+    for (int i = 0; i < n; ++i) {
+        cudaPointerAttributes at{};
+        const bool pinned = cudaPointerGetAttributes(&at, host_src[i]) == cudaSuccess &&
+                            at.type == cudaMemoryTypeHost && at.devicePointer != nullptr;
+        if (!pinned) cudaGetLastError();  // (clear a lookup's error state)
+        const uintptr_t al =
+            reinterpret_cast<uintptr_t>(pinned ? at.devicePointer : host_src[i]) | reinterpret_cast<uintptr_t>(dev_dst[i]) |
+            static_cast<uintptr_t>(bytes[i]);
+        if (pinned && (al & 15u) == 0) {
+            ksrc[nk] = at.devicePointer;
+            kdst[nk] = dev_dst[i];
+            kbytes[nk] = bytes[i];
+            if (++nk == kStageMax) {
+                if (launch_stage_blobs(ksrc, kdst, kbytes, nk, stream) != cudaSuccess) return MOE_E_CUDA;
+                nk = 0;
+            }
+        } else if (cudaMemcpyAsync(dev_dst[i], host_src[i], static_cast<size_t>(bytes[i]), cudaMemcpyHostToDevice,
+                                   stream) != cudaSuccess) {
             return MOE_E_CUDA;
+        }
+    }
+    if (nk && launch_stage_blobs(ksrc, kdst, kbytes, nk, stream) != cudaSuccess) return MOE_E_CUDA;
     return MOE_OK;
 }
 

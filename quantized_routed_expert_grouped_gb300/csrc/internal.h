@@ -125,6 +125,12 @@ cudaError_t launch_combine(const float* out, int64_t os, const int32_t* ids, con
 cudaError_t launch_transcode_cb(int src_type, const int8_t* codebook, int dst_type, int K, int rows, int n_blobs,
                                 const void* const* src_blobs, void* const* dst_blobs, int32_t* err, cudaStream_t s);
 
+// The residency split's staging copies: blob i < n, bytes[i] (a multiple of 16) from src[i] (pinned
+// host memory, device-accessible, 16-byte aligned) to dst[i] (device, 16-byte aligned), by one
+// kernel per kStageMax blobs.
+constexpr int kStageMax = 8;
+cudaError_t launch_stage_blobs(const void* const* src, void* const* dst, const int64_t* bytes, int n, cudaStream_t s);
+
 cudaError_t launch_qsa_block_scores(const float* q, int T, const int8_t* keys, const float* scale, long long n_blocks,
                                     float* scores, cudaStream_t s);
 

@@ -215,7 +215,7 @@ def test_fused_bad_groups_are_reported_and_skipped(m, orc):
 
 def test_staged_host_expert_call(m, orc):
     """The residency split: a second call whose expert lives in pinned host memory, copied into a
-    device staging slot with moe_stage_blobs (one cudaMemcpyAsync per blob) and run with the
+    device staging slot with moe_stage_blobs (its copy kernel, pinned blobs) and run with the
     one-launch call, first eagerly and then captured with the copies in one CUDA graph; its out
     rows equal the same call on the device-resident copy of the expert bit for bit, and the
     oracle's chain."""
@@ -279,3 +279,31 @@ def test_staged_host_expert_call(m, orc):
     orc.grouped_gemv(L.dn_t, wl.F, wl.N, dnb, ge[:1], gs[:2], 1, hq_ref, ent_out=ed, out=oref, cb=L.cb_dn)
     rows = [2, n + 4]
     assert H.rel_err(B.out.cpu().numpy()[rows], oref[rows]) <= (TOL if flips == 0 and scale_diffs == 0 else 2e-3)
+
+
+def test_stage_blobs_kernel_and_copy_paths(m):
+    """moe_stage_blobs: pinned 16-byte aligned blobs of whole 16-byte words go through the copy
+    kernel (ten of them: two launches of at most eight), a pinned blob of an odd size and pageable
+    blobs through cudaMemcpyAsync; every slot ends equal to its source byte for byte, eagerly and,
+    for the pinned blobs, captured in a CUDA graph."""
+    g = torch.Generator().manual_seed(5)
+    sizes = [1_105_920, 2_088_960] + [4096 * (i + 1) + 16 * i for i in range(8)]
+    pinned = [torch.randint(0, 256, (n,), dtype=torch.uint8, generator=g).pin_memory() for n in sizes]
+    odd = torch.randint(0, 256, (1000,), dtype=torch.uint8, generator=g).pin_memory()
+    pageable = [torch.randint(0, 256, (n,), dtype=torch.uint8, generator=g) for n in (65536, 4112)]
+    srcs = pinned + [odd] + pageable
+    slots = [torch.zeros(h.numel(), dtype=torch.uint8, device="cuda") for h in srcs]
+    m.stage_blobs(srcs, slots)
+    torch.cuda.synchronize()
+    for h, d in zip(srcs, slots):
+        assert torch.equal(d.cpu(), h)
+    for d in slots:
+        d.zero_()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        m.stage_blobs(pinned + [odd], slots[:len(pinned) + 1], stream=s)
+    graph.replay()
+    torch.cuda.synchronize()
+    for h, d in zip(pinned + [odd], slots):
+        assert torch.equal(d.cpu(), h)
