@@ -22,6 +22,11 @@ __device__ __forceinline__ void set_err(int32_t* err, int bits) {
 // wait: block until the grids this one depends on have completed and their writes are visible
 // (a no-op when the launch carries no programmatic dependency).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// a hint: bring the 128-byte line holding p into L2 (returns nothing, changes no result; L2 stays
+// coherent with later writes to the line, so it may precede pdl_wait)
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 // let the next grid in the stream start launching (it still waits for this grid's completion
 // before its own pdl_wait returns).
 __device__ __forceinline__ void pdl_trigger() {

@@ -467,6 +467,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     const uint8_t** pcA = L.off_ptr ? reinterpret_cast<const uint8_t**>(smem + L.off_ptr) : nullptr;
     const uint8_t** pcD = pcA ? pcA + A.n_experts : nullptr;
 
+    // the call's inputs (routing ids, activation rows, up to NT lines of each) into L2 while the
+    // grid before this one finishes: the first reads after the dependency wait then hit L2
+    if constexpr (!GIVEN) {
+        const uintptr_t xa = reinterpret_cast<uintptr_t>(L.x) & ~uintptr_t(127);
+        const uintptr_t xe = reinterpret_cast<uintptr_t>(L.x + static_cast<int64_t>(L.T) * A.K);
+        const uintptr_t ia = reinterpret_cast<uintptr_t>(L.ids) & ~uintptr_t(127);
+        const uintptr_t ie = reinterpret_cast<uintptr_t>(L.ids + n);
+        const uintptr_t xl = xa + static_cast<uintptr_t>(tid) * 128u;
+        const uintptr_t il = ia + static_cast<uintptr_t>(NT - 1 - tid) * 128u;
+        if (xl < xe) prefetch_l2(reinterpret_cast<const void*>(xl));
+        if (il < ie) prefetch_l2(reinterpret_cast<const void*>(il));
+    }
     if (tid < 256) misc[tid] = 0;
     if (tid == 0) {
         for (int s = 0; s < SB; ++s) {
