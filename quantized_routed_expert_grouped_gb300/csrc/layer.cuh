@@ -313,22 +313,40 @@ __device__ __forceinline__ void build_tables(const LayerArgs& L, const uint8_t* 
 // (MOE_ERR_START), its weight pointers are misaligned (MOE_ERR_ALIGN) or one of its entries has a
 // source row outside the activation rows or a destination outside the output rows
 // (MOE_ERR_ENTRY; the whole group, where the separate kernels skip the entry alone). The tables
-// number entries from grp_start[0] (*ebase), like a routed call's from 0.
+// number entries from grp_start[0] (*ebase), like a routed call's from 0. G: n_groups as read after
+// the dependency wait. Two rounds of dependent reads: grp_start[0] with the lanes' first groups,
+// then every entry of the table's range at once (a lane per entry, in bounds for any index below
+// cap_entries), whose rows go into the tables before the groups are checked against them.
 template <int GT, int DT>
-__device__ __forceinline__ void load_groups(const LayerArgs& L, const uint8_t* const* pcA, const uint8_t* const* pcD,
-                                            GroupInfo* giA, GroupInfo* giD, int2* entA, int2* entD, int* rng,
-                                            int* ebase, int lane) {
+__device__ __forceinline__ void load_groups(const LayerArgs& L, int G, const uint8_t* const* pcA,
+                                            const uint8_t* const* pcD, GroupInfo* giA, GroupInfo* giD, int2* entA,
+                                            int2* entD, int* rng, int* ebase, int lane) {
     const GemvArgs& A = L.gu;
     const GemvArgs& D = L.dn;
     const bool report = blockIdx.x == 0;
-    int G = *L.g_ng;
     if (G < 0 || G > L.g_cap_groups) {
         if (report && lane == 0) set_err(A.err, MOE_ERR_NGROUPS);
         G = G < 0 ? 0 : L.g_cap_groups;
     }
     const int base = G > 0 ? L.g_start[0] : 0;
+    int x0 = 0, s0 = 0, s1 = 0;  // the lane's first group (these loads do not wait for base)
+    if (lane < G) {
+        x0 = L.g_expert[lane];
+        s0 = L.g_start[lane];
+        s1 = L.g_start[lane + 1];
+    }
+    if (base >= 0) {
+        const int elim = base + L.n < L.g_cap_entries ? base + L.n : L.g_cap_entries;
+#pragma unroll 4
+        for (int e = base + lane; e < elim; e += 32) {
+            entA[e - base] = make_int2(L.g_src[e], e - base);
+            entD[e - base] = make_int2(e - base, L.g_dst[e]);
+        }
+    }
+    __syncwarp();
     for (int g = lane; g < G; g += 32) {
-        const int x = L.g_expert[g], e0 = L.g_start[g], e1 = L.g_start[g + 1];
+        const int x = g == lane ? x0 : L.g_expert[g], e0 = g == lane ? s0 : L.g_start[g],
+                  e1 = g == lane ? s1 : L.g_start[g + 1];
         bool ok = true;
         const uint8_t* pa = nullptr;
         const uint8_t* pd = nullptr;
@@ -347,8 +365,8 @@ __device__ __forceinline__ void load_groups(const LayerArgs& L, const uint8_t* c
                 ok = false;
                 if (report) set_err(A.err, MOE_ERR_ALIGN);
             } else {
-                for (int e = e0; e < e1; ++e) {
-                    const int sr = L.g_src[e], ds = L.g_dst[e];
+                for (int e = e0 - base; e < e1 - base; ++e) {
+                    const int sr = entA[e].x, ds = entD[e].y;
                     if (sr < 0 || sr >= L.T || ds < 0 || ds >= L.g_out_rows) {
                         ok = false;
                         if (report) set_err(A.err, MOE_ERR_ENTRY);
@@ -359,11 +377,6 @@ __device__ __forceinline__ void load_groups(const LayerArgs& L, const uint8_t* c
         }
         giA[g] = GroupInfo{pa, x, e0 - base, e1 - base, ok ? 1 : 0};
         giD[g] = GroupInfo{pd, x, e0 - base, e1 - base, ok ? 1 : 0};
-        if (ok)
-            for (int e = e0; e < e1; ++e) {
-                entA[e - base] = make_int2(L.g_src[e], e - base);
-                entD[e - base] = make_int2(e - base, L.g_dst[e]);
-            }
     }
     if (lane == 0) {
         *rng = G;
@@ -505,8 +518,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     pdl_trigger();
     // pre-built groups and none in this call (the same value for every thread): nothing to stage
     // or stream, only the end-of-call words
+    int given_ng = 0;  // pre-built groups: n_groups, read once here (also by load_groups)
     if constexpr (GIVEN) {
-        if (__ldcg(L.g_ng) == 0) {
+        given_ng = __ldcg(L.g_ng);
+        if (given_ng == 0) {
             end_call(L, misc, tid);
             return;
         }
@@ -554,7 +569,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 vmisc[6] = early;
             }
         }
-        if constexpr (GIVEN) load_groups<GT, DT>(L, pcA, pcD, giA, giD, entA, entD, rng, &misc[12], lane);
+        if constexpr (GIVEN) load_groups<GT, DT>(L, given_ng, pcA, pcD, giA, giD, entA, entD, rng, &misc[12], lane);
         else build_tables<GT, DT>(L, pcA, pcD, rgx, rgs, rng, rsrc, rdst, giA, giD, entA, entD, misc, lane);
         if (lane == 0) misc[3] = static_cast<int>(flag);
         flag = __shfl_sync(0xffffffffu, flag, 0);

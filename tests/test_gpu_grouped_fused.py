@@ -175,8 +175,9 @@ def test_fused_empty_calls_in_a_sync_pair(m, orc):
 
 def test_fused_bad_groups_are_reported_and_skipped(m, orc):
     """n_groups above cap is clamped (MOE_ERR_NGROUPS); a group with an expert id out of range
-    (MOE_ERR_EXPERT) or an entry whose source row is out of range (MOE_ERR_ENTRY) is skipped and
-    its rows stay NaN; every other group equals the three-launch call."""
+    (MOE_ERR_EXPERT) or an entry whose source or destination row is out of range (MOE_ERR_ENTRY)
+    is skipped and its rows stay NaN; every other group equals the three-launch call. (The CTAs
+    whose first work item is a unit of a skipped group copy nothing ahead of the tables.)"""
     wl = synth.WORKLOADS["verify"]
     L = H.make_layer(wl, (synth.CB2, synth.NL4), 4)
     B = H.make_bufs(L)
@@ -187,17 +188,19 @@ def test_fused_bad_groups_are_reported_and_skipped(m, orc):
     gs = B.grp_start.cpu().numpy()
     G = int(B.n_groups.item())
     ed = B.ent_dst.cpu().numpy()
-    # group 0: expert out of range; group 1: one entry's source row out of range
+    # group 0: expert out of range; group 1: one entry's source row out of range; group 2: one
+    # entry's destination row out of range
+    assert G >= 4
     B.grp_expert[0] = wl.E + 5
-    bad_e = int(gs[1])
-    B.ent_src[bad_e] = 99
+    B.ent_src[int(gs[1])] = 99
+    B.ent_dst[int(gs[3]) - 1] = B.out.shape[0] + 1
     B.out.fill_(float("nan"))
     sync = _sync(m, B, wl)
     H.expert_call(m, L, B).call_fused(sync)
     torch.cuda.synchronize()
     assert int(B.err.item()) == 2 | 8
     out, r = B.out.cpu().numpy(), ref.cpu().numpy()
-    skipped = set(range(gs[0], gs[2]))
+    skipped = set(range(gs[0], gs[3]))
     for e in range(gs[0], gs[G]):
         row = int(ed[e])
         if e in skipped:
