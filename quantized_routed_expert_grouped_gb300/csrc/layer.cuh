@@ -707,10 +707,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         // the first item of CTA b is item b; later ones come from the counter, whose next value is
         // fetched while the current item streams
         // (the counter's value is consumed only at the loop increment, so the atomic's round trip
-        // overlaps the item's copies instead of stalling lane 0 before them)
+        // overlaps the item's copies instead of stalling lane 0 before them; with pre-built groups
+        // and no item past the first round, as in a small second call, nothing is claimed: 0.26 us
+        // less per such call, where the routed form's window lost 0.3 % to the same test)
         int nx = 0;
+        const bool claim = !GIVEN || nitems > static_cast<int>(gridDim.x);
         for (int i = blockIdx.x; !stop && i < nitems; i = static_cast<int>(gridDim.x) + __shfl_sync(0xffffffffu, nx, 0)) {
-            if (lane == 0) nx = atomicAdd(work, 1);
+            if (lane == 0) nx = claim ? atomicAdd(work, 1) : nitems;
             if (i < nunits) {
                 const int g = i / upg, jb = i - g * upg;
                 const GroupInfo gr = giA[g];
