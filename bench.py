@@ -384,8 +384,9 @@ def sparse_calls(m, dev, reps=20):
     32, scattered destinations, its own expert from a 558 MB pool read cold), with grid_groups 0
     (the capacity) and 1; then ("fused") the same calls as one moe_expert_grouped_fused launch
     each, and the residency split: each call's expert copied from pinned host memory into a device
-    staging slot (moe_stage_blobs) before its call, copies and calls in one graph. Microseconds per
-    call from CUDA events around graph replays."""
+    staging slot (moe_stage_blobs) before its call, copies and calls in one graph; and both one-group
+    forms again with the gate/up blobs as CB2X slots (transcoded at load, the same integers).
+    Microseconds per call from CUDA events around graph replays."""
     wl = synth.WORKLOADS["sparse"]
     gu_t, dn_t = wl.pairs[0]
     E, calls, n = 256, 48, 4 * wl.k
@@ -487,6 +488,39 @@ def sparse_calls(m, dev, reps=20):
             cs[c].call_fused(sync)
     fused["host_staged_one_group_2_entries"] = graph_us(staged)
     fused["host_staged_bytes_per_call"] = int(host_gu[0].numel() + host_dn[0].numel())
+    # the same one-group calls on CB2X slots (the gate/up blobs transcoded at load time, the same
+    # integers): device-resident, and staged from host memory (host blobs transcoded once, untimed)
+    xb = synth.blob_bytes(synth.CB2X, 2 * wl.F, wl.N)
+    terr = torch.zeros(1, **i32)
+    pool_gx = torch.empty((E, xb), dtype=torch.uint8, device=dev)
+    m.transcode_cb(gu_t, cb_gu, synth.CB2X, wl.N, 2 * wl.F, tab_gu, tab(pool_gx), terr)
+    tab_gx = tab(pool_gx)
+    ges5 = [torch.tensor([(5 * c) % E] + [0] * (n - 1), **i32) for c in range(calls)]
+    cx = [m.ExpertCall(synth.CB2X, None, dn_t, cb_dn, wl.N, wl.F, tab_gx, tab_dn, E, ges5[c], gs, ngt, n, 0, cap_e,
+                       xq, es, ed, gu, hq, out, err, m.F_PDL | m.F_SYNC_PAIR | (m.F_SYNC_ODD if c % 2 else 0))
+          for c in range(calls)]
+    fused["one_group_2_entries_cb2x_slots"] = graph_us(lambda: [c.call_fused(sync) for c in cx])
+    one = lambda t: torch.tensor([t.data_ptr()], dtype=torch.int64, device=dev)
+    host_gx = []
+    for c in range(calls):
+        src, dst = host_gu[c].to(dev), torch.empty(xb, dtype=torch.uint8, device=dev)
+        m.transcode_cb(gu_t, cb_gu, synth.CB2X, wl.N, 2 * wl.F, one(src), one(dst), terr)
+        host_gx.append(dst.cpu().pin_memory())
+    torch.cuda.synchronize()
+    if int(terr.item()):
+        raise RuntimeError(f"sparse calls: transcoder error bits {int(terr.item())}")
+    slot_gx = torch.empty(xb, dtype=torch.uint8, device=dev)
+    stab_gx = torch.full((E,), slot_gx.data_ptr(), dtype=torch.int64, device=dev)
+    csx = [m.ExpertCall(synth.CB2X, None, dn_t, cb_dn, wl.N, wl.F, stab_gx, stab_dn, E, ges[c], gs, ngt, n, 0, cap_e,
+                        xq, es, ed, gu, hq, out, err, m.F_PDL | m.F_SYNC_PAIR | (m.F_SYNC_ODD if c % 2 else 0))
+           for c in range(calls)]
+
+    def staged_x():
+        for c in range(calls):
+            m.stage_blobs([host_gx[c], host_dn[c]], [slot_gx, slot_dn])
+            csx[c].call_fused(sync)
+    fused["host_staged_one_group_2_entries_cb2x_slots"] = graph_us(staged_x)
+    fused["host_staged_bytes_per_call_cb2x_slots"] = int(host_gx[0].numel() + host_dn[0].numel())
     fused.update({"unit": "us/call", "calls_per_graph": calls, "launches_per_call": 1})
     res["fused"] = fused
     return res
