@@ -54,6 +54,21 @@
 namespace moe {
 
 constexpr int kDescRing = 16;  // tile descriptors in flight per CTA (ring indices)
+
+// Division of the non-negative ring and item indices by a divisor fixed for the launch (the ring
+// depth, the chunks per row): one multiply-high by a reciprocal computed once per CTA instead of a
+// division sequence per work item. Exact for every q below 2^32 / (d - 1), far beyond the indices
+// a call reaches; d = 1 passes q through.
+struct SmallDiv {
+    uint32_t m;
+    int d;
+    __device__ __forceinline__ explicit SmallDiv(int dv)
+        : m(dv > 1 ? 0xFFFFFFFFu / static_cast<uint32_t>(dv) + 1u : 0u), d(dv) {}
+    __device__ __forceinline__ int div(int q) const {
+        return d > 1 ? static_cast<int>(__umulhi(static_cast<uint32_t>(q), m)) : q;
+    }
+    __device__ __forceinline__ int mod(int q) const { return q - div(q) * d; }
+};
 constexpr int kUnitBufs = 4;   // gate/up units in flight per CTA (h buffers in shared memory)
 
 // Advance a sync array's call epoch (the next call's flag is epoch + 1). The epoch never takes
@@ -632,6 +647,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     // The producer warp also stages each down group's q8_1 h rows (4-entry batches) into one of
     // two buffers: a buffer is refilled once every tile that read it has been released.
     const int S = A.stages, RT = A.RT, half = RT >> 1, RTD = D.RT;
+    const SmallDiv divS(S);
     const int tpg = (D.rows + RTD - 1) / RTD;
     int dchunk = (G * tpg) / (2 * static_cast<int>(gridDim.x));  // about two down items per CTA
     dchunk = dchunk < 1 ? 1 : dchunk > 3 ? 3 : dchunk;
@@ -659,7 +675,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         // ring slot j % S free for index j: the tile S indices earlier released (lane 0)
         auto slot_free = [&](int j) -> bool {
             if (vmisc[1]) return false;
-            if (j >= S && !mbar_wait_bounded(&empty[j % S], static_cast<uint32_t>(j / S - 1) & 1u)) {
+            const int jq = divS.div(j), js = j - jq * S;
+            if (j >= S && !mbar_wait_bounded(&empty[js], static_cast<uint32_t>(jq - 1) & 1u)) {
                 set_err(A.err, MOE_ERR_TIMEOUT);
                 vmisc[1] = 1;
                 return false;
@@ -697,10 +714,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         const uint64_t pol = l2_evict_first();  // the weights are read once per call
         // copy of ring index j's tile into its slot; vmisc[6]: copies issued (lane 0)
         auto copy_tile = [&](int j, const uint8_t* src0, uint32_t b0, const uint8_t* src1, uint32_t b1) {
-            uint8_t* dst = smem + A.off_ring + static_cast<size_t>(j % S) * A.stage_bytes;
-            mbar_arrive_expect_tx(&full[j % S], b0 + b1);
-            bulk_g2s_hint(dst, src0, b0, &full[j % S], pol);
-            if (b1) bulk_g2s_hint(dst + b0, src1, b1, &full[j % S], pol);
+            const int js = divS.mod(j);
+            uint8_t* dst = smem + A.off_ring + static_cast<size_t>(js) * A.stage_bytes;
+            mbar_arrive_expect_tx(&full[js], b0 + b1);
+            bulk_g2s_hint(dst, src0, b0, &full[js], pol);
+            if (b1) bulk_g2s_hint(dst + b0, src1, b1, &full[js], pol);
             vmisc[6] = j + 1;
         };
         const uint32_t hb = static_cast<uint32_t>(half) * static_cast<uint32_t>(A.row_bytes);
@@ -776,7 +794,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                             if (st_n >= nbuf) {
                                 const int lim = nbuf == 2 ? st_p0 : nbuf == 3 ? st_p1 : nbuf == 4 ? st_p2 : nbuf == 5 ? st_p3 : st_p4;
                                 for (int j = issued - S > 0 ? issued - S : 0; ok && j < lim; ++j)
-                                    ok = mbar_wait_bounded(&empty[j % S], static_cast<uint32_t>(j / S) & 1u);
+                                    ok = mbar_wait_bounded(&empty[divS.mod(j)], static_cast<uint32_t>(divS.div(j)) & 1u);
                             }
                             st_p4 = st_p3;
                             st_p3 = st_p2;
@@ -844,6 +862,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
         }
     } else {
         const uint32_t loff = GT == MOE_CB3 ? lane * 4u : (lane & 15u) * 8u;
+        const SmallDiv divN(D.nch);
         const int64_t gst = A.out_stride;
         // the ring index whose work items are [qb, qb + qn), its descriptor (qn < 0: not read yet)
         int q = 0, qb = 0, qn = -1;
@@ -885,10 +904,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 qn = -1;
             }
             if (!have) break;
-            const int slot = q % S, j = it - qb;
+            const int qs = divS.div(q), slot = q - qs * S, j = it - qb;
             const uint8_t* tile = smem + A.off_ring + static_cast<size_t>(slot) * A.stage_bytes;
             float* part = reinterpret_cast<float*>(smem + A.off_part + static_cast<size_t>(slot) * A.part_bytes);
-            if (!vmisc[1] && !mbar_wait_bounded(&full[slot], static_cast<uint32_t>(q / S) & 1u)) {
+            if (!vmisc[1] && !mbar_wait_bounded(&full[slot], static_cast<uint32_t>(qs) & 1u)) {
                 set_err(A.err, MOE_ERR_TIMEOUT);
                 vmisc[1] = 1;
             }
@@ -964,7 +983,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
                 // ---- (sub-tile, chunk) item j of down tile rows a0 .. a0+a1-1 of group g for entries
                 // e0 .. e0+ne-1, whose h rows the producer staged in slots a6 .. a6+ne-1
                 const int row0 = a0, nrows = a1, s0 = a6;
-                const int nsb = (nrows + 31) >> 5, sb = j / D.nch, c = j - sb * D.nch;
+                const int nsb = (nrows + 31) >> 5, sb = divN.div(j), c = j - sb * D.nch;
                 const int nr = nrows - sb * 32 < 32 ? nrows - sb * 32 : 32;
                 const int slots[kLayerBatch] = {s0, s0 + (ne > 1 ? 1 : 0)};
                 if (lane < nr)
