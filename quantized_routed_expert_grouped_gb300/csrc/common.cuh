@@ -75,6 +75,21 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
+// Division of the non-negative ring and item indices by a divisor fixed for the launch (a ring
+// depth, chunks or row blocks per row or group): one multiply-high by a reciprocal computed once per CTA instead of a
+// division sequence per work item. Exact for every q below 2^32 / (d - 1), far beyond the indices
+// a call reaches; d = 1 passes q through.
+struct SmallDiv {
+    uint32_t m;
+    int d;
+    __device__ __forceinline__ explicit SmallDiv(int dv)
+        : m(dv > 1 ? 0xFFFFFFFFu / static_cast<uint32_t>(dv) + 1u : 0u), d(dv) {}
+    __device__ __forceinline__ int div(int q) const {
+        return d > 1 ? static_cast<int>(__umulhi(static_cast<uint32_t>(q), m)) : q;
+    }
+    __device__ __forceinline__ int mod(int q) const { return q - div(q) * d; }
+};
+
 // The retries of mbar_wait_bounded, out of line: the first try_wait sleeps until the phase
 // completes (or its time hint runs out), so the loop is cold code that need not sit in the callers'
 // hot loops.

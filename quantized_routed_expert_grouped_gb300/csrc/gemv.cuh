@@ -356,8 +356,11 @@ struct Tile {
     int g, row0, nrows;
 };
 
-__device__ __forceinline__ Tile next_tile(long long& cur, long long end, int rbpg, int rt8) {
-    const int g = static_cast<int>(cur / rbpg);
+// rdiv divides by rbpg; qlim: the indices below which its reciprocal is exact (the 64-bit
+// division beyond)
+__device__ __forceinline__ Tile next_tile(long long& cur, long long end, int rbpg, int rt8, const SmallDiv& rdiv,
+                                          long long qlim) {
+    const int g = cur < qlim ? rdiv.div(static_cast<int>(cur)) : static_cast<int>(cur / rbpg);
     const int off = static_cast<int>(cur - static_cast<long long>(g) * rbpg);
     long long n = rbpg - off < rt8 ? rbpg - off : rt8;
     if (n > end - cur) n = end - cur;
@@ -816,7 +819,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
     long long* cum = reinterpret_cast<long long*>(gi + a.cap_groups);
     int2* ent = reinterpret_cast<int2*>(smem + a.off_ent);  // per entry: (act row or -1, out row)
     const int S = a.stages;
+    const SmallDiv sdiv(S);
     const int rbpg = a.rows >> 3, rt8 = a.RT >> 3;
+    // (the 2^31 - 1 cap keeps the index's int conversion exact)
+    const SmallDiv rdiv(rbpg);
+    const long long qlim = rbpg > 1 ? (0xFFFFFFFFll / (rbpg - 1) < 0x7FFFFFFFll ? 0xFFFFFFFFll / (rbpg - 1) : 0x7FFFFFFFll)
+                                    : 0x7FFFFFFFll;
     // the whole activation matrix fits in the act region: staged once, indexed by act row
     const bool all_rows = a.n_act_rows <= a.act_cap;
 
@@ -908,12 +916,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
     const uint64_t pol = l2_evict_first();  // the weights are read once per call
     auto produce_one = [&](bool wait_empty) -> int {  // 1 issued, 0 range exhausted, -1 timeout
         while (pcur < rb1) {
-            const Tile t = next_tile(pcur, rb1, rbpg, rt8);
+            const Tile t = next_tile(pcur, rb1, rbpg, rt8, rdiv, qlim);
             const GroupInfo g = gi[t.g];
             if (g.cost == 0) continue;
-            const int s = issued % S;
+            const int iq = sdiv.div(issued), s = issued - iq * S;
             if (wait_empty && issued >= S) {
-                if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>(issued / S - 1) & 1u)) return -1;
+                if (!mbar_wait_bounded(&empty[s], static_cast<uint32_t>(iq - 1) & 1u)) return -1;
             }
             const uint32_t bytes = static_cast<uint32_t>(t.nrows) * static_cast<uint32_t>(a.row_bytes);
             mbar_arrive_expect_tx(&full[s], bytes);
@@ -980,19 +988,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1) gemv_kernel(const GemvArgs a) 
         return;
     }
     const int TPe = fast ? a.TP : 1;
+    const SmallDiv tdiv(TPe);
     const int scnt = a.WPS * 32, st = ct - set * scnt;  // thread index within the set
 
     long long ccur = rb0;
     int k = 0, cur_g = -1, cur_b0 = -1;
     bool aborted = false;
     while (ccur < rb1) {
-        const Tile t = next_tile(ccur, rb1, rbpg, rt8);
+        const Tile t = next_tile(ccur, rb1, rbpg, rt8, rdiv, qlim);
         const GroupInfo g = gi[t.g];
         if (g.cost == 0) continue;
         const int kk = k++;
-        if (kk % TPe != set) continue;
-        const int slot = kk % S;
-        const uint32_t parity = static_cast<uint32_t>(kk / S) & 1u;
+        if (tdiv.mod(kk) != set) continue;
+        const int kq = sdiv.div(kk), slot = kk - kq * S;
+        const uint32_t parity = static_cast<uint32_t>(kq) & 1u;
         const uint8_t* tile = smem + a.off_ring + static_cast<size_t>(slot) * a.stage_bytes;
         float* part = reinterpret_cast<float*>(smem + a.off_part + static_cast<size_t>(slot) * a.part_bytes);
         if (!aborted && !(wait_issued(misc, kk) && mbar_wait_bounded(&full[slot], parity))) {

@@ -54,21 +54,6 @@
 namespace moe {
 
 constexpr int kDescRing = 16;  // tile descriptors in flight per CTA (ring indices)
-
-// Division of the non-negative ring and item indices by a divisor fixed for the launch (the ring
-// depth, the chunks per row): one multiply-high by a reciprocal computed once per CTA instead of a
-// division sequence per work item. Exact for every q below 2^32 / (d - 1), far beyond the indices
-// a call reaches; d = 1 passes q through.
-struct SmallDiv {
-    uint32_t m;
-    int d;
-    __device__ __forceinline__ explicit SmallDiv(int dv)
-        : m(dv > 1 ? 0xFFFFFFFFu / static_cast<uint32_t>(dv) + 1u : 0u), d(dv) {}
-    __device__ __forceinline__ int div(int q) const {
-        return d > 1 ? static_cast<int>(__umulhi(static_cast<uint32_t>(q), m)) : q;
-    }
-    __device__ __forceinline__ int mod(int q) const { return q - div(q) * d; }
-};
 constexpr int kUnitBufs = 4;   // gate/up units in flight per CTA (h buffers in shared memory)
 
 // Advance a sync array's call epoch (the next call's flag is epoch + 1). The epoch never takes
