@@ -950,19 +950,27 @@ def run_case(args):
     if args.case_aux:
         # the kernels around the path, once per step each on the same layer's shapes: router top-k
         # (T x 128 logits), the weighted combine (T x 8 rows of 2560), the load-time transcoding of
-        # the layer's 128 CB3 gate/up blobs to CB3X (200 MB read), and QSA block scores at 1M tokens
+        # the layer's 128 CB3 gate/up blobs to CB3X (200 MB read), QSA block scores at 1M tokens,
+        # and the staging copies of the residency split
         logits = torch.from_numpy(np.random.default_rng(3).standard_normal((T, WL.E)).astype(np.float32)).to(dev)
         pool_tx = torch.empty((WL.E, synth.blob_bytes(XT, 2 * WL.F, WL.N)), dtype=torch.uint8, device=dev)
         nb = synth.QSA_CONTEXTS["1M"]
         qk, qs = synth.qsa_keys(nb, 77, device=dev)
         qq = torch.from_numpy(synth.qsa_queries(T, 5)).to(dev)
+        # the residency split's staging copies: two experts' CB3X gate/up and NL4 down blobs
+        # (6.39 MB) from pinned host memory into device slots
+        hbl = [torch.zeros(synth.blob_bytes(t, r, c), dtype=torch.uint8, pin_memory=True)
+               for t, r, c in ((XT, 2 * WL.F, WL.N), (DN_T, WL.N, WL.F)) * 2]
+        sl = [torch.empty(h.numel(), dtype=torch.uint8, device=dev) for h in hbl]
         for _ in range(args.steps):
             tid, tw = m.router_topk(logits, WL.k)
             y = m.combine(out, tid, tw, WL.E)
             m.transcode_cb(GU_T, cb_gu, XT, WL.N, 2 * WL.F, tab(pool_gu), tab(pool_tx), err)
             sc = m.qsa_block_scores(qq, qk, qs)
+            m.stage_blobs(hbl, sl)
         torch.cuda.synchronize()
-        extra = {"aux": "router_topk, combine, transcode (CB3 -> CB3X, 128 experts), qsa (1M tokens)",
+        extra = {"aux": "router_topk, combine, transcode (CB3 -> CB3X, 128 experts), qsa (1M tokens), "
+                        "stage_blobs (2 experts, 6.39 MB from pinned host memory)",
                  "y_finite": bool(torch.isfinite(y).all().item()), "scores": int(sc.numel())}
     print(json.dumps({"case": f"one layer of window48 at T={T}" + (" (fused)" if args.case_fused else ""),
                       "err": int(err.item()),
@@ -976,7 +984,7 @@ def main():
     ap.add_argument("--case-slot", action="store_true", help="profiling case with the gate/up pool in slot layout")
     ap.add_argument("--case-fused", action="store_true", help="profiling case with the fused layer launch")
     ap.add_argument("--case-aux", action="store_true",
-                    help="profiling case: also run the router, combine, transcoding and QSA kernels")
+                    help="profiling case: also run the router, combine, transcoding, QSA and staging kernels")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
