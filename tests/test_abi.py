@@ -110,3 +110,38 @@ def test_layer_call_host_errors(m):
     assert call(n_experts=0) == -4 and call(n_experts=(1 << 26) + 1) == -4
     assert call(sync=d + 4) == -6                                 # sync holds 8-byte pairs
 
+
+
+def test_fused_grouped_call_and_staging_host_errors(m):
+    """The one-launch expert call and the staging copies reject bad host-visible arguments before
+    any CUDA call (so these run without a GPU)."""
+    L = m.lib()
+    W = m.WFmt
+    d = 16
+
+    def call(sync=d, **kw):
+        f = dict(gu_fmt=W(1, None), down_fmt=W(3, ctypes.c_void_p(d)), n_embd=2560, n_ff=768, n_experts=64,
+                 w_gu=d, w_down=d, grp_expert=d, grp_start=d, n_groups=d, cap_groups=32, grid_groups=0,
+                 cap_entries=34, xq=d, n_xq_rows=4, ent_src=d, ent_dst=d, gu=d, hq=d, out=d, out_rows=38,
+                 out_row_stride=2560, err=None, flags=0)
+        f.update(kw)
+        c = m.ExpertCallC(**f)
+        return L.moe_expert_grouped_fused(ctypes.byref(c), None if sync is None else ctypes.c_void_p(sync), None)
+
+    assert L.moe_expert_grouped_fused(None, ctypes.c_void_p(d), None) == -1
+    assert call(sync=None) == -1 and call(grp_start=None) == -1 and call(ent_dst=None) == -1
+    assert call(down_fmt=W(4, ctypes.c_void_p(d))) == -2        # CB2 down: not a down format of the fused call
+    assert call(n_ff=700) == -3
+    assert call(cap_groups=0) == -4 and call(n_xq_rows=0) == -4 and call(out_rows=0) == -4
+    assert call(out_row_stride=100) == -3
+    assert call(xq=d + 2) == -6 and call(gu=d + 8) == -6 and call(sync=d + 4) == -6
+    # staging: n < 0, a NULL blob or slot, a size <= 0, a slot not 16-byte aligned; n = 0 is a no-op
+    src = (ctypes.c_void_p * 2)(d, d)
+    dst = (ctypes.c_void_p * 2)(32, 48)
+    by = (ctypes.c_int64 * 2)(64, 64)
+    assert L.moe_stage_blobs(None, None, None, 0, None) == 0
+    assert L.moe_stage_blobs(src, dst, by, -1, None) == -3
+    assert L.moe_stage_blobs(None, dst, by, 2, None) == -1
+    assert L.moe_stage_blobs(src, dst, (ctypes.c_int64 * 2)(64, 0), 2, None) == -3
+    assert L.moe_stage_blobs(src, (ctypes.c_void_p * 2)(32, 40), by, 2, None) == -6
+    assert L.moe_stage_blobs((ctypes.c_void_p * 2)(d, None), dst, by, 2, None) == -1
