@@ -31,8 +31,8 @@
 //  * The activations are staged as q8_1 by every CTA (one lane quad per block).
 //  * Down chunks: the producer copies the chunk's weight tiles into free slots first, then polls
 //    (bounded) the flagged copies of the group's q8_1 h rows until every pair carries the call's
-//    flag, staging them into one of two buffers as they arrive (4-entry batches; a buffer is
-//    refilled once every tile that read it has been released), then publishes the tiles. The
+//    flag, staging them into one of up to six buffers as they arrive (2-entry batches; a buffer
+//    is refilled once every tile that read it has been released), then publishes the tiles. The
 //    wait and the staging are one L2 round trip, and the writers issue no fence. A down tile
 //    holds up to nsub 32-row sub-tiles; its (sub-tile, 256-weight chunk) work items are dealt to
 //    the consumer warps in turn across tiles, and the last warp of a sub-tile sums its chunks
