@@ -634,7 +634,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1) layer_kernel(const LayerArgs L
     const int S = A.stages, RT = A.RT, half = RT >> 1, RTD = D.RT;
     const SmallDiv divS(S);
     const int tpg = (D.rows + RTD - 1) / RTD;
-    int dchunk = (G * tpg) / (2 * static_cast<int>(gridDim.x));  // about two down items per CTA
+    int dchunk = (2 * G * tpg) / (5 * static_cast<int>(gridDim.x));  // about 2.5 down items per CTA
     dchunk = dchunk < 1 ? 1 : dchunk > 3 ? 3 : dchunk;
     const int nunits = G * upg, cpg = (tpg + dchunk - 1) / dchunk;
     const int nitems = nunits + G * cpg;
